@@ -1,0 +1,397 @@
+"""Pins for the CPU oracle: checks against what the pages and the mathematics fix.
+
+None of these re-types an oracle formula and compares it with itself; each one
+compares the oracle with a printed value, a closed form, a library routine, an
+invariant, or brute force on a tiny domain.
+"""
+import math
+
+import numpy as np
+import pytest
+import scipy.linalg
+
+import workloads
+from conftest import read_golden
+
+GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def unpack_codes(codes: np.ndarray, C: int) -> np.ndarray:
+    lo = codes & 15
+    hi = codes >> 4
+    out = np.empty((codes.shape[0], codes.shape[1] * 2), np.uint8)
+    out[:, 0::2] = lo
+    out[:, 1::2] = hi
+    return out[:, :C]
+
+
+# ------------------------------------------------------------------ E2M1
+
+
+def test_e2m1_all_codes_round_trip(orc):
+    for c in range(16):
+        v = orc.e2m1_decode([c])[0]
+        assert abs(v) == GRID[c & 7]
+        assert math.copysign(1.0, v) == (-1.0 if c & 8 else 1.0)
+        assert orc.e2m1_rne([v])[0] == c
+
+
+def test_e2m1_rne_golden_cases(orc):
+    rows = read_golden("e2m1_rne_cases.txt")
+    x = np.array([float(r[0]) for r in rows], np.float32)
+    want = np.array([int(r[1], 16) for r in rows], np.uint8)
+    got = orc.e2m1_rne(x)
+    bad = [(rows[i][0], hex(got[i]), rows[i][1]) for i in np.nonzero(got != want)[0]]
+    assert not bad, bad
+
+
+def test_e2m1_rne_is_nearest_brute_force(orc):
+    rng = np.random.default_rng(5)
+    q = np.concatenate([rng.uniform(-7, 7, 200000), rng.uniform(-0.3, 0.3, 20000)]).astype(np.float32)
+    codes = orc.e2m1_rne(q)
+    g = GRID[codes & 7]
+    a = np.abs(q.astype(np.float64))
+    d_best = np.min(np.abs(np.minimum(a, 6.0)[:, None] - GRID[None, :]), axis=1)
+    assert np.all(np.abs(np.minimum(a, 6.0) - g) == d_best)
+    nz = q != 0
+    assert np.all(((codes[nz] & 8) != 0) == (q[nz] < 0))
+
+
+# ------------------------------------------------------------------ E4M3
+
+
+def test_e4m3_golden_values(orc):
+    for code_hex, val in read_golden("e4m3_values.txt"):
+        v = orc.e4m3_decode([int(code_hex, 16)])[0]
+        if val == "nan":
+            assert math.isnan(v)
+        else:
+            assert v == float(val) and math.copysign(1, v) == math.copysign(1, float(val))
+
+
+def test_e4m3_all_256_codes_round_trip(orc):
+    vals = orc.e4m3_decode(np.arange(256))
+    for b in range(256):
+        if b in (0x7F, 0xFF):
+            assert math.isnan(vals[b])
+            continue
+        assert math.isfinite(vals[b])
+        assert orc.e4m3_rne_satfinite([vals[b]])[0] == b
+    pos = vals[:0x7F]
+    assert np.all(np.diff(pos) > 0), "non-negative codes must increase with the value"
+    assert pos.max() == 448.0
+
+
+def test_e4m3_rne_brute_force(orc):
+    finite = orc.e4m3_decode(np.arange(0x7F)).astype(np.float64)  # 0 .. 448, codes 0..0x7E
+    mids = (finite[:-1] + finite[1:]) / 2
+    rng = np.random.default_rng(11)
+    xs = np.concatenate([
+        mids, np.nextafter(mids, 0), np.nextafter(mids, 1000), finite,
+        np.exp(rng.uniform(np.log(1e-4), np.log(600.0), 200000)),
+        [0.0, 448.0, 448.5, 463.9, 464.0, 480.0, 1e30, np.inf],
+    ]).astype(np.float32)
+    got = orc.e4m3_rne_satfinite(xs)
+    x = xs.astype(np.float64)
+    for i in range(x.size):
+        if x[i] > 448.0:
+            want = 0x7E
+        else:
+            d = np.abs(finite - x[i])
+            best = np.nonzero(d == d.min())[0]
+            want = best[0] if best.size == 1 else [b for b in best if b % 2 == 0][0]
+        assert got[i] == want, (xs[i], hex(got[i]), hex(want))
+
+
+# ------------------------------------------------------------------ Philox
+
+
+def test_philox_known_answers(orc):
+    for row in read_golden("philox4x32_10_kat.txt"):
+        w = [int(v, 16) for v in row]
+        out = orc.philox4x32_10(w[0:4], w[4:6])
+        assert [int(v) for v in out] == w[6:10]
+
+
+def test_sr_word_stream_layout(orc):
+    seed = 0x1234_5678_9ABC_DEF0
+    idx = np.array([0, 1, 2, 3, 4, 7, 1 << 33, (1 << 33) + 2, 12345678901], np.uint64)
+    words = orc.sr_words(seed, idx)
+    for i, w in zip(idx.tolist(), words.tolist()):
+        blk = i >> 2
+        out = orc.philox4x32_10([blk & 0xFFFFFFFF, blk >> 32, 0, 0], [seed & 0xFFFFFFFF, seed >> 32])
+        assert w == int(out[i & 3])
+
+
+# ------------------------------------------------------------------ RHT
+
+
+def test_rht_matches_sylvester_hadamard(orc):
+    H = scipy.linalg.hadamard(16).astype(np.float64)
+    cols = orc.rht16(np.eye(16, dtype=np.float32), 0)  # row k = transform of e_k
+    assert np.array_equal(cols.T.astype(np.float64) * 4.0, H)
+    assert np.array_equal(H @ H.T, 16 * np.eye(16))
+
+
+def test_rht_signs_and_orthogonality(orc):
+    rng = np.random.default_rng(3)
+    H = scipy.linalg.hadamard(16).astype(np.float64)
+    for seed in (0, 1, 99, 2**40 + 5):
+        mask = orc.rht_sign_mask(seed)
+        sigma = np.array([-1.0 if (mask >> j) & 1 else 1.0 for j in range(16)])
+        v = rng.standard_normal((64, 16)).astype(np.float32)
+        y = orc.rht16(v, mask).astype(np.float64)
+        ref = 0.25 * (v.astype(np.float64) * sigma) @ H.T
+        assert np.allclose(y, ref, rtol=0, atol=1e-6 * np.abs(v).max())
+        assert np.allclose(np.linalg.norm(y, axis=1), np.linalg.norm(v.astype(np.float64), axis=1), rtol=1e-6)
+    assert len({orc.rht_sign_mask(s) for s in range(32)}) > 24
+
+
+def test_rht_involution_without_signs(orc):
+    v = np.random.default_rng(4).standard_normal((32, 16)).astype(np.float32)
+    back = orc.rht16(orc.rht16(v, 0), 0)  # (H/4)(H/4) = H H^T / 16 = I
+    assert np.allclose(back, v, rtol=0, atol=4e-7 * np.abs(v).max())
+
+
+# ------------------------------------------------------------------ SR
+
+
+@pytest.mark.parametrize("q", [0.3, 0.8, 1.2, 1.9, 2.7, 3.01, 4.9, 5.999, -3.3, -0.1])
+def test_sr_unbiased_and_between_neighbours(orc, q):
+    n = 1 << 16
+    words = orc.sr_words(77, np.arange(n, dtype=np.uint64))
+    codes = orc.e2m1_sr(np.full(n, q, np.float32), words)
+    vals = orc.e2m1_decode(codes[:4096])  # decode via the oracle on a subset
+    a = abs(q)
+    lo = GRID[GRID <= a].max()
+    hi = GRID[GRID > a].min()
+    mags = GRID[codes & 7]
+    assert set(np.unique(mags)).issubset({lo, hi})
+    assert np.all(np.abs(vals) == mags[:4096])
+    p = (a - lo) / (hi - lo)
+    mean = mags.mean()
+    sigma = (hi - lo) * math.sqrt(p * (1 - p) / n)
+    assert abs(mean - a) <= 3 * sigma + 1e-12
+
+
+def test_sr_seed_behaviour(orc):
+    x = workloads.gradients(32, 64, seed=4)
+    a = orc.quantize(x, rounding=orc.ROUND_SR, sr_seed=1)
+    b = orc.quantize(x, rounding=orc.ROUND_SR, sr_seed=1)
+    c = orc.quantize(x, rounding=orc.ROUND_SR, sr_seed=2)
+    assert np.array_equal(a.codes, b.codes) and np.array_equal(a.sf, b.sf)
+    assert not np.array_equal(a.codes, c.codes)
+
+
+# ------------------------------------------------------------- quantizer
+
+
+def _mixed_matrix(rows=64, cols=256, seed=21):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((rows, cols)).astype(np.float32)
+    x[: rows // 4] = rng.standard_t(3, (rows // 4, cols)) * 0.05
+    x[rows // 4: rows // 2] = rng.uniform(-1, 1, (rows // 4, cols))
+    x[rows // 2:, ::37] *= 30.0
+    x[3, 16:32] = 0.0  # one all-zero block
+    x[5, 32:48] = 0.0
+    x[5, 40] = 7.0  # one single-outlier block
+    return workloads.bf16_bits(x)
+
+
+def _true_block_sse(y64, sf_bytes_rm, s_t, orc):
+    """FP64 SSE of each block for the given scale bytes, nearest-grid brute force."""
+    R, C = y64.shape
+    eff = orc.e4m3_decode(sf_bytes_rm).astype(np.float64) * s_t  # [R, nb]
+    e = np.repeat(eff, 16, axis=1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        a = np.where(e > 0, np.abs(y64) / e, 0.0)
+    a = np.minimum(a, 6.0)
+    g = GRID[np.argmin(np.abs(a[..., None] - GRID), axis=-1)]
+    xhat = np.sign(y64) * g * e
+    return ((y64 - xhat) ** 2).reshape(R, C // 16, 16).sum(-1)
+
+
+def test_choice_matches_brute_force(orc):
+    x = _mixed_matrix()
+    R, C = x.shape
+    nb = C // 16
+    y64 = workloads.bf16_to_f32(x).astype(np.float64)
+    q46 = orc.quantize(x, sf_layout=orc.SF_ROWMAJOR)
+    q6 = orc.quantize(x, scale_rule=orc.SCALE_6, sf_layout=orc.SF_ROWMAJOR)
+    q4 = orc.quantize(x, scale_rule=orc.SCALE_4, sf_layout=orc.SF_ROWMAJOR)
+    s_t = q46.tensor_scale
+    assert s_t == np.float32(np.abs(y64).max() / 2688.0)
+    E6 = _true_block_sse(y64, q6.sf.reshape(R, nb), s_t, orc)
+    E4 = _true_block_sse(y64, q4.sf.reshape(R, nb), s_t, orc)
+    chose4 = ((q46.choice[:, :, None] >> np.arange(32, dtype=np.uint32)) & 1).reshape(R, -1)[:, :nb].astype(bool)
+    brute4 = E4 < E6
+    same = q4.sf.reshape(R, nb) == q6.sf.reshape(R, nb)  # identical candidates: a tie, 6 wins
+    assert not np.any(chose4 & same)
+    near = (np.abs(E4 - E6) <= 1e-3 * np.maximum(E4, E6)) & ~same
+    ok = ~near & ~same
+    assert np.all(chose4[ok] == brute4[ok])
+    assert near.mean() < 0.01
+    assert 0.05 < chose4.mean() < 0.95  # both candidates are exercised
+    # the 4/6 output uses the chosen candidate's scale byte
+    sf46 = q46.sf.reshape(R, nb)
+    assert np.array_equal(sf46, np.where(chose4, q4.sf.reshape(R, nb), q6.sf.reshape(R, nb)))
+    # scale candidates agree with E4M3(a_b / (M s_t)) computed in FP64
+    ab = np.abs(y64).reshape(R, nb, 16).max(-1)
+    for M, q in ((6, q6), (4, q4)):
+        want = orc.e4m3_rne_satfinite((ab / (M * np.float64(s_t))).astype(np.float32))
+        got = q.sf.reshape(R, nb)
+        assert (want == got).mean() > 0.99
+        assert np.all(np.abs(want.astype(int) - got.astype(int)) <= 1)
+
+
+def test_four_over_six_never_worse_than_six(orc):
+    x = _mixed_matrix(seed=22)
+    R, C = x.shape
+    y64 = workloads.bf16_to_f32(x).astype(np.float64)
+    d46 = orc.dequantize(orc.quantize(x)).astype(np.float64)
+    d6 = orc.dequantize(orc.quantize(x, scale_rule=orc.SCALE_6)).astype(np.float64)
+    s46 = ((d46 - y64) ** 2).reshape(R, -1, 16).sum(-1)
+    s6 = ((d6 - y64) ** 2).reshape(R, -1, 16).sum(-1)
+    assert np.all(s46 <= s6 * (1 + 1e-3) + 1e-30)
+    assert s46.sum() < s6.sum()
+
+
+def test_dequantized_values_lie_on_grid_times_scale(orc):
+    x = _mixed_matrix(seed=23)
+    for kw in ({}, {"rounding": 1, "sr_seed": 9}, {"block_2d": True}, {"hadamard": True, "hadamard_seed": 3}):
+        q = orc.quantize(x, sf_layout=orc.SF_ROWMAJOR, **kw)
+        d = orc.dequantize(q).astype(np.float64)
+        eff = np.repeat(orc.e4m3_decode(q.sf.reshape(q.rows, -1)).astype(np.float64) * q.tensor_scale, 16, 1)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            ratio = np.where(eff > 0, np.abs(d) / eff, 0.0)
+        on = np.min(np.abs(ratio[..., None] - GRID), axis=-1) <= 1e-6 * np.maximum(ratio, 1)
+        assert on.all(), kw
+
+
+def test_hand_built_block_prefers_four_and_ties_go_to_six(orc):
+    x = np.zeros((1, 64), np.float32)
+    x[0, 0] = 2688.0  # tensor amax -> s_t = 1
+    x[0, 16:20] = [64.0, 48.0, 32.0, 16.0]  # = 16 * [4, 3, 2, 1]: exact with sf_4 = 16
+    x[0, 32:48] = 0.0  # all-zero block: both scales 0, equal error -> 6
+    x[0, 48] = 2688.0  # block max = amax: the 4-candidate saturates to 448 like the 6-candidate
+    q = orc.quantize(workloads.bf16_bits(x), sf_layout=orc.SF_ROWMAJOR)
+    assert q.tensor_scale == 1.0
+    bits = int(q.choice[0, 0])
+    assert bits & 2, "block 1 is exact under the 4-scale and must keep 4"
+    assert not bits & 4 and not bits & 8 and not bits & 1
+    assert q.sf[1] == orc.e4m3_rne_satfinite([16.0])[0]
+    assert q.sf[2] == 0 and q.sf[3] == 0x7E and q.sf[0] == 0x7E
+    d = orc.dequantize(q)
+    assert np.array_equal(d[0, 16:20], x[0, 16:20])
+
+
+def test_all_zero_tensor(orc):
+    q = orc.quantize(np.zeros((16, 64), np.uint16))
+    assert q.tensor_scale == 0.0
+    assert not q.sf.any() and not q.codes.any() and not q.choice.any()
+
+
+def test_supplied_amax_is_used(orc):
+    x = _mixed_matrix(seed=24)
+    q = orc.quantize(x, amax=1000.0)
+    assert q.tensor_scale == np.float32(np.float32(1000.0) / np.float32(2688.0))
+    assert not np.array_equal(q.sf, orc.quantize(x).sf)
+
+
+def test_transposed_equals_quantizing_the_materialized_transpose(orc):
+    x = _mixed_matrix(rows=48, cols=80, seed=25)
+    xt = np.ascontiguousarray(x.T)
+    for kw in ({}, {"hadamard": True, "hadamard_seed": 12}, {"scale_rule": orc.SCALE_6}):
+        a = orc.quantize(x, transpose=True, **kw)
+        b = orc.quantize(xt, **kw)
+        assert a.rows == 80 and a.cols == 48
+        assert np.array_equal(a.codes, b.codes) and np.array_equal(a.sf, b.sf)
+        assert a.tensor_scale == b.tensor_scale and np.array_equal(a.choice, b.choice)
+
+
+@pytest.mark.parametrize("rounding", [0, 1])
+def test_2d_transposed_is_the_transpose(orc, rounding):
+    x = _mixed_matrix(rows=48, cols=96, seed=26)
+    a = orc.quantize(x, block_2d=True, rounding=rounding, sr_seed=5, sf_layout=orc.SF_ROWMAJOR)
+    b = orc.quantize(x, block_2d=True, transpose=True, rounding=rounding, sr_seed=5, sf_layout=orc.SF_ROWMAJOR)
+    ca = unpack_codes(a.codes, 96)
+    cb = unpack_codes(b.codes, 48)
+    assert np.array_equal(ca.T, cb)
+    sa = a.sf.reshape(48, 6)
+    sb = b.sf.reshape(96, 3)
+    for i in range(3):
+        for j in range(6):
+            assert np.all(sa[16 * i: 16 * i + 16, j] == sa[16 * i, j])
+            assert sb[16 * j, i] == sa[16 * i, j]
+
+
+def test_2d_tile_uses_one_scale_and_beats_six_only(orc):
+    x = _mixed_matrix(rows=64, cols=128, seed=27)
+    y64 = workloads.bf16_to_f32(x).astype(np.float64)
+    q = orc.quantize(x, block_2d=True, sf_layout=orc.SF_ROWMAJOR)
+    q6 = orc.quantize(x, block_2d=True, scale_rule=orc.SCALE_6, sf_layout=orc.SF_ROWMAJOR)
+    s = q.sf.reshape(64, 8)
+    assert np.array_equal(s, np.repeat(s[::16], 16, axis=0))
+    t = lambda d: ((d - y64) ** 2).reshape(4, 16, 8, 16).sum((1, 3))  # noqa: E731
+    assert np.all(t(orc.dequantize(q)) <= t(orc.dequantize(q6)) * (1 + 1e-3) + 1e-30)
+
+
+def test_sf_swizzle_offsets_by_hand(orc):
+    # 128 rows x 4 scale columns per 512-byte tile; 32-row groups interleave at 4-byte
+    # steps inside 16-byte rows; tiles row-major over (row tile, column tile).
+    cases = [((0, 0, 8), 0), ((1, 0, 8), 16), ((31, 0, 8), 496), ((32, 0, 8), 4), ((33, 0, 8), 20),
+             ((64, 0, 8), 8), ((96, 0, 8), 12), ((127, 3, 8), 511), ((0, 4, 8), 512),
+             ((128, 0, 8), 1024), ((130, 5, 8), 1569), ((0, 1, 1), 1), ((129, 0, 1), 528)]
+    for (r, c, nb), off in cases:
+        assert orc.sf_offset(r, c, nb) == off, (r, c, nb)
+    assert orc.sf_bytes(130, 9) == 256 * 12
+    x = _mixed_matrix(rows=130 - 2, cols=144, seed=28)
+    a = orc.quantize(x)
+    b = orc.quantize(x, sf_layout=orc.SF_ROWMAJOR)
+    assert np.array_equal(orc.sf_to_rowmajor(a.sf, a.rows, 9), b.sf.reshape(a.rows, 9))
+    mask = np.ones(a.sf.size, bool)
+    mask[[orc.sf_offset(r, c, 9) for r in range(a.rows) for c in range(9)]] = False
+    assert not a.sf[mask].any(), "pad bytes must be zero"
+
+
+def test_gemm_reference_closed_form(orc):
+    K, M, N = 64, 3, 5
+    A = np.full((M, K), 1.5, np.float32)
+    W = np.tile(np.arange(1, N + 1, dtype=np.float32)[:, None], (1, K))
+    W[:, ::2] *= -1
+    out, bnd = orc.gemm_rows(A, W, [0, 2])
+    assert np.array_equal(out, np.zeros((2, N)))
+    assert np.array_equal(bnd, np.tile(1.5 * K * np.arange(1, N + 1), (2, 1)))
+    rng = np.random.default_rng(1)
+    A = rng.standard_normal((7, 96)).astype(np.float32)
+    W = rng.standard_normal((11, 96)).astype(np.float32)
+    out, _ = orc.gemm_rows(A, W, [1, 6])
+    assert np.allclose(out, (A.astype(np.float64) @ W.T.astype(np.float64))[[1, 6]], rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------- the page's worked example
+
+
+def test_page5_block_size_mae_reproduced(orc):
+    torch = pytest.importorskip("torch")
+    torch.manual_seed(0)
+    x = torch.randn(4096)
+    x[::512] *= 20
+    for block, mae in read_golden("page5_mae.txt"):
+        assert f"{orc.mae_nearest_grid(x.numpy(), int(block)):.4f}" == mae
+
+
+def test_page5_mae_falls_as_blocks_shrink_on_own_generator(orc):
+    x = workloads.normal(1, 4096, seed=31).reshape(-1)
+    x[::512] *= 20
+    m = [orc.mae_nearest_grid(x, b) for b in (4096, 32, 16)]
+    assert m[0] > m[1] > m[2]
+
+
+def test_outlier_matrix_four_over_six_lowers_error(orc):
+    x = workloads.outlier_matrix()
+    y = workloads.bf16_to_f32(x).astype(np.float64)
+    d46 = orc.dequantize(orc.quantize(x)).astype(np.float64)
+    d6 = orc.dequantize(orc.quantize(x, scale_rule=orc.SCALE_6)).astype(np.float64)
+    assert np.abs(d46 - y).mean() < np.abs(d6 - y).mean()
+    assert ((d46 - y) ** 2).sum() < ((d6 - y) ** 2).sum()
