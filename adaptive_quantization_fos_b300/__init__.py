@@ -1,0 +1,279 @@
+"""Python binding of libfos.so -- Four Over Six NVFP4 quantization on B300.
+
+The C ABI (include/fos.h) is called through ctypes with raw device pointers
+taken from torch tensors; torch provides device memory and streams only.
+Every step of the computation runs in the library's CUDA kernels.  There is
+no CPU fallback: importing this package fails loudly when libfos.so is
+missing, and every call raises on a non-OK status.
+
+Low-level names mirror the C functions (``fos_quantize``, ``fos_dequantize``,
+``fos_gemm``, ...).  ``quantize`` / ``dequantize`` / ``gemm`` are thin
+conveniences that allocate the output tensors with torch and call them.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfos.so")
+
+FOS_OK, FOS_ERR_INVALID_ARG, FOS_ERR_UNSUPPORTED, FOS_ERR_CUDA, FOS_ERR_TIMEOUT = 0, 1, 2, 3, 4
+FOS_SCALE_4OVER6, FOS_SCALE_6, FOS_SCALE_4 = 0, 1, 2
+FOS_ROUND_RNE, FOS_ROUND_STOCHASTIC = 0, 1
+FOS_SF_SWIZZLED_128x4, FOS_SF_ROWMAJOR = 0, 1
+FOS_DTYPE_F32, FOS_DTYPE_BF16 = 0, 1
+
+
+class FosError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_lib.fos_status_string(status).decode()} (status {status})")
+
+
+class fos_quant_options(ctypes.Structure):
+    _fields_ = [
+        ("struct_size", ctypes.c_uint32),
+        ("scale_rule", ctypes.c_int32),
+        ("rounding", ctypes.c_int32),
+        ("block_2d", ctypes.c_int32),
+        ("transpose", ctypes.c_int32),
+        ("hadamard", ctypes.c_int32),
+        ("sf_layout", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("sr_seed", ctypes.c_uint64),
+        ("hadamard_seed", ctypes.c_uint64),
+        ("tensor_amax", ctypes.c_void_p),
+    ]
+
+
+class fos_nvfp4_tensor(ctypes.Structure):
+    _fields_ = [
+        ("codes", ctypes.c_void_p),
+        ("sf", ctypes.c_void_p),
+        ("tensor_scale", ctypes.c_void_p),
+        ("rows", ctypes.c_int64),
+        ("cols", ctypes.c_int64),
+        ("ld_codes", ctypes.c_int64),
+        ("sf_layout", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python -m adaptive_quantization_fos_b300.build` "
+            "(there is no CPU fallback)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i64, u64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_int32, ctypes.c_size_t
+    sig = {
+        "fos_abi_version": (i32, []),
+        "fos_status_string": (ctypes.c_char_p, [i32]),
+        "fos_sf_bytes": (i32, [i64, i64, i32, ctypes.POINTER(sz)]),
+        "fos_quantize_workspace_size": (i32, [i64, i64, ctypes.POINTER(fos_quant_options), ctypes.POINTER(sz)]),
+        "fos_tensor_amax": (i32, [vp, i64, i64, i64, i32, i32, u64, vp, vp, sz, vp]),
+        "fos_quantize": (i32, [vp, i64, i64, i64, ctypes.POINTER(fos_quant_options), vp, i64, vp, vp, vp, vp, sz,
+                               vp]),
+        "fos_dequantize": (i32, [ctypes.POINTER(fos_nvfp4_tensor), vp, i32, i64, vp]),
+        "fos_gemm": (i32, [ctypes.POINTER(fos_nvfp4_tensor), ctypes.POINTER(fos_nvfp4_tensor), vp, i64, vp, vp]),
+        "fos_e2m1_encode": (i32, [vp, i64, vp, vp]),
+        "fos_e4m3_encode": (i32, [vp, i64, vp, vp]),
+        "fos_philox4x32_10": (i32, [vp, i64, u64, vp, vp]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    return L
+
+
+_lib = _load()
+EXPORTED = ("fos_abi_version", "fos_status_string", "fos_sf_bytes", "fos_quantize_workspace_size",
+            "fos_tensor_amax", "fos_quantize", "fos_dequantize", "fos_gemm", "fos_e2m1_encode",
+            "fos_e4m3_encode", "fos_philox4x32_10")
+
+
+def _check(status: int, what: str) -> None:
+    if status != FOS_OK:
+        raise FosError(status, what)
+
+
+# ------------------------------------------------------- C-named wrappers
+
+
+def fos_abi_version() -> int:
+    return int(_lib.fos_abi_version())
+
+
+def fos_sf_bytes(out_rows: int, out_cols: int, sf_layout: int = FOS_SF_SWIZZLED_128x4) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.fos_sf_bytes(out_rows, out_cols, sf_layout, ctypes.byref(n)), "fos_sf_bytes")
+    return n.value
+
+
+def fos_quantize_workspace_size(rows: int, cols: int, opt: fos_quant_options) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.fos_quantize_workspace_size(rows, cols, ctypes.byref(opt), ctypes.byref(n)),
+           "fos_quantize_workspace_size")
+    return n.value
+
+
+def fos_quantize(x, rows, cols, ld_x, opt, codes, ld_codes, sf, tensor_scale, choice, workspace, workspace_bytes,
+                 stream) -> int:
+    """Raw call: all buffer arguments are integer device addresses (0 = NULL)."""
+    return int(_lib.fos_quantize(x, rows, cols, ld_x, ctypes.byref(opt), codes, ld_codes, sf, tensor_scale,
+                                 choice or None, workspace or None, workspace_bytes, stream))
+
+
+def fos_tensor_amax(x, rows, cols, ld_x, hadamard, transpose, hadamard_seed, amax_out, workspace,
+                    workspace_bytes, stream) -> int:
+    return int(_lib.fos_tensor_amax(x, rows, cols, ld_x, hadamard, transpose, hadamard_seed, amax_out, workspace,
+                                    workspace_bytes, stream))
+
+
+def fos_dequantize(q: fos_nvfp4_tensor, out, out_dtype, ld_out, stream) -> int:
+    return int(_lib.fos_dequantize(ctypes.byref(q), out, out_dtype, ld_out, stream))
+
+
+def fos_gemm(A: fos_nvfp4_tensor, B: fos_nvfp4_tensor, C, ldc, dev_status, stream) -> int:
+    return int(_lib.fos_gemm(ctypes.byref(A), ctypes.byref(B), C, ldc, dev_status or None, stream))
+
+
+def fos_e2m1_encode(x, n, codes, stream) -> int:
+    return int(_lib.fos_e2m1_encode(x, n, codes, stream))
+
+
+def fos_e4m3_encode(x, n, out, stream) -> int:
+    return int(_lib.fos_e4m3_encode(x, n, out, stream))
+
+
+def fos_philox4x32_10(counters, n, key, out, stream) -> int:
+    return int(_lib.fos_philox4x32_10(counters, n, key, out, stream))
+
+
+# -------------------------------------------------------- torch helpers
+
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _stream_ptr(stream=None) -> int:
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def options(*, scale_rule=FOS_SCALE_4OVER6, rounding=FOS_ROUND_RNE, block_2d=False, transpose=False,
+            hadamard=False, sf_layout=FOS_SF_SWIZZLED_128x4, sr_seed=0, hadamard_seed=0,
+            tensor_amax=None) -> fos_quant_options:
+    o = fos_quant_options()
+    o.struct_size = ctypes.sizeof(fos_quant_options)
+    o.scale_rule = scale_rule
+    o.rounding = rounding
+    o.block_2d = int(bool(block_2d))
+    o.transpose = int(bool(transpose))
+    o.hadamard = int(bool(hadamard))
+    o.sf_layout = sf_layout
+    o.reserved = 0
+    o.sr_seed = sr_seed
+    o.hadamard_seed = hadamard_seed
+    o.tensor_amax = None if tensor_amax is None else int(tensor_amax.data_ptr())
+    return o
+
+
+@dataclass
+class NVFP4Tensor:
+    """Device buffers of one quantized matrix (rows x cols values, blocks along cols)."""
+
+    codes: "object"  # uint8 [rows, ld_codes]
+    sf: "object"  # uint8 flat, fos_sf_bytes(rows, cols, sf_layout)
+    tensor_scale: "object"  # float32 [1]
+    rows: int
+    cols: int
+    sf_layout: int
+    choice: "object" = None  # uint8 [rows, cols/16] or None
+
+    def as_c(self) -> fos_nvfp4_tensor:
+        t = fos_nvfp4_tensor()
+        t.codes = self.codes.data_ptr()
+        t.sf = self.sf.data_ptr()
+        t.tensor_scale = self.tensor_scale.data_ptr()
+        t.rows = self.rows
+        t.cols = self.cols
+        t.ld_codes = self.codes.stride(0) if self.codes.dim() == 2 else self.cols // 2
+        t.sf_layout = self.sf_layout
+        return t
+
+
+class Quantizer:
+    """Reusable output/workspace buffers for repeated quantization of one shape."""
+
+    def __init__(self, rows: int, cols: int, *, device="cuda", with_choice=False, **opts):
+        torch = _torch()
+        self.rows, self.cols = rows, cols
+        self.opt_kwargs = dict(opts)
+        self.opt = options(**opts)
+        tr = bool(opts.get("transpose", False))
+        self.R, self.C = (cols, rows) if tr else (rows, cols)
+        layout = opts.get("sf_layout", FOS_SF_SWIZZLED_128x4)
+        ldc = max(8, ((self.C // 2 + 15) // 16) * 16)
+        self.out = NVFP4Tensor(
+            codes=torch.empty((self.R, ldc), dtype=torch.uint8, device=device),
+            sf=torch.empty(max(1, fos_sf_bytes(self.R, self.C, layout)), dtype=torch.uint8, device=device),
+            tensor_scale=torch.empty(1, dtype=torch.float32, device=device),
+            rows=self.R, cols=self.C, sf_layout=layout,
+            choice=torch.empty((self.R, self.C // 16), dtype=torch.uint8, device=device) if with_choice else None)
+        self.ws_bytes = fos_quantize_workspace_size(rows, cols, self.opt)
+        self.workspace = torch.empty(max(1, self.ws_bytes), dtype=torch.uint8, device=device)
+
+    def __call__(self, x, stream=None) -> NVFP4Tensor:
+        assert x.dtype == _torch().bfloat16 and x.dim() == 2 and x.shape == (self.rows, self.cols)
+        assert x.stride(1) == 1
+        o = self.out
+        st = fos_quantize(x.data_ptr(), self.rows, self.cols, x.stride(0), self.opt, o.codes.data_ptr(),
+                          o.codes.stride(0), o.sf.data_ptr(), o.tensor_scale.data_ptr(),
+                          o.choice.data_ptr() if o.choice is not None else 0, self.workspace.data_ptr(),
+                          self.ws_bytes, _stream_ptr(stream))
+        _check(st, "fos_quantize")
+        return o
+
+
+def quantize(x, *, with_choice=False, stream=None, **opts) -> NVFP4Tensor:
+    """Quantize a bf16 [rows, cols] CUDA tensor (contiguous rows) to NVFP4."""
+    q = Quantizer(x.shape[0], x.shape[1], device=x.device, with_choice=with_choice, **opts)
+    return q(x, stream=stream)
+
+
+def tensor_amax(x, *, hadamard=False, transpose=False, hadamard_seed=0, stream=None):
+    torch = _torch()
+    out = torch.empty(1, dtype=torch.float32, device=x.device)
+    ws = torch.empty(fos_quantize_workspace_size(x.shape[0], x.shape[1], options()), dtype=torch.uint8,
+                     device=x.device)
+    _check(fos_tensor_amax(x.data_ptr(), x.shape[0], x.shape[1], x.stride(0), int(hadamard), int(transpose),
+                           hadamard_seed, out.data_ptr(), ws.data_ptr(), ws.numel(), _stream_ptr(stream)),
+           "fos_tensor_amax")
+    return out
+
+
+def dequantize(q: NVFP4Tensor, dtype=None, stream=None):
+    torch = _torch()
+    dtype = torch.float32 if dtype is None else dtype
+    out = torch.empty((q.rows, q.cols), dtype=dtype, device=q.codes.device)
+    code = FOS_DTYPE_BF16 if dtype == torch.bfloat16 else FOS_DTYPE_F32
+    _check(fos_dequantize(q.as_c(), out.data_ptr(), code, q.cols, _stream_ptr(stream)), "fos_dequantize")
+    return out
+
+
+def gemm(A: NVFP4Tensor, B: NVFP4Tensor, out=None, status=None, stream=None):
+    """C = A . B^T (bf16) from two NVFP4 operands quantized along K."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty((A.rows, B.rows), dtype=torch.bfloat16, device=A.codes.device)
+    _check(fos_gemm(A.as_c(), B.as_c(), out.data_ptr(), out.stride(0),
+                    status.data_ptr() if status is not None else 0, _stream_ptr(stream)), "fos_gemm")
+    return out

@@ -1,0 +1,224 @@
+// C ABI of the Four Over Six NVFP4 library: argument validation and launches.
+// No function here allocates device memory or synchronizes the stream.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "fos.h"
+#include "fos_internal.h"
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+fos_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FOS_OK : FOS_ERR_CUDA; }
+
+bool valid_options(const fos_quant_options* o) {
+  if (!o || o->struct_size < sizeof(fos_quant_options)) return false;
+  if (o->scale_rule < FOS_SCALE_4OVER6 || o->scale_rule > FOS_SCALE_4) return false;
+  if (o->rounding != FOS_ROUND_RNE && o->rounding != FOS_ROUND_STOCHASTIC) return false;
+  if ((o->block_2d | o->transpose | o->hadamard) & ~1) return false;
+  if (o->sf_layout != FOS_SF_SWIZZLED_128x4 && o->sf_layout != FOS_SF_ROWMAJOR) return false;
+  return o->reserved == 0;
+}
+
+int64_t sf_bytes_of(int64_t R, int64_t nb, int32_t layout) {
+  if (layout == FOS_SF_ROWMAJOR) return R * nb;
+  return ((R + 127) / 128) * 128 * ((nb + 3) / 4) * 4;
+}
+
+// Shared checks of the source matrix.
+bool valid_source(const void* x, int64_t rows, int64_t cols, int64_t ld_x, bool rows16) {
+  if (rows < 0 || cols < 0 || cols % 16 != 0 || ld_x < cols || ld_x % 8 != 0) return false;
+  if ((!x && rows * cols != 0) || !aligned(x, 16)) return false;
+  if (rows16 && rows % 16 != 0) return false;
+  return true;
+}
+
+__global__ void amax_final_kernel(const float* partials, int n, float* out) {
+  __shared__ float s[256];
+  float m = 0.0f;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) m = fmaxf(m, partials[i]);
+  s[threadIdx.x] = m;
+  __syncthreads();
+  for (int o = blockDim.x / 2; o > 0; o >>= 1) {
+    if ((int)threadIdx.x < o) s[threadIdx.x] = fmaxf(s[threadIdx.x], s[threadIdx.x + o]);
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *out = s[0];
+}
+
+int amax_tasks_grid(int64_t rows, int64_t cols, bool cols_kernel) {
+  int64_t tasks = cols_kernel ? (rows / 16) * ((cols + 127) / 128) : rows * ((cols / 16 + 31) / 32);
+  return fos::amax_grid(tasks);
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t fos_abi_version(void) { return FOS_ABI_VERSION; }
+
+const char* fos_status_string(fos_status s) {
+  switch (s) {
+    case FOS_OK: return "ok";
+    case FOS_ERR_INVALID_ARG: return "invalid argument";
+    case FOS_ERR_UNSUPPORTED: return "unsupported";
+    case FOS_ERR_CUDA: return "CUDA launch error";
+    case FOS_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+fos_status fos_sf_bytes(int64_t out_rows, int64_t out_cols, int32_t sf_layout, size_t* bytes) {
+  if (!bytes || out_rows < 0 || out_cols < 0 || out_cols % 16 != 0) return FOS_ERR_INVALID_ARG;
+  if (sf_layout != FOS_SF_SWIZZLED_128x4 && sf_layout != FOS_SF_ROWMAJOR) return FOS_ERR_INVALID_ARG;
+  *bytes = (size_t)sf_bytes_of(out_rows, out_cols / 16, sf_layout);
+  return FOS_OK;
+}
+
+fos_status fos_quantize_workspace_size(int64_t rows, int64_t cols, const fos_quant_options* opt, size_t* bytes) {
+  if (!bytes || rows < 0 || cols < 0 || !valid_options(opt)) return FOS_ERR_INVALID_ARG;
+  *bytes = opt->tensor_amax ? 0 : fos::kQuantWorkspaceBytes;
+  return FOS_OK;
+}
+
+fos_status fos_tensor_amax(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int32_t hadamard,
+                           int32_t transpose, uint64_t hadamard_seed, float* amax_out, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream) {
+  if (!valid_source(x, rows, cols, ld_x, hadamard && transpose) || !amax_out) return FOS_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < fos::kQuantWorkspaceBytes || !aligned(workspace, 4)) return FOS_ERR_INVALID_ARG;
+  const bool cols_kernel = hadamard && transpose;
+  fos::AmaxParams a{};
+  a.x = static_cast<const uint16_t*>(x);
+  a.rows = rows;
+  a.cols = cols;
+  a.ld = ld_x;
+  a.hk0 = (uint32_t)hadamard_seed;
+  a.hk1 = (uint32_t)(hadamard_seed >> 32);
+  a.aligned32 = aligned(x, 32) && ld_x % 16 == 0;
+  a.partials = static_cast<float*>(workspace);
+  const int g = amax_tasks_grid(rows, cols, cols_kernel);
+  cudaError_t e = fos::launch_amax(a, hadamard != 0, transpose != 0, g, stream);
+  if (e != cudaSuccess) return FOS_ERR_CUDA;
+  amax_final_kernel<<<1, 256, 0, stream>>>(a.partials, g, amax_out);
+  return cuda_status(cudaGetLastError());
+}
+
+fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x, const fos_quant_options* opt,
+                        uint8_t* codes, int64_t ld_codes, uint8_t* sf, float* tensor_scale, uint8_t* choice,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!valid_options(opt)) return FOS_ERR_INVALID_ARG;
+  const bool tr = opt->transpose != 0, two_d = opt->block_2d != 0, rht = opt->hadamard != 0;
+  if (!valid_source(x, rows, cols, ld_x, tr || two_d)) return FOS_ERR_INVALID_ARG;
+  const int64_t R = tr ? cols : rows, C = tr ? rows : cols, nb = C / 16;
+  const bool empty = R == 0 || C == 0;
+  if ((!empty && (!codes || !sf)) || !tensor_scale) return FOS_ERR_INVALID_ARG;
+  if (ld_codes < C / 2 || ld_codes % 8 != 0 || !aligned(codes, 8) || !aligned(sf, 4)) return FOS_ERR_INVALID_ARG;
+  if (!opt->tensor_amax &&
+      (!workspace || workspace_bytes < fos::kQuantWorkspaceBytes || !aligned(workspace, 4)))
+    return FOS_ERR_INVALID_ARG;
+
+  const bool aligned32 = aligned(x, 32) && ld_x % 16 == 0;
+  const bool cols_amax = rht && tr;
+  int n_partials = 0;
+  if (!opt->tensor_amax) {
+    fos::AmaxParams a{};
+    a.x = static_cast<const uint16_t*>(x);
+    a.rows = rows;
+    a.cols = cols;
+    a.ld = ld_x;
+    a.hk0 = (uint32_t)opt->hadamard_seed;
+    a.hk1 = (uint32_t)(opt->hadamard_seed >> 32);
+    a.aligned32 = aligned32;
+    a.partials = static_cast<float*>(workspace);
+    n_partials = amax_tasks_grid(rows, cols, cols_amax);
+    if (fos::launch_amax(a, rht, tr, n_partials, stream) != cudaSuccess) return FOS_ERR_CUDA;
+  }
+
+  fos::QuantParams p{};
+  p.x = static_cast<const uint16_t*>(x);
+  p.rows = rows;
+  p.cols = cols;
+  p.ld = ld_x;
+  p.R = R;
+  p.nb = nb;
+  p.codes = codes;
+  p.ld_codes = ld_codes;
+  p.sf = sf;
+  p.sf_layout = opt->sf_layout;
+  p.choice = choice;
+  p.tensor_scale = tensor_scale;
+  p.amax_src = opt->tensor_amax ? opt->tensor_amax : static_cast<const float*>(workspace);
+  p.n_partials = n_partials;
+  p.sr_k0 = (uint32_t)opt->sr_seed;
+  p.sr_k1 = (uint32_t)(opt->sr_seed >> 32);
+  p.hk0 = (uint32_t)opt->hadamard_seed;
+  p.hk1 = (uint32_t)(opt->hadamard_seed >> 32);
+  p.aligned32 = aligned32;
+
+  int kind;
+  int64_t tasks;
+  if (two_d) {
+    kind = tr ? 3 : 2;
+    tasks = (rows / 16) * ((cols / 16 + 1) / 2);
+  } else if (tr) {
+    kind = 1;
+    tasks = (rows / 16) * ((cols + 127) / 128);
+  } else {
+    kind = 0;
+    tasks = R * ((nb + 31) / 32);
+  }
+  const int grid = fos::quant_grid(tasks);
+  if (fos::launch_quant(p, opt->scale_rule, kind, rht, opt->rounding == FOS_ROUND_STOCHASTIC, grid, stream) !=
+      cudaSuccess)
+    return FOS_ERR_CUDA;
+  if (opt->sf_layout == FOS_SF_SWIZZLED_128x4 && (R % 128 != 0 || nb % 4 != 0)) {
+    if (fos::launch_sf_pad(sf, sf_bytes_of(R, nb, opt->sf_layout), R, nb, stream) != cudaSuccess)
+      return FOS_ERR_CUDA;
+  }
+  return FOS_OK;
+}
+
+fos_status fos_dequantize(const fos_nvfp4_tensor* q, void* out, int32_t out_dtype, int64_t ld_out,
+                          cudaStream_t stream) {
+  if (!q || !out || !q->codes || !q->sf || !q->tensor_scale) return FOS_ERR_INVALID_ARG;
+  if (q->rows < 0 || q->cols < 0 || q->cols % 16 != 0 || q->ld_codes < q->cols / 2 || q->ld_codes % 8 != 0)
+    return FOS_ERR_INVALID_ARG;
+  if (q->sf_layout != FOS_SF_SWIZZLED_128x4 && q->sf_layout != FOS_SF_ROWMAJOR) return FOS_ERR_INVALID_ARG;
+  if (out_dtype != FOS_DTYPE_F32 && out_dtype != FOS_DTYPE_BF16) return FOS_ERR_INVALID_ARG;
+  if (ld_out < q->cols || !aligned(out, 16) || !aligned(q->codes, 8)) return FOS_ERR_INVALID_ARG;
+  if ((out_dtype == FOS_DTYPE_F32 && ld_out % 4 != 0) || (out_dtype == FOS_DTYPE_BF16 && ld_out % 8 != 0))
+    return FOS_ERR_INVALID_ARG;
+  fos::DequantParams p{};
+  p.codes = q->codes;
+  p.sf = q->sf;
+  p.tensor_scale = q->tensor_scale;
+  p.rows = q->rows;
+  p.cols = q->cols;
+  p.ld_codes = q->ld_codes;
+  p.ld_out = ld_out;
+  p.sf_layout = q->sf_layout;
+  p.out = out;
+  return cuda_status(fos::launch_dequant(p, out_dtype == FOS_DTYPE_BF16, stream));
+}
+
+fos_status fos_e2m1_encode(const float* x, int64_t n, uint8_t* codes, cudaStream_t stream) {
+  if (n < 0 || (n > 0 && (!x || !codes))) return FOS_ERR_INVALID_ARG;
+  if (n == 0) return FOS_OK;
+  return cuda_status(fos::launch_e2m1_encode(x, n, codes, stream));
+}
+
+fos_status fos_e4m3_encode(const float* x, int64_t n, uint8_t* out, cudaStream_t stream) {
+  if (n < 0 || (n > 0 && (!x || !out))) return FOS_ERR_INVALID_ARG;
+  if (n == 0) return FOS_OK;
+  return cuda_status(fos::launch_e4m3_encode(x, n, out, stream));
+}
+
+fos_status fos_philox4x32_10(const uint32_t* counters, int64_t n, uint64_t key, uint32_t* out, cudaStream_t stream) {
+  if (n < 0 || (n > 0 && (!counters || !out))) return FOS_ERR_INVALID_ARG;
+  if (n == 0) return FOS_OK;
+  return cuda_status(fos::launch_philox(counters, n, key, out, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,61 @@
+// Internal launch interface between the C ABI (fos_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "fos.h"
+
+namespace fos {
+
+// Upper bound on the number of CTAs of the amax pass (= partial maxima the
+// quantize kernels reduce in their prologue).
+constexpr int kMaxAmaxPartials = 2048;
+constexpr size_t kQuantWorkspaceBytes = kMaxAmaxPartials * sizeof(float);
+
+struct AmaxParams {
+  const uint16_t* x;
+  int64_t rows, cols, ld;
+  uint32_t hk0, hk1;  // RHT seed words
+  bool aligned32;
+  float* partials;
+};
+
+struct QuantParams {
+  const uint16_t* x;
+  int64_t rows, cols, ld;  // source matrix
+  int64_t R, nb;           // output rows and scale columns
+  uint8_t* codes;
+  int64_t ld_codes;
+  uint8_t* sf;
+  int32_t sf_layout;
+  uint8_t* choice;
+  float* tensor_scale;
+  const float* amax_src;   // tensor_amax (n_partials == 0) or the amax partials
+  int32_t n_partials;
+  uint32_t sr_k0, sr_k1, hk0, hk1;  // SR and RHT seed words
+  bool aligned32;
+};
+
+struct DequantParams {
+  const uint8_t* codes;
+  const uint8_t* sf;
+  const float* tensor_scale;
+  int64_t rows, cols, ld_codes, ld_out;
+  int32_t sf_layout;
+  void* out;
+};
+
+int amax_grid(int64_t n_warp_tasks);
+int quant_grid(int64_t n_warp_tasks);
+cudaError_t launch_amax(const AmaxParams& p, bool hadamard, bool transpose, int grid, cudaStream_t s);
+// kind: 0 rows (1D), 1 cols (1D transposed), 2 2D, 3 2D transposed
+cudaError_t launch_quant(const QuantParams& p, int rule, int kind, bool rht, bool sr, int grid, cudaStream_t s);
+cudaError_t launch_sf_pad(uint8_t* sf, int64_t bytes, int64_t R, int64_t nb, cudaStream_t s);
+cudaError_t launch_dequant(const DequantParams& p, bool bf16, cudaStream_t s);
+cudaError_t launch_e2m1_encode(const float* x, int64_t n, uint8_t* out, cudaStream_t s);
+cudaError_t launch_e4m3_encode(const float* x, int64_t n, uint8_t* out, cudaStream_t s);
+cudaError_t launch_philox(const uint32_t* ctr, int64_t n, uint64_t key, uint32_t* out, cudaStream_t s);
+
+}  // namespace fos

@@ -1,0 +1,616 @@
+// NVFP4 Four Over Six quantization kernels for sm_103a.
+//
+// Kernels (all HBM-streaming; no tensor cores -- the work is per-element
+// arithmetic, not a contraction):
+//   amax_rows    max|y| of X (RHT along rows optional) -> one partial per CTA
+//   amax_cols    max|y| with the RHT running down columns (transposed input)
+//   quant_rows   1D blocks along rows: one thread owns one 16-value block
+//   quant_cols   1D blocks down columns (transposed output): one thread owns
+//                4 adjacent columns x 16 rows
+//   quant_2d     16x16 tiles: 16 lanes own the 16 source rows of a tile
+//   sf_pad_zero  zero the padding bytes of the swizzled scale layout
+//   dequant      x_hat = g * (sf * s_t)
+// Each quantize kernel reduces the amax partials itself in its prologue, so
+// the amax pass needs no atomics, no memset and no extra finalize launch.
+#include <cuda_runtime.h>
+
+#include <cfloat>
+#include <cstdint>
+
+#include "fos_device.cuh"
+#include "fos_internal.h"
+
+namespace fos {
+
+// ------------------------------------------------------------------ amax
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// CTA-wide max; every thread returns the result.
+__device__ __forceinline__ float block_max(float v, float* s_red) {
+  v = warp_max(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) s_red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    float u = lane < (int)(blockDim.x >> 5) ? s_red[lane] : 0.0f;
+    u = warp_max(u);
+    if (lane == 0) s_red[32] = u;
+  }
+  __syncthreads();
+  float r = s_red[32];
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ void load_block16(const uint16_t* p, bool aligned32, uint32_t (&w)[8]) {
+  if (aligned32)
+    ldg256(p, w);
+  else
+    ldg128x2(p, w);
+}
+
+// max|y| of 16 bf16 values held as 8 words (no transform): integer max of the
+// magnitude bit patterns, which orders non-negative bf16 like their values.
+__device__ __forceinline__ float absmax16_bits(const uint32_t (&w)[8]) {
+  uint32_t m = w[0] & 0x7FFF7FFFu;
+#pragma unroll
+  for (int k = 1; k < 8; ++k) m = max_u16x2(m, w[k] & 0x7FFF7FFFu);
+  return fmaxf(bf16lo(m), bf16hi(m));
+}
+
+// words -> 16 floats, flipping signs with the RHT sign mask first (exact).
+__device__ __forceinline__ void unpack16(const uint32_t (&w)[8], uint32_t mask, float (&y)[16]) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    uint32_t s = (((mask >> (2 * k)) & 1u) << 15) | (((mask >> (2 * k + 1)) & 1u) << 31);
+    uint32_t v = w[k] ^ s;
+    y[2 * k] = bf16lo(v);
+    y[2 * k + 1] = bf16hi(v);
+  }
+}
+
+// RHT butterflies (stride 1, 2, 4, 8) and the 1/4 scaling; signs already applied.
+__device__ __forceinline__ void hadamard16(float (&v)[16]) { rht16(v, 0u); }
+
+__device__ __forceinline__ float absmax16(const float (&y)[16]) {
+  float m = fabsf(y[0]);
+#pragma unroll
+  for (int j = 1; j < 16; ++j) m = fmaxf(m, fabsf(y[j]));
+  return m;
+}
+
+template <bool RHT>
+__global__ void __launch_bounds__(256) amax_rows_kernel(AmaxParams p) {
+  __shared__ float s_red[33];
+  const int lane = threadIdx.x & 31;
+  const uint32_t rht_mask = RHT ? rht_sign_mask(p.hk0, p.hk1) : 0u;
+  const int64_t nb = p.cols >> 4;
+  const int64_t wpr = (nb + 31) >> 5;
+  const int64_t n_tasks = p.rows * wpr;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  float m = 0.0f;
+  for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n_tasks; t += nwarps) {
+    int64_t r = t / wpr, b = (t - r * wpr) * 32 + lane;
+    if (b >= nb) continue;
+    uint32_t w[8];
+    load_block16(p.x + r * p.ld + b * 16, p.aligned32, w);
+    if (!RHT) {
+      m = fmaxf(m, absmax16_bits(w));
+    } else {
+      float y[16];
+      unpack16(w, rht_mask, y);
+      hadamard16(y);
+      m = fmaxf(m, absmax16(y));
+    }
+  }
+  m = block_max(m, s_red);
+  if (threadIdx.x == 0) p.partials[blockIdx.x] = m;
+}
+
+// RHT down columns: a lane owns 4 adjacent columns x 16 rows.
+__global__ void __launch_bounds__(256) amax_cols_kernel(AmaxParams p) {
+  __shared__ float s_red[33];
+  const int lane = threadIdx.x & 31;
+  const uint32_t rht_mask = rht_sign_mask(p.hk0, p.hk1);
+  const int64_t ngroups = (p.cols + 127) >> 7;  // 128 columns per warp task
+  const int64_t n_tasks = (p.rows >> 4) * ngroups;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  float m = 0.0f;
+  for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n_tasks; t += nwarps) {
+    int64_t rb = t / ngroups, c0 = (t - rb * ngroups) * 128 + 4 * lane;
+    if (c0 >= p.cols) continue;
+    uint2 d[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) d[i] = __ldg(reinterpret_cast<const uint2*>(p.x + (rb * 16 + i) * p.ld + c0));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float y[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        uint32_t wv = (k < 2) ? d[i].x : d[i].y;
+        uint32_t s = ((rht_mask >> i) & 1u) << 31;
+        y[i] = __uint_as_float(((k & 1) ? (wv & 0xFFFF0000u) : (wv << 16)) ^ s);
+      }
+      hadamard16(y);
+      m = fmaxf(m, absmax16(y));
+    }
+  }
+  m = block_max(m, s_red);
+  if (threadIdx.x == 0) p.partials[blockIdx.x] = m;
+}
+
+// ------------------------------------------------------- quantize prologue
+
+__device__ __forceinline__ TensorConsts quant_prologue(const QuantParams& p, float* s_red) {
+  float amax;
+  if (p.n_partials == 0) {
+    amax = __ldg(p.amax_src);
+  } else {
+    float m = 0.0f;
+    for (int i = threadIdx.x; i < p.n_partials; i += blockDim.x) m = fmaxf(m, __ldg(p.amax_src + i));
+    amax = block_max(m, s_red);
+  }
+  TensorConsts tc = tensor_consts(amax);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *p.tensor_scale = tc.s_t;
+  return tc;
+}
+
+// One candidate's squared error given its row residual sum S (or the raw
+// sum of squares when its scale is 0).
+__device__ __forceinline__ float cand_err(float S, uint32_t sf, float eff, const float (&y)[16]) {
+  if (sf == 0) return sumsq16(y);
+  return __fmul_rn(S, __fmul_rn(eff, eff));
+}
+
+template <bool SR>
+__device__ __forceinline__ float cand16(const float (&y)[16], float inv, const uint32_t (&w)[16], uint32_t& lo,
+                                        uint32_t& hi) {
+  if (SR) return cand_sr16(y, inv, w, lo, hi);
+  return cand_rne16(y, inv, lo, hi);
+}
+
+// Quantize one 1D block of 16 transformed values: result codes/scale/choice.
+template <int RULE, bool SR>
+__device__ __forceinline__ void quant_block(const float (&y)[16], float ab, const TensorConsts& tc,
+                                            const uint32_t (&w)[16], uint32_t& lo, uint32_t& hi, uint32_t& sf,
+                                            bool& four) {
+  Cands c = candidates(ab, tc);
+  uint32_t lo6 = 0, hi6 = 0, lo4 = 0, hi4 = 0;
+  float E6 = 0.0f, E4 = 0.0f;
+  if (RULE != FOS_SCALE_4) E6 = cand_err(cand16<SR>(y, c.inv6, w, lo6, hi6), c.sf6, c.eff6, y);
+  if (RULE != FOS_SCALE_6) E4 = cand_err(cand16<SR>(y, c.inv4, w, lo4, hi4), c.sf4, c.eff4, y);
+  four = (RULE == FOS_SCALE_4) || (RULE == FOS_SCALE_4OVER6 && E4 < E6);
+  lo = four ? lo4 : lo6;
+  hi = four ? hi4 : hi6;
+  sf = four ? c.sf4 : c.sf6;
+}
+
+template <bool SR>
+__device__ __forceinline__ void sr_words16(uint64_t i0, const QuantParams& p, uint32_t (&w)[16]) {
+  if (!SR) return;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    U4 u = sr_words4(i0 + 4 * g, p.sr_k0, p.sr_k1);
+    w[4 * g] = u.x;
+    w[4 * g + 1] = u.y;
+    w[4 * g + 2] = u.z;
+    w[4 * g + 3] = u.w;
+  }
+}
+
+// ------------------------------------------------------------ quant_rows
+// Warp task = one row and 32 consecutive blocks (512 values); lane = block.
+template <int RULE, bool RHT, bool SR>
+__global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
+  __shared__ float s_red[33];
+  const TensorConsts tc = quant_prologue(p, s_red);
+  const uint32_t rht_mask = RHT ? rht_sign_mask(p.hk0, p.hk1) : 0u;
+  const int lane = threadIdx.x & 31;
+  const int64_t nb = p.nb;
+  const int64_t wpr = (nb + 31) >> 5;
+  const int64_t n_tasks = p.R * wpr;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (t >= n_tasks) return;
+  int64_t r = t / wpr, ch = t - r * wpr;
+  const int64_t dr = nwarps / wpr, dch = nwarps - dr * wpr;
+
+  uint32_t wcur[8];
+  {
+    int64_t b = ch * 32 + lane;
+    if (b < nb) load_block16(p.x + r * p.ld + b * 16, p.aligned32, wcur);
+  }
+  for (;;) {
+    // next task, and its prefetch
+    int64_t tn = t + nwarps, rn = r + dr, chn = ch + dch;
+    if (chn >= wpr) {
+      chn -= wpr;
+      ++rn;
+    }
+    uint32_t wnext[8];
+    if (tn < n_tasks) {
+      int64_t bn = chn * 32 + lane;
+      if (bn < nb) load_block16(p.x + rn * p.ld + bn * 16, p.aligned32, wnext);
+    }
+
+    const int64_t b = ch * 32 + lane;
+    const bool valid = b < nb;
+    uint32_t lo = 0, hi = 0, sf = 0;
+    bool four = false;
+    if (valid) {
+      float y[16];
+      float ab;
+      if (RHT) {
+        unpack16(wcur, rht_mask, y);
+        hadamard16(y);
+        ab = absmax16(y);
+      } else {
+        unpack16(wcur, 0u, y);
+        ab = absmax16_bits(wcur);
+      }
+      uint32_t w[16];
+      sr_words16<SR>((uint64_t)r * (uint64_t)p.cols + (uint64_t)b * 16, p, w);
+      quant_block<RULE, SR>(y, ab, tc, w, lo, hi, sf, four);
+      *reinterpret_cast<uint2*>(p.codes + r * p.ld_codes + b * 8) = make_uint2(lo, hi);
+      if (p.choice) p.choice[r * nb + b] = four ? 1 : 0;
+    }
+    if (p.sf_layout == FOS_SF_SWIZZLED_128x4) {
+      // four consecutive blocks of a row are four consecutive bytes
+      uint32_t v = sf;
+      v |= __shfl_down_sync(0xFFFFFFFFu, sf, 1) << 8;
+      v |= __shfl_down_sync(0xFFFFFFFFu, sf, 2) << 16;
+      v |= __shfl_down_sync(0xFFFFFFFFu, sf, 3) << 24;
+      if (valid && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(p.sf + sf_off(r, b, nb, 0)) = v;
+    } else if (valid) {
+      p.sf[r * nb + b] = (uint8_t)sf;
+    }
+
+    if (tn >= n_tasks) break;
+    t = tn;
+    r = rn;
+    ch = chn;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) wcur[k] = wnext[k];
+  }
+}
+
+// ------------------------------------------------------------ quant_cols
+// Transposed output: a lane owns source columns c0..c0+3 (output rows) and
+// the 16 source rows of output block rb.
+template <int RULE, bool RHT, bool SR>
+__global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
+  __shared__ float s_red[33];
+  const TensorConsts tc = quant_prologue(p, s_red);
+  const uint32_t rht_mask = RHT ? rht_sign_mask(p.hk0, p.hk1) : 0u;
+  const int lane = threadIdx.x & 31;
+  const int64_t ngroups = (p.cols + 127) >> 7;
+  const int64_t n_tasks = (p.rows >> 4) * ngroups;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t nb = p.nb;  // = rows / 16
+  for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n_tasks; t += nwarps) {
+    const int64_t rb = t / ngroups, c0 = (t - rb * ngroups) * 128 + 4 * lane;
+    if (c0 >= p.cols) continue;
+    uint2 d[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) d[i] = __ldg(reinterpret_cast<const uint2*>(p.x + (rb * 16 + i) * p.ld + c0));
+#pragma unroll 1
+    for (int k = 0; k < 4; ++k) {
+      float y[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        uint32_t wv = (k < 2) ? d[i].x : d[i].y;
+        uint32_t s = RHT ? (((rht_mask >> i) & 1u) << 31) : 0u;
+        y[i] = __uint_as_float(((k & 1) ? (wv & 0xFFFF0000u) : (wv << 16)) ^ s);
+      }
+      if (RHT) hadamard16(y);
+      const float ab = absmax16(y);
+      uint32_t w[16];
+      if (SR) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          U4 u = sr_words4((uint64_t)(rb * 16 + i) * (uint64_t)p.cols + (uint64_t)c0, p.sr_k0, p.sr_k1);
+          w[i] = k == 0 ? u.x : (k == 1 ? u.y : (k == 2 ? u.z : u.w));
+        }
+      }
+      uint32_t lo, hi, sf;
+      bool four;
+      quant_block<RULE, SR>(y, ab, tc, w, lo, hi, sf, four);
+      const int64_t orow = c0 + k;
+      *reinterpret_cast<uint2*>(p.codes + orow * p.ld_codes + rb * 8) = make_uint2(lo, hi);
+      p.sf[sf_off(orow, rb, nb, p.sf_layout)] = (uint8_t)sf;
+      if (p.choice) p.choice[orow * nb + rb] = four ? 1 : 0;
+    }
+  }
+}
+
+// -------------------------------------------------------------- quant_2d
+// Warp task = 16 source rows x 32 source columns (two tiles); lane l owns
+// source row (l & 15) of tile (l >> 4).  Tile reductions use xor-shuffles
+// within each 16-lane half; the error tree pairs adjacent rows first.
+__device__ __forceinline__ float half_max(float v) {
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float half_tree_sum(float v) {
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+template <int RULE, bool RHT, bool SR, bool TRANS>
+__global__ void __launch_bounds__(256) quant_2d_kernel(QuantParams p) {
+  __shared__ float s_red[33];
+  const TensorConsts tc = quant_prologue(p, s_red);
+  const uint32_t rht_mask = RHT ? rht_sign_mask(p.hk0, p.hk1) : 0u;
+  const int lane = threadIdx.x & 31, i = lane & 15, half = lane >> 4;
+  const int64_t ntc = p.cols >> 4;               // tiles along source columns
+  const int64_t npair = (ntc + 1) >> 1;
+  const int64_t n_tasks = (p.rows >> 4) * npair;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n_tasks; t += nwarps) {
+    const int64_t tr = t / npair, tcol = (t - tr * npair) * 2 + half;
+    const bool valid = tcol < ntc;  // uniform within each 16-lane half
+    const int64_t r = tr * 16 + i, c0 = tcol * 16;
+    uint32_t wv[8];
+    float y[16];
+    if (valid) {
+      load_block16(p.x + r * p.ld + c0, p.aligned32, wv);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) wv[k] = 0u;
+    }
+    if (RHT && !TRANS) {
+      unpack16(wv, rht_mask, y);
+      hadamard16(y);
+    } else {
+      unpack16(wv, 0u, y);
+    }
+    if (RHT && TRANS) {
+      // transform down the 16 source rows of each column: across lanes
+      if ((rht_mask >> i) & 1u) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) y[j] = -y[j];
+      }
+#pragma unroll
+      for (int h = 1; h < 16; h <<= 1) {
+        const bool upper = (i & h) != 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float o = __shfl_xor_sync(0xFFFFFFFFu, y[j], h);
+          y[j] = upper ? __fsub_rn(o, y[j]) : __fadd_rn(y[j], o);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) y[j] = __fmul_rn(y[j], 0.25f);
+    }
+    const float ab = half_max(absmax16(y));
+    uint32_t w[16];
+    sr_words16<SR>((uint64_t)r * (uint64_t)p.cols + (uint64_t)c0, p, w);
+    Cands c = candidates(ab, tc);
+    uint32_t lo6 = 0, hi6 = 0, lo4 = 0, hi4 = 0;
+    float E6 = 0.0f, E4 = 0.0f;
+    if (RULE != FOS_SCALE_4) {
+      float S = cand16<SR>(y, c.inv6, w, lo6, hi6);
+      if (c.sf6 == 0) S = sumsq16(y);
+      S = half_tree_sum(S);
+      E6 = c.sf6 ? __fmul_rn(S, __fmul_rn(c.eff6, c.eff6)) : S;
+    }
+    if (RULE != FOS_SCALE_6) {
+      float S = cand16<SR>(y, c.inv4, w, lo4, hi4);
+      if (c.sf4 == 0) S = sumsq16(y);
+      S = half_tree_sum(S);
+      E4 = c.sf4 ? __fmul_rn(S, __fmul_rn(c.eff4, c.eff4)) : S;
+    }
+    const bool four = (RULE == FOS_SCALE_4) || (RULE == FOS_SCALE_4OVER6 && E4 < E6);
+    const uint32_t lo = four ? lo4 : lo6, hi = four ? hi4 : hi6, sf = four ? c.sf4 : c.sf6;
+    if (!TRANS) {
+      if (valid) {
+        *reinterpret_cast<uint2*>(p.codes + r * p.ld_codes + tcol * 8) = make_uint2(lo, hi);
+        p.sf[sf_off(r, tcol, p.nb, p.sf_layout)] = (uint8_t)sf;
+        if (p.choice) p.choice[r * p.nb + tcol] = four ? 1 : 0;
+      }
+    } else {
+      // lane i collects output row (source column) c0 + i: nibble i of every
+      // source row j of its tile, j = 0..15 in order along the output row
+      uint32_t olo = 0, ohi = 0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        uint32_t slo = __shfl_sync(0xFFFFFFFFu, lo, (half << 4) | j);
+        uint32_t shi = __shfl_sync(0xFFFFFFFFu, hi, (half << 4) | j);
+        uint32_t nib = ((i < 8 ? slo : shi) >> (4 * (i & 7))) & 15u;
+        if (j < 8)
+          olo |= nib << (4 * j);
+        else
+          ohi |= nib << (4 * (j - 8));
+      }
+      if (valid) {
+        const int64_t orow = c0 + i;
+        *reinterpret_cast<uint2*>(p.codes + orow * p.ld_codes + tr * 8) = make_uint2(olo, ohi);
+        p.sf[sf_off(orow, tr, p.nb, p.sf_layout)] = (uint8_t)sf;
+        if (p.choice) p.choice[orow * p.nb + tr] = four ? 1 : 0;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------ sf padding
+
+__global__ void sf_pad_zero_kernel(uint8_t* sf, int64_t bytes, int64_t R, int64_t nb) {
+  const int64_t n_ct = (nb + 3) >> 2;
+  for (int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; o < bytes; o += (int64_t)gridDim.x * blockDim.x) {
+    int64_t tile = o >> 9, w = o & 511;
+    int64_t rt = tile / n_ct, ct = tile - rt * n_ct;
+    int64_t r = rt * 128 + ((w >> 2) & 3) * 32 + (w >> 4);
+    int64_t c = ct * 4 + (w & 3);
+    if (r >= R || c >= nb) sf[o] = 0;
+  }
+}
+
+// ----------------------------------------------------------- dequantize
+
+template <bool BF16>
+__global__ void __launch_bounds__(256) dequant_kernel(DequantParams p) {
+  const int64_t nb = p.cols >> 4;
+  const int64_t n = p.rows * nb;
+  const float s_t = __ldg(p.tensor_scale);
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = t / nb, b = t - r * nb;
+    const uint2 cw = *reinterpret_cast<const uint2*>(p.codes + r * p.ld_codes + b * 8);
+    const uint32_t s = p.sf[sf_off(r, b, nb, p.sf_layout)];
+    const float eff = __fmul_rn(e4m3x2_decode(s).x, s_t);
+    float v[16];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      uint32_t byte = ((k < 4 ? cw.x : cw.y) >> (8 * (k & 3))) & 0xFFu;
+      F2 g = e2m1x2_decode(byte);
+      F2 x = mul2(g, F2{eff, eff});
+      v[2 * k] = x.x;
+      v[2 * k + 1] = x.y;
+    }
+    if (BF16) {
+      uint32_t o[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+        o[k] = *reinterpret_cast<uint32_t*>(&h);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + r * p.ld_out + b * 16);
+      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    } else {
+      float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + r * p.ld_out + b * 16);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- codecs
+
+__global__ void e2m1_encode_kernel(const float* x, int64_t n, uint8_t* out) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = (uint8_t)(e2m1x2(x[i], 0.0f) & 15u);
+}
+
+__global__ void e4m3_encode_kernel(const float* x, int64_t n, uint8_t* out) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = (uint8_t)(e4m3x2(x[i], 0.0f) & 0xFFu);
+}
+
+__global__ void philox_kernel(const uint32_t* ctr, int64_t n, uint32_t k0, uint32_t k1, uint32_t* out) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    U4 u = philox10(ctr[4 * i], ctr[4 * i + 1], ctr[4 * i + 2], ctr[4 * i + 3], k0, k1);
+    out[4 * i] = u.x;
+    out[4 * i + 1] = u.y;
+    out[4 * i + 2] = u.z;
+    out[4 * i + 3] = u.w;
+  }
+}
+
+// ------------------------------------------------------------- launchers
+
+static int sm_count() {
+  int dev = 0, n = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
+}
+
+int amax_grid(int64_t n_warp_tasks) {
+  int64_t g = (n_warp_tasks + 7) / 8;
+  int64_t cap = (int64_t)sm_count() * 4;
+  if (cap > kMaxAmaxPartials) cap = kMaxAmaxPartials;
+  if (g > cap) g = cap;
+  return (int)(g < 1 ? 1 : g);
+}
+
+cudaError_t launch_amax(const AmaxParams& p, bool hadamard, bool transpose, int grid, cudaStream_t s) {
+  if (hadamard && transpose)
+    amax_cols_kernel<<<grid, 256, 0, s>>>(p);
+  else if (hadamard)
+    amax_rows_kernel<true><<<grid, 256, 0, s>>>(p);
+  else
+    amax_rows_kernel<false><<<grid, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <int RULE, bool RHT, bool SR>
+static void launch_q(const QuantParams& p, int kind, int grid, cudaStream_t s) {
+  switch (kind) {
+    case 0: quant_rows_kernel<RULE, RHT, SR><<<grid, 256, 0, s>>>(p); break;
+    case 1: quant_cols_kernel<RULE, RHT, SR><<<grid, 256, 0, s>>>(p); break;
+    case 2: quant_2d_kernel<RULE, RHT, SR, false><<<grid, 256, 0, s>>>(p); break;
+    default: quant_2d_kernel<RULE, RHT, SR, true><<<grid, 256, 0, s>>>(p); break;
+  }
+}
+
+template <int RULE>
+static void launch_q_rule(const QuantParams& p, int kind, bool rht, bool sr, int grid, cudaStream_t s) {
+  if (rht) {
+    if (sr) launch_q<RULE, true, true>(p, kind, grid, s);
+    else launch_q<RULE, true, false>(p, kind, grid, s);
+  } else {
+    if (sr) launch_q<RULE, false, true>(p, kind, grid, s);
+    else launch_q<RULE, false, false>(p, kind, grid, s);
+  }
+}
+
+int quant_grid(int64_t n_warp_tasks) {
+  int64_t g = (n_warp_tasks + 7) / 8;
+  int64_t cap = (int64_t)sm_count() * 8;
+  if (g > cap) g = cap;
+  return (int)(g < 1 ? 1 : g);
+}
+
+cudaError_t launch_quant(const QuantParams& p, int rule, int kind, bool rht, bool sr, int grid, cudaStream_t s) {
+  switch (rule) {
+    case FOS_SCALE_6: launch_q_rule<FOS_SCALE_6>(p, kind, rht, sr, grid, s); break;
+    case FOS_SCALE_4: launch_q_rule<FOS_SCALE_4>(p, kind, rht, sr, grid, s); break;
+    default: launch_q_rule<FOS_SCALE_4OVER6>(p, kind, rht, sr, grid, s); break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sf_pad(uint8_t* sf, int64_t bytes, int64_t R, int64_t nb, cudaStream_t s) {
+  int64_t g = (bytes + 255) / 256;
+  if (g > 1024) g = 1024;
+  sf_pad_zero_kernel<<<(int)(g < 1 ? 1 : g), 256, 0, s>>>(sf, bytes, R, nb);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const DequantParams& p, bool bf16, cudaStream_t s) {
+  int64_t n = p.rows * (p.cols >> 4);
+  int64_t g = (n + 255) / 256;
+  int64_t cap = (int64_t)sm_count() * 8;
+  if (g > cap) g = cap;
+  if (g < 1) g = 1;
+  if (bf16)
+    dequant_kernel<true><<<(int)g, 256, 0, s>>>(p);
+  else
+    dequant_kernel<false><<<(int)g, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_e2m1_encode(const float* x, int64_t n, uint8_t* out, cudaStream_t s) {
+  e2m1_encode_kernel<<<(int)((n + 255) / 256 < 4096 ? (n + 255) / 256 + 1 : 4096), 256, 0, s>>>(x, n, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_e4m3_encode(const float* x, int64_t n, uint8_t* out, cudaStream_t s) {
+  e4m3_encode_kernel<<<(int)((n + 255) / 256 < 4096 ? (n + 255) / 256 + 1 : 4096), 256, 0, s>>>(x, n, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_philox(const uint32_t* ctr, int64_t n, uint64_t key, uint32_t* out, cudaStream_t s) {
+  philox_kernel<<<(int)((n + 255) / 256 < 4096 ? (n + 255) / 256 + 1 : 4096), 256, 0, s>>>(
+      ctr, n, (uint32_t)key, (uint32_t)(key >> 32), out);
+  return cudaGetLastError();
+}
+
+}  // namespace fos

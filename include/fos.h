@@ -1,0 +1,198 @@
+/*
+ * fos.h -- Four Over Six NVFP4 quantization and block-scaled FP4 GEMM for
+ * NVIDIA B300 (sm_103a).  Plain C ABI: device pointers, sizes, an options
+ * struct and a CUDA stream.
+ *
+ * What the library computes (cited by page title and section):
+ *   - "FP4" (Ultralytics glossary), "FP4 Nasıl Çalışır": FP4 is E2M1 with the
+ *     value grid {0, ±0.5, ±1, ±1.5, ±2, ±3, ±4, ±6}; NVFP4 groups 16 values
+ *     under one E4M3 block scale and adds an FP32 per-tensor scale.
+ *   - "Four Over Six" (Transformers docs), first section: each 16-value block
+ *     is scaled so that its largest magnitude lands on 4 or on 6, whichever
+ *     gives the lower quantization error; options: random Hadamard transform,
+ *     2D block scaling, transposed inputs, stochastic rounding.
+ *   - "FP4", "FP4 ile Çıkarım ve Eğitim": FP4 matrix products accumulate at
+ *     higher precision (fos_gemm accumulates in FP32 in tensor memory).
+ *
+ * Exact definition (identical bit for bit to the CPU reference used by the
+ * tests):
+ *   y      = x, or 0.25*H16*diag(s)*x per 16-block along the blocking
+ *            dimension when the RHT is on (H16 Sylvester Hadamard, butterflies
+ *            of stride 1,2,4,8; s_j = 1-2*bit_j of word 0 of
+ *            Philox4x32-10(counter (0,0,0,1), key = hadamard_seed)).
+ *   s_t    = amax / 2688 (= 6*448), amax = max|y| over the tensor.
+ *   k_M    = 1 / (M*s_t) for M in {6, 4}, once per tensor.
+ *   per block (16 values, or a 16x16 tile): a = max|y|;
+ *   sf_M   = E4M3_rne_satfinite(a * k_M);  eff_M = float(sf_M) * s_t;
+ *   q      = y * min(1/eff_M, FLT_MAX);  code = E2M1(q) (RNE, or stochastic:
+ *            round up iff ((w >> 8) * 2^-24) < p, w = word (i mod 4) of
+ *            Philox4x32-10(counter (lo32(i/4), hi32(i/4), 0, 0), key = sr_seed),
+ *            i = r*cols + c the source index of the element);
+ *   E_M    = (sum (q - g)^2) * eff_M^2 with g the code's value (sum over a
+ *            16-block: two FMA chains over even/odd positions then one add;
+ *            over a 2D tile: per source row as above, then a pairwise tree),
+ *            or sum y^2 when sf_M == 0;
+ *   keep 4 iff E_4 < E_6 (ties keep 6).
+ *
+ * All pointers named "device" are device pointers owned by the caller.  The
+ * library allocates no device memory and keeps no global state besides
+ * cached driver entry points; every call enqueues asynchronous work on
+ * `stream` and returns without synchronizing.  A call that fails argument
+ * validation returns FOS_ERR_INVALID_ARG (or FOS_ERR_UNSUPPORTED) and
+ * enqueues nothing.  FOS_ERR_CUDA means a launch failed; the CUDA error is
+ * left for cudaGetLastError().
+ */
+#ifndef FOS_H
+#define FOS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FOS_ABI_VERSION 1
+
+typedef enum fos_status {
+  FOS_OK = 0,
+  FOS_ERR_INVALID_ARG = 1,
+  FOS_ERR_UNSUPPORTED = 2,
+  FOS_ERR_CUDA = 3,
+  FOS_ERR_TIMEOUT = 4 /* written to a device status word by a kernel whose bounded wait ran out */
+} fos_status;
+
+typedef enum fos_scale_rule {
+  FOS_SCALE_4OVER6 = 0, /* the adaptive rule: keep the candidate with lower error */
+  FOS_SCALE_6 = 1,      /* plain NVFP4: block max mapped to 6 */
+  FOS_SCALE_4 = 2       /* block max mapped to 4 (baseline for tests) */
+} fos_scale_rule;
+
+typedef enum fos_rounding { FOS_ROUND_RNE = 0, FOS_ROUND_STOCHASTIC = 1 } fos_rounding;
+
+typedef enum fos_sf_layout {
+  /* 128 rows x 4 scale columns per 512-byte tile, tiles row-major over
+   * (row tile, column tile), (r, c) at (r%32)*16 + ((r%128)/32)*4 + c%4 inside
+   * a tile; rows padded to 128 and scale columns to 4 with zero bytes.  This
+   * is the layout the block-scaled tensor-core MMA reads (fos_gemm). */
+  FOS_SF_SWIZZLED_128x4 = 0,
+  FOS_SF_ROWMAJOR = 1 /* [rows][cols/16], no padding */
+} fos_sf_layout;
+
+typedef enum fos_dtype { FOS_DTYPE_F32 = 0, FOS_DTYPE_BF16 = 1 } fos_dtype;
+
+typedef struct fos_quant_options {
+  uint32_t struct_size;  /* sizeof(fos_quant_options) */
+  int32_t scale_rule;    /* fos_scale_rule */
+  int32_t rounding;      /* fos_rounding */
+  int32_t block_2d;      /* 0: 1x16 blocks; 1: 16x16 tiles, one scale per tile */
+  int32_t transpose;     /* 1: the output describes X^T (blocks run along X's rows) */
+  int32_t hadamard;      /* 1: apply the random Hadamard transform first */
+  int32_t sf_layout;     /* fos_sf_layout */
+  int32_t reserved;      /* must be 0 */
+  uint64_t sr_seed;      /* key of the stochastic-rounding Philox stream */
+  uint64_t hadamard_seed;/* key of the RHT sign vector */
+  const float* tensor_amax; /* optional device pointer: use this amax and skip the amax pass */
+} fos_quant_options;
+
+/* A quantized matrix: rows x cols logical values, blocks along cols. */
+typedef struct fos_nvfp4_tensor {
+  const uint8_t* codes;      /* device: rows x ld_codes bytes, 2 codes per byte, even column in the low nibble */
+  const uint8_t* sf;         /* device: E4M3 block scales in sf_layout */
+  const float* tensor_scale; /* device: 1 float, s_t */
+  int64_t rows;
+  int64_t cols;              /* multiple of 16 */
+  int64_t ld_codes;          /* bytes between rows, >= cols/2 */
+  int32_t sf_layout;
+  int32_t reserved;
+} fos_nvfp4_tensor;
+
+/* Library and CUDA-side version; FOS_ABI_VERSION of the built library. */
+int32_t fos_abi_version(void);
+const char* fos_status_string(fos_status s);
+
+/* Bytes of the scale buffer for an output of out_rows x out_cols values
+ * (out_cols % 16 == 0).  INVALID_ARG on negative sizes or a bad layout. */
+fos_status fos_sf_bytes(int64_t out_rows, int64_t out_cols, int32_t sf_layout, size_t* bytes);
+
+/* Device scratch fos_quantize needs for these options (0 when
+ * opt->tensor_amax is given). */
+fos_status fos_quantize_workspace_size(int64_t rows, int64_t cols, const fos_quant_options* opt,
+                                       size_t* bytes);
+
+/*
+ * fos_tensor_amax -- the tensor amax step: *amax_out = max|y| over the bf16
+ * matrix X [rows, cols] (row stride ld_x elements), y = X or its RHT along
+ * cols (transpose = 0) or along rows (transpose = 1).
+ *   x: device, 16-byte aligned, ld_x % 8 == 0, cols % 16 == 0, and
+ *      rows % 16 == 0 when hadamard && transpose.
+ *   amax_out: device float.  workspace: device, >= fos_quantize_workspace_size().
+ */
+fos_status fos_tensor_amax(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int32_t hadamard,
+                           int32_t transpose, uint64_t hadamard_seed, float* amax_out, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * fos_quantize -- NVFP4 quantization with the Four Over Six block-scale rule.
+ *   x         device bf16 [rows, cols], row stride ld_x elements; 16-byte
+ *             aligned; ld_x % 8 == 0; cols % 16 == 0; rows % 16 == 0 when
+ *             opt->transpose or opt->block_2d.  Values must be finite.
+ *   Output orientation: R_out x C_out = rows x cols, or cols x rows when
+ *   opt->transpose.  Blocks run along C_out.
+ *   codes     device, R_out rows of ld_codes bytes (ld_codes >= C_out/2,
+ *             ld_codes % 8 == 0, 8-byte aligned); two E2M1 codes per byte.
+ *   sf        device, fos_sf_bytes(R_out, C_out, opt->sf_layout) bytes; pad
+ *             bytes are written 0.  For 2D tiles the tile's scale is stored in
+ *             each of its 16 rows.
+ *   tensor_scale  device float, receives s_t.
+ *   choice    optional device [R_out][C_out/16] bytes: 1 where the block kept
+ *             the 4 candidate (NULL: not written).
+ *   workspace device scratch of fos_quantize_workspace_size() bytes (may be
+ *             NULL when opt->tensor_amax is given).
+ * The RHT output is not undone: codes describe the transformed values.
+ */
+fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                        const fos_quant_options* opt, uint8_t* codes, int64_t ld_codes, uint8_t* sf,
+                        float* tensor_scale, uint8_t* choice, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream);
+
+/*
+ * fos_dequantize -- x_hat = g * (float(sf) * s_t), each product rounded to FP32;
+ * out_dtype FOS_DTYPE_F32, or FOS_DTYPE_BF16 (the FP32 value rounded to
+ * nearest even).  out: device [q->rows][ld_out] elements.
+ */
+fos_status fos_dequantize(const fos_nvfp4_tensor* q, void* out, int32_t out_dtype, int64_t ld_out,
+                          cudaStream_t stream);
+
+/*
+ * fos_gemm -- C = (s_tA * s_tB) * sum_k (gA*sfA)(gB*sfB), the NVFP4 linear-layer
+ * contraction C[m][n] = A[m,:] . B[n,:] with A [M,K] and B [N,K] both
+ * quantized along K.  Products and FP32 accumulation run on the tcgen05
+ * tensor cores (block-scaled MMA, 16-value E4M3 scales); the result is
+ * scaled once in FP32 and rounded to bf16.
+ *   A, B      K % 256 == 0 (same K), FOS_SF_SWIZZLED_128x4 scales, codes 16-byte
+ *             aligned with ld_codes % 16 == 0; M % 128 == 0, N % 256 == 0.
+ *   C         device bf16 [M][ldc], ldc % 8 == 0, 16-byte aligned.
+ *   dev_status optional device int32: a kernel whose bounded pipeline wait
+ *             runs out writes FOS_ERR_TIMEOUT there and leaves C incomplete.
+ */
+fos_status fos_gemm(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* C, int64_t ldc,
+                    int32_t* dev_status, cudaStream_t stream);
+
+/* ---- element codecs (the conversions the quantizer uses), for testing ---- */
+
+/* codes[i] = E2M1 code (RNE, saturating, sign kept) of x[i]; one code per byte. */
+fos_status fos_e2m1_encode(const float* x, int64_t n, uint8_t* codes, cudaStream_t stream);
+/* out[i] = E4M3 byte (RNE, saturating to 448) of x[i]. */
+fos_status fos_e4m3_encode(const float* x, int64_t n, uint8_t* out, cudaStream_t stream);
+/* out[4*i .. 4*i+3] = Philox4x32-10(counter[4*i..], key = (lo32(key), hi32(key))). */
+fos_status fos_philox4x32_10(const uint32_t* counters, int64_t n, uint64_t key, uint32_t* out,
+                             cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FOS_H */

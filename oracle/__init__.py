@@ -49,6 +49,8 @@ class _Opts(ctypes.Structure):
         ("hadamard_seed", ctypes.c_uint64),
         ("use_amax", ctypes.c_int32),
         ("amax", ctypes.c_float),
+        ("src_row0", ctypes.c_int64),
+        ("src_cols", ctypes.c_int64),
     ]
 
 
@@ -231,6 +233,8 @@ def quantize(
     amax: float | None = None,
     ld: int | None = None,
     ld_codes: int | None = None,
+    src_row0: int = 0,
+    src_cols: int = 0,
 ) -> QResult:
     """Quantize a bf16 matrix given as uint16 bit patterns [rows, cols].
 
@@ -244,7 +248,7 @@ def quantize(
     else:
         cols, ld = ld, x.shape[1]
     return _quantize(x, rows, cols, ld, scale_rule, rounding, block_2d, transpose, hadamard,
-                     sf_layout, sr_seed, hadamard_seed, amax, ld_codes)
+                     sf_layout, sr_seed, hadamard_seed, amax, ld_codes, src_row0, src_cols)
 
 
 def quantize_view(x_bf16: np.ndarray, cols: int, **kw) -> QResult:
@@ -254,11 +258,11 @@ def quantize_view(x_bf16: np.ndarray, cols: int, **kw) -> QResult:
     return _quantize(x, rows, cols, ld, kw.get("scale_rule", SCALE_4OVER6), kw.get("rounding", ROUND_RNE),
                      kw.get("block_2d", False), kw.get("transpose", False), kw.get("hadamard", False),
                      kw.get("sf_layout", SF_SWIZZLED), kw.get("sr_seed", 0), kw.get("hadamard_seed", 0),
-                     kw.get("amax", None), kw.get("ld_codes", None))
+                     kw.get("amax", None), kw.get("ld_codes", None), kw.get("src_row0", 0), kw.get("src_cols", 0))
 
 
 def _quantize(x, rows, cols, ld, scale_rule, rounding, block_2d, transpose, hadamard, sf_layout,
-              sr_seed, hadamard_seed, amax, ld_codes) -> QResult:
+              sr_seed, hadamard_seed, amax, ld_codes, src_row0=0, src_cols=0) -> QResult:
     R, C = (cols, rows) if transpose else (rows, cols)
     nb = C // 16
     ldc = C // 2 if ld_codes is None else ld_codes
@@ -268,7 +272,7 @@ def _quantize(x, rows, cols, ld, scale_rule, rounding, block_2d, transpose, hada
     choice = np.zeros((max(R, 1), max(nw, 1)), np.uint32)
     ts = np.zeros(1, np.float32)
     o = _Opts(scale_rule, rounding, int(block_2d), int(transpose), int(hadamard), sf_layout,
-              sr_seed, hadamard_seed, 0 if amax is None else 1, 0.0 if amax is None else amax)
+              sr_seed, hadamard_seed, 0 if amax is None else 1, 0.0 if amax is None else amax, src_row0, src_cols)
     rc = lib().orc_quantize(_p(x), rows, cols, ld, ctypes.byref(o), _p(codes), ldc, _p(sf), _p(ts),
                             _p(choice))
     if rc != 0:

@@ -255,6 +255,11 @@ typedef struct {
   uint64_t hadamard_seed;
   int32_t use_amax; /* 1: take amax from the field below */
   float amax;
+  /* Source coordinates of x inside a larger matrix, for the stochastic-rounding
+   * element index i = (src_row0 + r) * src_cols + c (src_cols 0: cols).  Lets a
+   * caller quantize sampled rows of a big matrix with the big matrix's indices. */
+  int64_t src_row0;
+  int64_t src_cols;
 } orc_options;
 
 static float bf16_to_f32(uint16_t h) {
@@ -332,7 +337,7 @@ int orc_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, cons
     for (int64_t c = 0; c < C; ++c) {
       int64_t sr = o->transpose ? c : r, sc = o->transpose ? r : c;
       y[r * C + c] = bf16_to_f32(x[sr * ld + sc]);
-      src[r * C + c] = (uint64_t)sr * (uint64_t)cols + (uint64_t)sc;
+      src[r * C + c] = (uint64_t)(o->src_row0 + sr) * (uint64_t)(o->src_cols ? o->src_cols : cols) + (uint64_t)sc;
     }
   /* step 2, R6 */
   if (o->hadamard) {

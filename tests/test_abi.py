@@ -1,0 +1,116 @@
+"""The C-ABI library (no GPU needed): it loads, exports every call that
+include/fos.h declares, its structs have the header's layout, and argument
+validation rejects bad input without launching anything."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fos.h")
+
+
+@pytest.fixture(scope="module")
+def fos():
+    import adaptive_quantization_fos_b300 as fos
+
+    return fos
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fos_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_function(fos):
+    lib = ctypes.CDLL(fos.LIB_PATH)
+    names = declared_functions()
+    assert "fos_quantize" in names and "fos_gemm" in names and "fos_dequantize" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(fos.EXPORTED)
+
+
+def test_struct_layout_matches_header(fos, tmp_path):
+    src = tmp_path / "layout.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "fos.h"\n'
+        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu\\n\", sizeof(fos_quant_options),"
+        " offsetof(fos_quant_options, sr_seed), offsetof(fos_quant_options, tensor_amax),"
+        " sizeof(fos_nvfp4_tensor), offsetof(fos_nvfp4_tensor, rows), offsetof(fos_nvfp4_tensor, sf_layout));"
+        "return 0;}\n")
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), "-I", "/usr/local/cuda/include", str(src),
+                           "-o", str(exe)])
+    got = [int(v) for v in subprocess.check_output([str(exe)]).split()]
+    O, T = fos.fos_quant_options, fos.fos_nvfp4_tensor
+    assert got == [ctypes.sizeof(O), O.sr_seed.offset, O.tensor_amax.offset, ctypes.sizeof(T), T.rows.offset,
+                   T.sf_layout.offset]
+
+
+def test_version_and_sizes(fos):
+    assert fos.fos_abi_version() == 1
+    assert fos.fos_sf_bytes(300, 1040) == 384 * 68
+    assert fos.fos_sf_bytes(300, 1040, fos.FOS_SF_ROWMAJOR) == 300 * 65
+    assert fos.fos_sf_bytes(0, 0) == 0
+    o = fos.options()
+    assert fos.fos_quantize_workspace_size(64, 64, o) > 0
+    with pytest.raises(fos.FosError):
+        fos.fos_sf_bytes(10, 17)
+
+
+def test_validation_rejects_without_launch(fos):
+    INVALID = fos.FOS_ERR_INVALID_ARG
+    o = fos.options()
+    fake = 1 << 20  # never dereferenced: validation fails first
+    ws = fos.fos_quantize_workspace_size(32, 64, o)
+    q = lambda **kw: fos.fos_quantize(  # noqa: E731
+        kw.get("x", fake), kw.get("rows", 32), kw.get("cols", 64), kw.get("ld", 64), kw.get("opt", o),
+        kw.get("codes", fake), kw.get("ldc", 32), kw.get("sf", fake), kw.get("ts", fake), 0,
+        kw.get("ws", fake), kw.get("wsb", ws), 0)
+    assert q(cols=40, ld=40) == INVALID  # cols % 16
+    assert q(ld=60) == INVALID  # ld < cols
+    assert q(ld=68) == INVALID  # ld % 8
+    assert q(x=fake + 2) == INVALID  # alignment
+    assert q(x=0) == INVALID
+    assert q(codes=0) == INVALID
+    assert q(ldc=16) == INVALID  # ld_codes < C/2
+    assert q(ws=0) == INVALID
+    assert q(wsb=4) == INVALID
+    assert q(rows=-1) == INVALID
+    assert q(rows=24, opt=fos.options(transpose=True)) == INVALID  # rows % 16
+    assert q(rows=24, opt=fos.options(block_2d=True)) == INVALID
+    bad = fos.options()
+    bad.scale_rule = 7
+    assert q(opt=bad) == INVALID
+    bad = fos.options()
+    bad.struct_size = 8
+    assert q(opt=bad) == INVALID
+    t = fos.fos_nvfp4_tensor()
+    assert fos.fos_dequantize(t, fake, 0, 64, 0) == INVALID
+    assert fos.fos_e2m1_encode(0, 5, 0, 0) == INVALID
+
+
+def test_gemm_validation(fos):
+    INVALID = fos.FOS_ERR_INVALID_ARG
+    fake = 1 << 20
+    A = fos.fos_nvfp4_tensor(codes=fake, sf=fake, tensor_scale=fake, rows=128, cols=256, ld_codes=128)
+    B = fos.fos_nvfp4_tensor(codes=fake, sf=fake, tensor_scale=fake, rows=256, cols=512, ld_codes=256)
+    assert fos.fos_gemm(A, B, fake, 256, 0, 0) == INVALID  # K differs
+    B.cols, B.ld_codes = 256, 128
+    assert fos.fos_gemm(A, B, fake, 100, 0, 0) == INVALID  # ldc < N
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    import importlib.util
+
+    spec = importlib.util.spec_from_file_location(
+        "fos_copy", os.path.join(ROOT, "adaptive_quantization_fos_b300", "__init__.py"))
+    mod = importlib.util.module_from_spec(spec)
+    src = open(spec.origin).read().replace('LIB_PATH = os.path.join(_PKG, "libfos.so")',
+                                           f'LIB_PATH = {str(tmp_path / "missing.so")!r}')
+    with pytest.raises(ImportError):
+        exec(compile(src, spec.origin, "exec"), mod.__dict__)
