@@ -64,7 +64,7 @@ class fos_nvfp4_tensor(ctypes.Structure):
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(
-            f"{LIB_PATH} is missing: build it with `python -m adaptive_quantization_fos_b300.build` "
+            f"{LIB_PATH} is missing: build it with `python adaptive_quantization_fos_b300/build.py` "
             "(there is no CPU fallback)")
     L = ctypes.CDLL(LIB_PATH)
     vp, i64, u64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_int32, ctypes.c_size_t

@@ -1,6 +1,8 @@
 """Build libfos.so (the CUDA library behind include/fos.h) for sm_103a.
 
-    python -m adaptive_quantization_fos_b300.build [--verbose]
+    python adaptive_quantization_fos_b300/build.py [--verbose] [--force]
+
+(run by path: importing the package itself needs the built library).
 
 nvcc cross-compiles without a GPU.  Objects go to _build/ at the repo root;
 the shared library is written next to this file.
