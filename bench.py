@@ -1,0 +1,548 @@
+#!/usr/bin/env python
+"""Benchmark of the Four Over Six NVFP4 hot path on B300.
+
+Headline: NVFP4 4/6 quantization throughput (Gelem/s, and the HBM GB/s of the
+quantize kernel against the measured copy bandwidth) on the weight set of one
+Qwen3-8B decoder layer (q, k, v, o, gate, up, down: 192.9M bf16 values,
+Student-t nu = 4, std 0.02), 1D 16-value blocks, round-to-nearest-even.  One
+step quantizes all seven matrices through the public C-ABI call (the amax
+pass and the quantize pass).  The step's inputs (386 MB) are larger than the
+126 MB L2, so every matrix is evicted before it is read again.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fos|reference]
+
+Under torchrun (N > 1) every rank quantizes its own copy of the weight set
+(weak scaling, no data-path collective); the timing takes the max over ranks.
+`--impl reference` times the CPU oracle (test infrastructure) on a bounded
+sample of the same workload, on the host cores, on rank 0 only.
+
+Secondary measurements (same JSON line): the activation (RHT, row-major and
+transposed), gradient (stochastic rounding, 1D and 2D) and linear-layer
+(quantize + NVFP4 GEMM) workloads, and an end-to-end number with host
+buffers.  `--case NAME` runs one small case for profiling instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "NVFP4 4/6 quantize Gelem/s + HBM GB/s (% of peak); NVFP4 GEMM TFLOP/s"
+WORKLOAD = ("qwen3-8b layer weights q,k,v,o,gate,up,down (192.9M bf16 values, Student-t nu=4 std 0.02); "
+            "NVFP4 4/6, 1D 16-value blocks, RNE, swizzled 128x4 scales")
+BYTES_PER_ELEM_QUANT = 2.0 + 0.5 + 1.0 / 16.0  # read bf16, write 4-bit code + 1/16 E4M3 scale
+BYTES_PER_ELEM_AMAX = 2.0
+CPU_SAMPLE_ROWS = 2048  # rows of each matrix timed on the host for the CPU baseline
+REF_SAMPLE_ROWS = 256  # rows of each matrix per step of the reference arm
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "quant_rows_kernel_traffic.txt")
+
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    """Hash of the sources of the quantize kernel (to tell whether a recorded
+    DRAM-traffic figure still belongs to the current kernel)."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in ("fos_quant.cu", "fos_device.cuh"):
+        with open(os.path.join(ROOT, "adaptive_quantization_fos_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic_per_elem() -> float | None:
+    """DRAM bytes per value of the quantize kernel from the committed ncu
+    summary, or None when it was taken on other kernel sources."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    kv = {}
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            if "=" in line and not line.startswith("#"):
+                k, v = line.strip().split("=", 1)
+                kv[k.strip()] = v.strip()
+    if kv.get("source_sha") != kernel_source_hash():
+        return None
+    try:
+        return float(kv["dram_bytes_per_value"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """Samples the SM clock and the clock-event reasons through NVML (the
+    driver's libnvidia-ml, via ctypes) while the timed region runs."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+               0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, device_index: int, period_s: float = 0.005):
+        import ctypes
+
+        self.period = period_s
+        self.samples: list[tuple[int, int]] = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._ok = False
+        self.err = ""
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit failed")
+            self.nv = nv
+            self.h = ctypes.c_void_p()
+            if not self._handle_by_bus(device_index) and nv.nvmlDeviceGetHandleByIndex_v2(
+                    self._nvml_index(device_index), ctypes.byref(self.h)) != 0:
+                raise RuntimeError("no NVML handle")
+            v = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(self.h, self.NVML_CLOCK_SM, ctypes.byref(v)) == 0:
+                self.max_mhz = v.value
+            self._reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self._ok = True
+        except Exception as e:  # noqa: BLE001
+            self.err = str(e)
+
+    def _handle_by_bus(self, idx) -> bool:
+        import ctypes
+
+        try:
+            import torch
+
+            pr = torch.cuda.get_device_properties(idx)
+            bus = "%08X:%02X:%02X.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+            return self.nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h)) == 0
+        except Exception:  # noqa: BLE001
+            return False
+
+    @staticmethod
+    def _nvml_index(idx: int) -> int:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        parts = [p for p in vis.split(",") if p.strip()]
+        if idx < len(parts) and parts[idx].strip().isdigit():
+            return int(parts[idx])
+        return idx
+
+    def _run(self):
+        import ctypes
+
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, self.NVML_CLOCK_SM, ctypes.byref(clk)) == 0 and \
+                    self._reasons_fn(self.h, ctypes.byref(rs)) == 0:
+                self.samples.append((clk.value, rs.value))
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self._ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self._ok:
+            self._stop.set()
+            self.t.join()
+
+    def summary(self) -> dict:
+        if not self._ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "note": self.err or "no samples"}
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        return {"sm_mhz": statistics.median(s for s, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": [n for b, n in self.REASONS.items() if bits & b and n != "gpu_idle"],
+                "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------ distributed
+
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend: str):
+        if self.world > 1:
+            import torch.distributed as dist
+
+            kw = {}
+            if backend == "nccl":
+                import torch
+
+                kw["device_id"] = torch.device("cuda", self.local_rank)
+            dist.init_process_group(backend, **kw)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float, device) -> float:
+        if not self.pg:
+            return v
+        import torch
+
+        t = torch.tensor([v], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------ CPU oracle
+
+
+def cpu_oracle_rate(mats: dict, rows_per_matrix: int) -> tuple[float, str, float]:
+    """Time the oracle on the first `rows_per_matrix` rows of each matrix."""
+    import oracle
+
+    oracle.build()
+    n = 0
+    t0 = time.perf_counter()
+    for bits in mats.values():
+        sub = np.ascontiguousarray(bits[:rows_per_matrix])
+        oracle.quantize(sub)
+        n += sub.size
+    dt = time.perf_counter() - t0
+    sample = f"first {rows_per_matrix} rows of each of the 7 matrices ({n / 1e6:.1f}M values), 1 thread"
+    return n / dt / 1e9, sample, dt
+
+
+# ---------------------------------------------------------------- fos arm
+
+
+def _events(torch, n):
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def _to_dev(torch, bits, dev):
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def run_fos(args, dist: Dist) -> None:
+    import torch
+
+    import adaptive_quantization_fos_b300 as fos
+
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    dist.init("nccl")
+    stream = torch.cuda.current_stream()
+    pk = peaks()
+
+    mats_np = workloads.qwen3_8b_weights()
+    mats = {k: _to_dev(torch, v, dev) for k, v in mats_np.items()}
+    qs = {k: fos.Quantizer(*v.shape, device=dev) for k, v in mats.items()}
+    elems = sum(v.numel() for v in mats.values())
+    launches_per_step = 0
+    for k in qs:
+        r, c = mats[k].shape
+        launches_per_step += 2 + (1 if (r % 128 or (c // 16) % 4) else 0)
+
+    def step():
+        for k, q in qs.items():
+            q(mats[k])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    e0, e1 = _events(torch, 2)
+    dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    dist.barrier()
+    t_ms = dist.max(e0.elapsed_time(e1), dev)
+    ms_per_step = t_ms / args.steps
+    value = dist.world * elems * args.steps / (t_ms * 1e-3) / 1e9
+
+    # the dominant kernel alone: the quantize pass with the amax supplied, one
+    # event pair per launch, cycling over all seven matrices (L2 evicted)
+    amax = {k: fos.tensor_amax(v) for k, v in mats.items()}
+    qk = {k: fos.Quantizer(*v.shape, device=dev, tensor_amax=amax[k]) for k, v in mats.items()}
+    reps = max(3, min(args.steps, 50))
+    for k in mats:
+        qk[k](mats[k])
+    torch.cuda.synchronize()
+    ev = _events(torch, 2 * reps * len(mats))
+    i = 0
+    for _ in range(reps):
+        for k in mats:
+            ev[i].record(stream)
+            qk[k](mats[k])
+            ev[i + 1].record(stream)
+            i += 2
+    torch.cuda.synchronize()
+    tot_t = sum(ev[j].elapsed_time(ev[j + 1]) for j in range(0, len(ev), 2))
+    n_launch = reps * len(mats)
+    achieved = elems * reps * BYTES_PER_ELEM_QUANT / (tot_t * 1e-3) / 1e9
+    tpe = recorded_traffic_per_elem()
+    roofline = {"bound": "hbm", "kernel": "quant_rows_kernel (4/6, RNE, 1D)", "achieved": round(achieved, 1),
+                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                "peak_source": pk["source"] + " copy bandwidth (hbm_gbs), burst",
+                "bytes_per_elem": BYTES_PER_ELEM_QUANT,
+                "traffic": None if tpe is None else round(tpe * elems / len(mats)),
+                "traffic_note": "DRAM read+write bytes per launch (average over the 7 launches), scaled from the "
+                                "committed ncu capture by values processed" if tpe else "no current capture",
+                "algorithmic_bytes_per_launch": round(BYTES_PER_ELEM_QUANT * elems / len(mats)),
+                "avg_launch_us": round(tot_t / n_launch * 1e3, 2)}
+
+    out = {"metric": METRIC, "value": round(value, 2), "unit": "Gelem/s", "n_gpus": dist.world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+           "data": "synthetic",
+           "config": {"workload": WORKLOAD, "elements_per_step": elems, "input_bytes_per_step": 2 * elems,
+                      "l2": "inputs larger than L2 (386 MB per step, 126 MB L2)",
+                      "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "single GPU",
+                      "step_two_pass_gbs": round(elems * (BYTES_PER_ELEM_QUANT + BYTES_PER_ELEM_AMAX) /
+                                                 (ms_per_step * 1e-3) / 1e9, 1)},
+           "roofline": roofline, "gpu_launches": launches_per_step * args.steps, "clocks": clk.summary()}
+
+    if not args.no_extras and dist.rank == 0:
+        out["e2e"] = e2e_host_buffers(torch, fos, mats_np, dev, max(2, min(args.steps, 5)))
+        out["secondary"] = secondary(torch, fos, dev, pk)
+    if dist.rank == 0 and dist.world == 1 and not args.no_extras:
+        rate, sample, secs = cpu_oracle_rate(mats_np, CPU_SAMPLE_ROWS)
+        out["cpu_baseline"] = {"value": round(rate, 6), "unit": "Gelem/s", "cores": 1, "kind": "oracle",
+                               "sample": sample, "seconds": round(secs, 2)}
+    if dist.rank == 0:
+        print(json.dumps(out), flush=True)
+    dist.close()
+
+
+def e2e_host_buffers(torch, fos, mats_np, dev, steps) -> dict:
+    """Same metric through the public API with host buffers: per step, copy the
+    inputs host->device from pinned memory, quantize, copy codes, scales and
+    tensor scales back to pinned host memory."""
+    host_in = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory() for k, v in mats_np.items()}
+    dev_in = {k: torch.empty(v.shape, dtype=torch.bfloat16, device=dev) for k, v in host_in.items()}
+    qs = {k: fos.Quantizer(*v.shape, device=dev) for k, v in host_in.items()}
+    host_out = {}
+    for k, q in qs.items():
+        o = q.out
+        host_out[k] = (torch.empty(o.codes.shape, dtype=torch.uint8).pin_memory(),
+                       torch.empty(o.sf.shape, dtype=torch.uint8).pin_memory(),
+                       torch.empty(1, dtype=torch.float32).pin_memory())
+    h2d = sum(v.numel() * 2 for v in host_in.values())
+    d2h = sum(a.numel() + b.numel() + 4 for a, b, _ in host_out.values())
+
+    def step():
+        for k, q in qs.items():
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+            o = q(dev_in[k])
+            a, b, c = host_out[k]
+            a.copy_(o.codes, non_blocking=True)
+            b.copy_(o.sf, non_blocking=True)
+            c.copy_(o.tensor_scale, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    e0, e1 = _events(torch, 2)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) * 1e-3
+    elems = sum(v.numel() for v in host_in.values())
+    return {"value": round(elems * steps / t / 1e9, 3), "unit": "Gelem/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def _time_calls(torch, fn, reps: int) -> float:
+    """Average ms per call of fn over reps (after one warm-up call)."""
+    fn()
+    torch.cuda.synchronize()
+    e0, e1 = _events(torch, 2)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def secondary(torch, fos, dev, pk) -> dict:
+    res = {}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > L2, written between calls
+
+    def measure(name, bits, reps=10, **opts):
+        x = _to_dev(torch, bits, dev)
+        q = fos.Quantizer(*x.shape, device=dev, **opts)
+
+        def call():
+            flush.fill_(1)
+            q(x)
+
+        t_flush = _time_calls(torch, lambda: flush.fill_(1), reps)
+        t = _time_calls(torch, call, reps) - t_flush
+        n = x.numel()
+        res[name] = {"ms": round(t, 4), "gelem_s": round(n / (t * 1e-3) / 1e9, 2),
+                     "two_pass_gbs": round(n * (BYTES_PER_ELEM_QUANT + BYTES_PER_ELEM_AMAX) / (t * 1e-3) / 1e9, 1),
+                     "shape": list(x.shape), "options": {k: v for k, v in opts.items() if k != "tensor_amax"}}
+
+    act = workloads.activations(16384, 4096, seed=3001)
+    measure("activation_rht_rowmajor", act, hadamard=True, hadamard_seed=3002)
+    measure("activation_rht_transposed", act, hadamard=True, hadamard_seed=3002, transpose=True)
+    del act
+    grad = workloads.gradients(8192, 12288, seed=4001)
+    measure("gradient_sr_1d", grad, rounding=fos.FOS_ROUND_STOCHASTIC, sr_seed=4002)
+    measure("gradient_sr_2d", grad, rounding=fos.FOS_ROUND_STOCHASTIC, sr_seed=4002, block_2d=True)
+    measure("gradient_rne_2d", grad, block_2d=True)
+    del grad
+    res["linear_forward"] = linear_forward(torch, fos, dev, pk)
+    return res
+
+
+def linear_forward(torch, fos, dev, pk) -> dict:
+    """Quantize A (8192 x 4096 activations) and W (12288 x 4096 weights) with
+    4/6 1D RNE, then C = A W^T in NVFP4 on the tensor cores."""
+    A = _to_dev(torch, workloads.activations(8192, 4096, seed=5001), dev)
+    W = _to_dev(torch, workloads.student_t(12288, 4096, seed=5002), dev)
+    qa, qw = fos.Quantizer(*A.shape, device=dev), fos.Quantizer(*W.shape, device=dev)
+    a, w = qa(A), qw(W)
+    C = torch.empty((8192, 12288), dtype=torch.bfloat16, device=dev)
+    try:
+        fos.gemm(a, w, out=C)
+    except fos.FosError as e:
+        return {"status": f"gemm unavailable: {e}"}
+    flops = 2.0 * 8192 * 12288 * 4096
+    t = _time_calls(torch, lambda: fos.gemm(a, w, out=C), 20)
+    tf = flops / (t * 1e-3) / 1e12
+    fp4_peak = pk["bf16_tflops"] * 6.0  # measured bf16 burst x nominal dense fp4/bf16 ratio (13.5 / 2.25)
+    return {"gemm_ms": round(t, 4), "tflops": round(tf, 1),
+            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+                         "frac": round(tf / fp4_peak, 4),
+                         "peak_source": "measured bf16 burst x 6 (nominal dense fp4/bf16 ratio)"}}
+
+
+# ---------------------------------------------------------- reference arm
+
+
+def run_reference(args, dist: Dist) -> None:
+    if dist.rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    mats_np = workloads.qwen3_8b_weights()
+    subs = {k: np.ascontiguousarray(v[:REF_SAMPLE_ROWS]) for k, v in mats_np.items()}
+    n = sum(v.size for v in subs.values())
+
+    def step():
+        for v in subs.values():
+            oracle.quantize(v)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt / 1e9
+    sample = f"first {REF_SAMPLE_ROWS} rows of each of the 7 matrices per step ({n / 1e6:.2f}M values), 1 thread"
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "Gelem/s", "n_gpus": dist.world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+           "config": {"workload": WORKLOAD, "elements_per_step": n, "l2": "host run (no GPU)"},
+           "cpu_baseline": {"value": round(value, 6), "unit": "Gelem/s", "cores": 1, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(value, 6), "unit": "Gelem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------ profiling
+
+
+def run_case(args) -> None:
+    """One small case for ncu: a few launches of one kernel, nothing else timed."""
+    import torch
+
+    import adaptive_quantization_fos_b300 as fos
+
+    dev = torch.device("cuda", 0)
+    if args.case == "quant_rows":
+        # 12288 x 8192 bf16 (201 MB > L2), amax supplied: only the quantize kernel runs
+        x = _to_dev(torch, workloads.student_t(12288, 8192, seed=9001), dev)
+        amax = fos.tensor_amax(x)
+        q = fos.Quantizer(*x.shape, device=dev, tensor_amax=amax)
+        for _ in range(3):
+            q(x)
+    elif args.case == "gemm":
+        A = _to_dev(torch, workloads.activations(8192, 4096, seed=5001), dev)
+        W = _to_dev(torch, workloads.student_t(12288, 4096, seed=5002), dev)
+        a = fos.quantize(A)
+        w = fos.quantize(W)
+        C = torch.empty((8192, 12288), dtype=torch.bfloat16, device=dev)
+        for _ in range(3):
+            fos.gemm(a, w, out=C)
+    else:
+        raise SystemExit(f"unknown case {args.case}")
+    torch.cuda.synchronize()
+    print(f"case {args.case} done")
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["fos", "reference"], default="fos")
+    ap.add_argument("--no-extras", action="store_true", help="headline only (no e2e, secondary, CPU baseline)")
+    ap.add_argument("--case", default=None, help="run one small profiling case instead of the benchmark")
+    args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    dist = Dist()
+    if args.gpus != dist.world and dist.world > 1:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE {dist.world}")
+    if args.impl == "reference":
+        run_reference(args, dist)
+    else:
+        run_fos(args, dist)
+
+
+if __name__ == "__main__":
+    main()
