@@ -76,6 +76,8 @@ def _load() -> ctypes.CDLL:
         "fos_tensor_amax": (i32, [vp, i64, i64, i64, i32, i32, u64, vp, vp, sz, vp]),
         "fos_quantize": (i32, [vp, i64, i64, i64, ctypes.POINTER(fos_quant_options), vp, i64, vp, vp, vp, vp, sz,
                                vp]),
+        "fos_quantize_noalloc": (i32, [vp, i64, i64, i64, ctypes.POINTER(fos_quant_options), vp, i64, vp, vp, vp,
+                                       vp]),
         "fos_dequantize": (i32, [ctypes.POINTER(fos_nvfp4_tensor), vp, i32, i64, vp]),
         "fos_gemm": (i32, [ctypes.POINTER(fos_nvfp4_tensor), ctypes.POINTER(fos_nvfp4_tensor), vp, i64, vp, vp]),
         "fos_e2m1_encode": (i32, [vp, i64, vp, vp]),
@@ -91,7 +93,7 @@ def _load() -> ctypes.CDLL:
 
 _lib = _load()
 EXPORTED = ("fos_abi_version", "fos_status_string", "fos_sf_bytes", "fos_quantize_workspace_size",
-            "fos_tensor_amax", "fos_quantize", "fos_dequantize", "fos_gemm", "fos_e2m1_encode",
+            "fos_tensor_amax", "fos_quantize", "fos_quantize_noalloc", "fos_dequantize", "fos_gemm", "fos_e2m1_encode",
             "fos_e4m3_encode", "fos_philox4x32_10")
 
 
@@ -125,6 +127,13 @@ def fos_quantize(x, rows, cols, ld_x, opt, codes, ld_codes, sf, tensor_scale, ch
     """Raw call: all buffer arguments are integer device addresses (0 = NULL)."""
     return int(_lib.fos_quantize(x, rows, cols, ld_x, ctypes.byref(opt), codes, ld_codes, sf, tensor_scale,
                                  choice or None, workspace or None, workspace_bytes, stream))
+
+
+def fos_quantize_noalloc(x, rows, cols, ld_x, opt, codes, ld_codes, sf, tensor_scale, choice, stream) -> int:
+    """Raw call of the entry point that needs no workspace (for callers that
+    cannot allocate device memory); buffers are integer device addresses."""
+    return int(_lib.fos_quantize_noalloc(x, rows, cols, ld_x, ctypes.byref(opt), codes, ld_codes, sf, tensor_scale,
+                                         choice or None, stream))
 
 
 def fos_tensor_amax(x, rows, cols, ld_x, hadamard, transpose, hadamard_seed, amax_out, workspace,

@@ -159,6 +159,26 @@ fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
                         cudaStream_t stream);
 
 /*
+ * fos_quantize_noalloc -- fos_quantize for callers that cannot allocate
+ * device memory (plugin hosts and inference runtimes that give an operator
+ * only its inputs and outputs and forbid cudaMalloc after start-up).  The
+ * pages have no counterpart; this is a library convenience.  Same arguments,
+ * results and validation as fos_quantize, minus the workspace: the amax
+ * pass's partial maxima go to a fixed 8 KiB array in device memory owned by
+ * the library (held on every GPU that loads it until the process exits).
+ *   - The first call on a device looks up the array's address; make it
+ *     before any stream capture.
+ *   - All calls share the array: calls that overlap on the GPU race on it.
+ *     Nothing in it needs clearing between calls.
+ *   - A call whose scratch need exceeds the array returns FOS_ERR_INVALID_ARG
+ *     (with the current kernels every call that fos_quantize accepts fits).
+ *   - Allocates nothing and calls no allocating routine.
+ */
+fos_status fos_quantize_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                const fos_quant_options* opt, uint8_t* codes, int64_t ld_codes, uint8_t* sf,
+                                float* tensor_scale, uint8_t* choice, cudaStream_t stream);
+
+/*
  * fos_dequantize -- x_hat = g * (float(sf) * s_t), each product rounded to FP32;
  * out_dtype FOS_DTYPE_F32, or FOS_DTYPE_BF16 (the FP32 value rounded to
  * nearest even).  out: device [q->rows][ld_out] elements.
