@@ -1,26 +1,537 @@
-// Block-scaled NVFP4 GEMM (tcgen05) -- argument validation; the kernel follows.
+// Block-scaled NVFP4 GEMM on the fifth-generation tensor cores (sm_103a).
+//
+// C[m][n] = bf16( (s_tA * s_tB) * sum_k (gA[m,k] sfA[m,k/16]) (gB[n,k] sfB[n,k/16]) )
+//
+// This is the contraction of the quantized linear layer: "FP4" (Ultralytics
+// glossary), "FP4 ile Çıkarım ve Eğitim", notes that FP4 matrix products
+// accumulate at higher precision; here the products and the FP32 accumulation
+// run in tcgen05.mma kind::mxf4nvf4 (E2M1 operands, one E4M3 scale per 16
+// values along K, "scale_vec::4X"), with the accumulator in tensor memory.
+//
+// Structure (one persistent CTA per SM, static round-robin over output tiles):
+//   warp 0      TMA producer: codes of A (128 x 256 values) and B (BN x 256)
+//               per stage with 128-byte swizzle, plus the stage's scale bytes
+//               (contiguous 512-byte chunks of the 128x4 layout) by bulk copy.
+//   warp 1      allocates tensor memory; one thread copies each stage's scale
+//               chunks into tensor memory (tcgen05.cp 32x128b.warpx4) and
+//               issues 4 MMAs of K = 64 per stage; tcgen05.commit frees the
+//               stage and, after the last stage, signals the accumulator.
+//   warps 2..   epilogue: each warp reads 32 accumulator lanes x 128 columns
+//               into registers, hands the accumulator back at once (so the
+//               next tile's MMAs start while it stores), scales, rounds to
+//               bf16 and stores.
+// Every mbarrier wait is bounded (globaltimer); on expiry the kernel records
+// FOS_ERR_TIMEOUT, all roles stop, in-flight copies and MMAs are drained
+// (again bounded) and the tensor memory is freed before the CTA exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
 #include <cstdint>
+#include <mutex>
 
 #include "fos.h"
 
 namespace {
+
+// ------------------------------------------------------------ constants
+constexpr int kBM = 128;              // rows of A per tile (= tensor-memory lanes)
+constexpr int kBKBytes = 128;         // codes bytes per row per stage (256 values)
+constexpr int kKPerMma = 64;          // values of K per MMA
+constexpr int kSfChunk = 512;         // scale bytes of 128 rows x 64 values
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
+
+template <int BN>
+struct Cfg {
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kABytes = kBM * kBKBytes;
+  static constexpr int kBBytes = BN * kBKBytes;
+  static constexpr int kSfaBytes = 4 * kSfChunk;
+  static constexpr int kSfbBytes = (BN / 128) * 4 * kSfChunk;
+  static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+  static constexpr int kEpiWarps = 4 * (BN / 128);
+  static constexpr int kThreads = 32 * (2 + kEpiWarps);
+  // tensor-memory columns: accumulator, then per stage 4 MMAs x (4 + BN/32)
+  static constexpr int kSfaCols = 16;
+  static constexpr int kSfbColsPerMma = BN / 32;
+  static constexpr int kSfStageCols = kSfaCols + 4 * kSfbColsPerMma;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
+  static_assert(kStageBytes % 1024 == 0, "stage buffers stay 1024-byte aligned");
+  static_assert(BN + kStages * kSfStageCols <= (int)kTmemCols, "tensor memory budget");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+struct GemmArgs {
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  const float* sta;
+  const float* stb;
+  uint16_t* c;
+  int64_t ldc;
+  int32_t m, n, k;       // k in values
+  int32_t tiles_m, tiles_n, num_kb;
+  int64_t sf_ktiles;     // 512-byte scale chunks per 128-row tile (= K / 64)
+  int32_t* status;
+  uint64_t timeout_ns;
+  int32_t stall_test;    // 1: the producer never fills a stage (bounded-wait self test)
+};
+
+// ------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete.  Gives up (returns
+// false) when the wait outlasts timeout_ns or, if abort is not null, when
+// another role has raised *abort.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                          volatile int* abort) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try(bar, parity)) return true;
+    if ((i & 15u) == 0) {
+      if (abort && *abort) return false;
+      if (globaltimer() - t0 > timeout_ns) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start >> 4 in bits 0-13, leading
+// byte offset >> 4 in 16-29, stride byte offset >> 4 in 32-45, the fixed
+// version 1 in 46-47, swizzle mode in 61-63 (2 = 128-byte, 0 = none).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t swizzle) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(sbo >> 4) << 32) |
+         (1ull << 46) | ((uint64_t)swizzle << 61);
+}
+
+// Instruction descriptor of kind::mxf4nvf4: E2M1 A and B (format 1), both
+// K-major, E4M3 scales (scale format 0), N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t mma_idesc(int m, int n) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
+// 32 lanes x 32 columns of 32-bit accumulator -> 32 registers per thread.
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&v)[32], int off) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+        "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr + off));
+}
+
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void raise_timeout(const GemmArgs& a, volatile int* abort) {
+  *abort = 1;
+  if (a.status) atomicExch(a.status, (int)FOS_ERR_TIMEOUT);
+}
+
+// ------------------------------------------------------------------ kernel
+template <int BN>
+__global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
+    gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                      const GemmArgs args) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  // bars[0, S): stage full; [S, 2S): stage empty; 2S: acc full; 2S+1: acc empty; 2S+2: drain
+  volatile int* abort = reinterpret_cast<volatile int*>(bars + 2 * C::kStages + 3);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (C::kStages + s); };
+  const uint32_t acc_full = bar0 + 8u * (2 * C::kStages);
+  const uint32_t acc_empty = acc_full + 8u;
+  const uint32_t drain_bar = acc_full + 16u;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, C::kEpiWarps);
+    mbar_init(drain_bar, 1);
+    *abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int n_tiles = args.tiles_m * args.tiles_n;
+  const int kmma_total = args.k / kKPerMma;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+        const int mb = t % args.tiles_m, nb = t / args.tiles_m;
+        for (int kb = 0; kb < args.num_kb; ++kb) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, args.timeout_ns, abort)) {
+            raise_timeout(args, abort);
+            ok = false;
+            break;
+          }
+          if (!args.stall_test) {
+            const int kkc = min(4, kmma_total - 4 * kb);
+            uint32_t tx = C::kABytes + C::kBBytes + kkc * kSfChunk;
+            int halves = 0;
+            for (int h = 0; h < BN / 128; ++h)
+              if ((nb * (BN / 128) + h) * 128 < args.n) ++halves;
+            tx += halves * kkc * kSfChunk;
+            const uint32_t st = smem_u32(smem + s * C::kStageBytes);
+            mbar_expect_tx(full_bar(s), tx);
+            tma_load_2d(st, &tm_a, kb * kBKBytes, mb * kBM, full_bar(s));
+            tma_load_2d(st + C::kABytes, &tm_b, kb * kBKBytes, nb * BN, full_bar(s));
+            const uint32_t sfa_dst = st + C::kABytes + C::kBBytes;
+            bulk_load(sfa_dst, args.sfa + ((int64_t)mb * args.sf_ktiles + 4 * kb) * kSfChunk, kkc * kSfChunk,
+                      full_bar(s));
+            for (int h = 0; h < halves; ++h)
+              bulk_load(sfa_dst + C::kSfaBytes + h * 4 * kSfChunk,
+                        args.sfb + ((int64_t)(nb * (BN / 128) + h) * args.sf_ktiles + 4 * kb) * kSfChunk,
+                        kkc * kSfChunk, full_bar(s));
+            ++issued;
+          }
+          if (++s == C::kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // let the copies in flight land before the CTA can exit (bounded)
+      if (!ok) {
+        for (int j = 0; j < C::kStages && j < issued; ++j) {
+          if (--s < 0) {
+            s = C::kStages - 1;
+            ph ^= 1u;
+          }
+          mbar_wait(full_bar(s), ph, args.timeout_ns, nullptr);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = mma_idesc(kBM, BN);
+      const uint32_t acc = tmem;
+      int s = 0;
+      uint32_t ph = 0, acc_ph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+        if (!mbar_wait(acc_empty, acc_ph ^ 1u, args.timeout_ns, abort)) {
+          raise_timeout(args, abort);
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < args.num_kb; ++kb) {
+          if (!mbar_wait(full_bar(s), ph, args.timeout_ns, abort)) {
+            raise_timeout(args, abort);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int kkc = min(4, kmma_total - 4 * kb);
+          const uint32_t st = smem_u32(smem + s * C::kStageBytes);
+          const uint32_t sfa_s = st + C::kABytes + C::kBBytes, sfb_s = sfa_s + C::kSfaBytes;
+          const uint32_t sf_col = tmem + BN + s * C::kSfStageCols;
+          for (int kk = 0; kk < kkc; ++kk) {
+            tc_cp_sf(sf_col + 4 * kk, smem_desc(sfa_s + kk * kSfChunk, 128, 128, 0));
+#pragma unroll
+            for (int h = 0; h < BN / 128; ++h)
+              tc_cp_sf(sf_col + C::kSfaCols + C::kSfbColsPerMma * kk + 4 * h,
+                       smem_desc(sfb_s + h * 4 * kSfChunk + kk * kSfChunk, 128, 128, 0));
+          }
+          const uint64_t adesc = smem_desc(st, 16, 1024, 2);
+          const uint64_t bdesc = smem_desc(st + C::kABytes, 16, 1024, 2);
+          for (int kk = 0; kk < kkc; ++kk) {
+            // +32 bytes of K per MMA inside the 128-byte swizzle atom
+            tc_mma(acc, adesc + 2 * kk, bdesc + 2 * kk, idesc, sf_col + 4 * kk,
+                   sf_col + C::kSfaCols + C::kSfbColsPerMma * kk, (kb | kk) != 0);
+          }
+          tc_commit(empty_bar(s));
+          if (++s == C::kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(acc_full);
+        acc_ph ^= 1u;
+      }
+      // all MMAs and copies issued so far complete before the memory is freed
+      tc_commit(drain_bar);
+      mbar_wait(drain_bar, 0, args.timeout_ns, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------ epilogue
+    const int q = warp & 3;                    // tensor-memory lane quadrant of this warp
+    const int h = (warp - 2) / 4;              // which 128-column half of the tile
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + 128 * h;
+    const float alpha = __fmul_rn(__ldg(args.sta), __ldg(args.stb));
+    uint32_t acc_ph = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+      const int mb = t % args.tiles_m, nb = t / args.tiles_m;
+      // one lane waits and the warp follows its verdict, so the warp stays
+      // converged for the .sync.aligned tensor-memory loads
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(acc_full, acc_ph, args.timeout_ns, abort) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) {
+        if (lane == 0) raise_timeout(args, abort);
+        break;
+      }
+      tc_fence_after();
+      uint32_t v[4][32];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) tc_ld32(lane_base, v[j], 32 * j);
+      tc_wait_ld();
+      // the loaded registers are valid only after the wait: tie every use to it
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(v[j][i]));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+      acc_ph ^= 1u;
+
+      const int row = mb * kBM + 32 * q + lane;
+      const int col0 = nb * BN + 128 * h;
+      if (row < args.m) {
+        uint16_t* dst = args.c + (int64_t)row * args.ldc + col0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int col = col0 + 32 * j + 8 * g;
+            if (col < args.n) {
+              uint4 o;
+              o.x = pack_bf16x2(__fmul_rn(__uint_as_float(v[j][8 * g + 0]), alpha),
+                                __fmul_rn(__uint_as_float(v[j][8 * g + 1]), alpha));
+              o.y = pack_bf16x2(__fmul_rn(__uint_as_float(v[j][8 * g + 2]), alpha),
+                                __fmul_rn(__uint_as_float(v[j][8 * g + 3]), alpha));
+              o.z = pack_bf16x2(__fmul_rn(__uint_as_float(v[j][8 * g + 4]), alpha),
+                                __fmul_rn(__uint_as_float(v[j][8 * g + 5]), alpha));
+              o.w = pack_bf16x2(__fmul_rn(__uint_as_float(v[j][8 * g + 6]), alpha),
+                                __fmul_rn(__uint_as_float(v[j][8 * g + 7]), alpha));
+              *reinterpret_cast<uint4*>(dst + 32 * j + 8 * g) = o;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- host side
+namespace {
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 bool valid_operand(const fos_nvfp4_tensor* t) {
   if (!t || !t->codes || !t->sf || !t->tensor_scale) return false;
-  if (t->rows < 0 || t->cols <= 0 || t->cols % 256 != 0) return false;
+  if (t->rows < 0 || t->rows > INT32_MAX || t->cols <= 0 || t->cols % kKPerMma != 0 || t->cols > INT32_MAX)
+    return false;
   if (t->ld_codes < t->cols / 2 || t->ld_codes % 16 != 0 || !aligned(t->codes, 16) || !aligned(t->sf, 16))
     return false;
   return t->sf_layout == FOS_SF_SWIZZLED_128x4;
 }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Row-major u8 matrix [rows][row_bytes] (stride ld bytes), box 128 bytes x
+// box_rows rows, 128-byte swizzle (the K-major layout the MMA descriptors name).
+bool make_codes_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes, int64_t ld,
+                    uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld};
+  cuuint32_t box[2] = {(cuuint32_t)kBKBytes, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                                 cudaSuccess)
+    return 148;
+  return n > 0 ? n : 148;
+}
+
+template <int BN>
+fos_status launch_gemm(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* Cout, int64_t ldc,
+                       int32_t* dev_status, uint64_t timeout_ns, int stall_test, int grid_cap, cudaStream_t stream) {
+  using C = Cfg<BN>;
+  CUtensorMap ta, tb;
+  const int64_t kbytes = A->cols / 2;
+  if (!make_codes_map(&ta, A->codes, A->rows, kbytes, A->ld_codes, kBM) ||
+      !make_codes_map(&tb, B->codes, B->rows, kbytes, B->ld_codes, BN))
+    return FOS_ERR_CUDA;
+  GemmArgs a{};
+  a.sfa = A->sf;
+  a.sfb = B->sf;
+  a.sta = A->tensor_scale;
+  a.stb = B->tensor_scale;
+  a.c = static_cast<uint16_t*>(Cout);
+  a.ldc = ldc;
+  a.m = (int32_t)A->rows;
+  a.n = (int32_t)B->rows;
+  a.k = (int32_t)A->cols;
+  a.tiles_m = (int32_t)((A->rows + kBM - 1) / kBM);
+  a.tiles_n = (int32_t)((B->rows + BN - 1) / BN);
+  a.num_kb = (int32_t)((A->cols + 255) / 256);
+  a.sf_ktiles = A->cols / kKPerMma;
+  a.status = dev_status;
+  a.timeout_ns = timeout_ns;
+  a.stall_test = stall_test;
+  const int64_t tiles = (int64_t)a.tiles_m * a.tiles_n;
+  if (tiles > INT32_MAX) return FOS_ERR_INVALID_ARG;
+  int grid = sm_count();
+  if (grid_cap > 0 && grid > grid_cap) grid = grid_cap;
+  if (grid > tiles) grid = (int)tiles;
+  if (cudaFuncSetAttribute(gemm_nvfp4_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+      cudaSuccess)
+    return FOS_ERR_CUDA;
+  gemm_nvfp4_kernel<BN><<<grid, C::kThreads, C::kSmemBytes, stream>>>(ta, tb, a);
+  return cudaGetLastError() == cudaSuccess ? FOS_OK : FOS_ERR_CUDA;
+}
+
+fos_status gemm_checked(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* C, int64_t ldc,
+                        int32_t* dev_status, uint64_t timeout_ns, int stall_test, cudaStream_t stream) {
+  if (!valid_operand(A) || !valid_operand(B) || !C) return FOS_ERR_INVALID_ARG;
+  if (A->cols != B->cols || B->rows % 8 != 0) return FOS_ERR_INVALID_ARG;
+  if (ldc < B->rows || ldc % 8 != 0 || !aligned(C, 16)) return FOS_ERR_INVALID_ARG;
+  if (dev_status && !aligned(dev_status, 4)) return FOS_ERR_INVALID_ARG;
+  if (A->rows == 0 || B->rows == 0) return FOS_OK;
+  // 256-column tiles unless the last one would be half empty
+  if (B->rows % 256 == 0 || B->rows % 256 > 128)
+    return launch_gemm<256>(A, B, C, ldc, dev_status, timeout_ns, stall_test, 0, stream);
+  return launch_gemm<128>(A, B, C, ldc, dev_status, timeout_ns, stall_test, 0, stream);
+}
+
 }  // namespace
 
 extern "C" fos_status fos_gemm(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* C, int64_t ldc,
                                int32_t* dev_status, cudaStream_t stream) {
-  (void)dev_status;
-  (void)stream;
-  if (!valid_operand(A) || !valid_operand(B) || !C) return FOS_ERR_INVALID_ARG;
-  if (A->cols != B->cols || A->rows % 128 != 0 || B->rows % 256 != 0) return FOS_ERR_INVALID_ARG;
-  if (ldc < B->rows || ldc % 8 != 0 || !aligned(C, 16)) return FOS_ERR_INVALID_ARG;
-  return FOS_ERR_UNSUPPORTED;
+  return gemm_checked(A, B, C, ldc, dev_status, kDefaultTimeoutNs, 0, stream);
 }

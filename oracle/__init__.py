@@ -302,6 +302,19 @@ def gemm_rows(A_hat: np.ndarray, W_hat: np.ndarray, rows) -> tuple[np.ndarray, n
     return out, bnd
 
 
+def gemm_rows_matmul(A_hat: np.ndarray, W_hat: np.ndarray, rows) -> tuple[np.ndarray, np.ndarray]:
+    """The same FP64 reference as ``gemm_rows`` -- the FP32-simulation fallback
+    of "Four Over Six" (first section): dequantize, then multiply -- with the
+    K-sums done by numpy's float64 matmul (a library primitive) instead of the
+    plain loop, for full-size shapes where the loop takes minutes.  Each sum is
+    over exact products of FP32 values in FP64, so it agrees with
+    ``gemm_rows`` to FP64 rounding (pinned against it in the CPU tests)."""
+    r = np.asarray(rows, dtype=np.int64)
+    a = np.asarray(A_hat, dtype=np.float32)[r].astype(np.float64)
+    w = np.asarray(W_hat, dtype=np.float32).astype(np.float64)
+    return a @ w.T, np.abs(a) @ np.abs(w).T
+
+
 def mae_nearest_grid(x, block: int) -> float:
     a = np.ascontiguousarray(x, dtype=np.float32)
     assert a.size % block == 0

@@ -102,6 +102,22 @@ def test_gemm_validation(fos):
     assert fos.fos_gemm(A, B, fake, 256, 0, 0) == INVALID  # K differs
     B.cols, B.ld_codes = 256, 128
     assert fos.fos_gemm(A, B, fake, 100, 0, 0) == INVALID  # ldc < N
+    assert fos.fos_gemm(A, B, fake + 8, 256, 0, 0) == INVALID  # C not 16-byte aligned
+    assert fos.fos_gemm(A, B, fake, 260, 0, 0) == INVALID  # ldc % 8
+    B.rows = 250
+    assert fos.fos_gemm(A, B, fake, 256, 0, 0) == INVALID  # N % 8
+    B.rows = 256
+    A.cols = B.cols = 96
+    assert fos.fos_gemm(A, B, fake, 256, 0, 0) == INVALID  # K % 64
+    A.cols = B.cols = 256
+    A.ld_codes = 136
+    assert fos.fos_gemm(A, B, fake, 256, 0, 0) == INVALID  # ld_codes % 16
+    A.ld_codes = 128
+    A.sf_layout = fos.FOS_SF_ROWMAJOR
+    assert fos.fos_gemm(A, B, fake, 256, 0, 0) == INVALID  # the MMA reads the 128x4 layout only
+    A.sf_layout = fos.FOS_SF_SWIZZLED_128x4
+    A.rows = 0
+    assert fos.fos_gemm(A, B, fake, 256, 0, 0) == fos.FOS_OK  # empty: nothing to launch
 
 
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):

@@ -369,6 +369,17 @@ def test_gemm_reference_closed_form(orc):
     assert np.allclose(out, (A.astype(np.float64) @ W.T.astype(np.float64))[[1, 6]], rtol=1e-12, atol=1e-12)
 
 
+def test_gemm_reference_matmul_matches_loop(orc):
+    rng = np.random.default_rng(2)
+    A = (rng.standard_normal((9, 320)) * 3).astype(np.float32)
+    W = rng.standard_t(4, (13, 320)).astype(np.float32)
+    rows = [0, 4, 8]
+    o1, b1 = orc.gemm_rows(A, W, rows)
+    o2, b2 = orc.gemm_rows_matmul(A, W, rows)
+    assert np.allclose(o1, o2, rtol=1e-13, atol=1e-12 * b1.max())
+    assert np.allclose(b1, b2, rtol=1e-13)
+
+
 # ------------------------------------------------- the page's worked example
 
 
