@@ -156,6 +156,7 @@ fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
   p.hk0 = (uint32_t)opt->hadamard_seed;
   p.hk1 = (uint32_t)(opt->hadamard_seed >> 32);
   p.aligned32 = aligned32;
+  p.codes16 = aligned(codes, 16) && ld_codes % 16 == 0;
 
   int kind;
   int64_t tasks;
@@ -167,9 +168,9 @@ fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
     tasks = (rows / 16) * ((cols + 127) / 128);
   } else {
     kind = 0;
-    tasks = R * ((nb + 31) / 32);
+    tasks = R * ((nb + 127) / 128);
   }
-  const int grid = fos::quant_grid(tasks);
+  const int grid = fos::quant_grid(tasks, kind);
   if (fos::launch_quant(p, opt->scale_rule, kind, rht, opt->rounding == FOS_ROUND_STOCHASTIC, grid, stream) !=
       cudaSuccess)
     return FOS_ERR_CUDA;

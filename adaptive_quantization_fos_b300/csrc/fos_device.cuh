@@ -136,6 +136,118 @@ __device__ __forceinline__ uint32_t e2m1x2_residual(float qlo, float qhi, float&
   return byte;
 }
 
+// RNE codes of 8 consecutive values in one word, and their 8 residuals q - g (each exact: g is the nearest grid value or the
+// saturation bound, so the difference is representable).  Byte k of the word
+// holds the codes of q[2k] (low nibble) and q[2k+1].
+__device__ __forceinline__ uint32_t e2m1x8_residual(const float (&q)[8], float (&r)[8]) {
+  uint32_t word;
+  asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\t.reg .b32 h0, h1, h2, h3, t0, t1, u0, u1, u2, u3;\n\t"
+      ".reg .b16 l0, g0, l1, g1, l2, g2, l3, g3, m1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c0, %10, %9;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c1, %12, %11;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c2, %14, %13;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c3, %16, %15;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h0, c0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h1, c1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h2, c2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h3, c3;\n\t"
+      "mov.b32 {l0, g0}, h0;\n\tmov.b32 {l1, g1}, h1;\n\tmov.b32 {l2, g2}, h2;\n\tmov.b32 {l3, g3}, h3;\n\t"
+      "mov.b16 m1, 0xBC00;\n\t"
+      "fma.rn.f32.f16 %1, l0, m1, %9;\n\t"
+      "fma.rn.f32.f16 %2, g0, m1, %10;\n\t"
+      "fma.rn.f32.f16 %3, l1, m1, %11;\n\t"
+      "fma.rn.f32.f16 %4, g1, m1, %12;\n\t"
+      "fma.rn.f32.f16 %5, l2, m1, %13;\n\t"
+      "fma.rn.f32.f16 %6, g2, m1, %14;\n\t"
+      "fma.rn.f32.f16 %7, l3, m1, %15;\n\t"
+      "fma.rn.f32.f16 %8, g3, m1, %16;\n\t"
+      "cvt.u32.u8 u0, c0;\n\tcvt.u32.u8 u1, c1;\n\tcvt.u32.u8 u2, c2;\n\tcvt.u32.u8 u3, c3;\n\t"
+      "prmt.b32 t0, u0, u1, 0x0040;\n\t"
+      "prmt.b32 t1, u2, u3, 0x0040;\n\t"
+      "prmt.b32 %0, t0, t1, 0x5410;\n\t}"
+      : "=r"(word), "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]),
+        "=f"(r[7])
+      : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+  return word;
+}
+
+// ------------------------------------------------ float pairs in 64 bits
+// A value pair (element 2k in the low half) kept in one 64-bit register, the
+// operand form of the packed f32x2 instructions.
+__device__ __forceinline__ uint64_t pack_f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ F2 unpack_f2(uint64_t v) {
+  F2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(v));
+  return d;
+}
+
+// Two bf16 values of one word -> their exact FP32 pair, as x * 1 + (-0) in
+// the mixed-precision FMA (exact for every finite x, signed zeros kept); this
+// keeps the conversion on the FMA pipe, off the busier integer/ALU pipe.
+__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
+  uint64_t r;
+  asm("{\n\t.reg .b16 l, h, one;\n\t.reg .f32 a, b, z;\n\t"
+      "mov.b32 {l, h}, %1;\n\tmov.b16 one, 0x3F80;\n\tmov.f32 z, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 a, l, one, z;\n\tfma.rn.f32.bf16 b, h, one, z;\n\tmov.b64 %0, {a, b};\n\t}"
+      : "=l"(r)
+      : "r"(w));
+  return r;
+}
+
+// One candidate on 8 consecutive values (4 pairs y[k]): q = y * inv (packed),
+// RNE E2M1 codes of q (returned as one word, byte k = codes of pair k), and
+// the squared residuals (q - g)^2 added to the two running sums in acc
+// (even positions in the low half), one packed FMA per pair in pair order.
+__device__ __forceinline__ uint32_t cand_rne8(const uint64_t (&y)[4], uint64_t inv2, uint64_t& acc) {
+  uint32_t word;
+  asm("{\n\t"
+      ".reg .b64 q0, q1, q2, q3, r0, r1, r2, r3;\n\t"
+      ".reg .f32 x0, x1, x2, x3, x4, x5, x6, x7, e0, e1, e2, e3, e4, e5, e6, e7;\n\t"
+      ".reg .b8 c0, c1, c2, c3;\n\t"
+      ".reg .b32 h0, h1, h2, h3, u0, u1, u2, u3, t0, t1;\n\t"
+      ".reg .b16 l0, g0, l1, g1, l2, g2, l3, g3, m1;\n\t"
+      "mul.rn.f32x2 q0, %2, %6;\n\t"
+      "mul.rn.f32x2 q1, %3, %6;\n\t"
+      "mul.rn.f32x2 q2, %4, %6;\n\t"
+      "mul.rn.f32x2 q3, %5, %6;\n\t"
+      "mov.b64 {x0, x1}, q0;\n\tmov.b64 {x2, x3}, q1;\n\tmov.b64 {x4, x5}, q2;\n\tmov.b64 {x6, x7}, q3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c0, x1, x0;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c1, x3, x2;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c2, x5, x4;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c3, x7, x6;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h0, c0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h1, c1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h2, c2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h3, c3;\n\t"
+      "mov.b32 {l0, g0}, h0;\n\tmov.b32 {l1, g1}, h1;\n\tmov.b32 {l2, g2}, h2;\n\tmov.b32 {l3, g3}, h3;\n\t"
+      "mov.b16 m1, 0xBC00;\n\t"
+      "fma.rn.f32.f16 e0, l0, m1, x0;\n\t"
+      "fma.rn.f32.f16 e1, g0, m1, x1;\n\t"
+      "fma.rn.f32.f16 e2, l1, m1, x2;\n\t"
+      "fma.rn.f32.f16 e3, g1, m1, x3;\n\t"
+      "fma.rn.f32.f16 e4, l2, m1, x4;\n\t"
+      "fma.rn.f32.f16 e5, g2, m1, x5;\n\t"
+      "fma.rn.f32.f16 e6, l3, m1, x6;\n\t"
+      "fma.rn.f32.f16 e7, g3, m1, x7;\n\t"
+      "mov.b64 r0, {e0, e1};\n\tmov.b64 r1, {e2, e3};\n\tmov.b64 r2, {e4, e5};\n\tmov.b64 r3, {e6, e7};\n\t"
+      "fma.rn.f32x2 %1, r0, r0, %1;\n\t"
+      "fma.rn.f32x2 %1, r1, r1, %1;\n\t"
+      "fma.rn.f32x2 %1, r2, r2, %1;\n\t"
+      "fma.rn.f32x2 %1, r3, r3, %1;\n\t"
+      "cvt.u32.u8 u0, c0;\n\tcvt.u32.u8 u1, c1;\n\tcvt.u32.u8 u2, c2;\n\tcvt.u32.u8 u3, c3;\n\t"
+      "mad.lo.u32 t0, u1, 256, u0;\n\t"
+      "mad.lo.u32 t1, u3, 256, u2;\n\t"
+      "mad.lo.u32 %0, t1, 65536, t0;\n\t}"
+      : "=r"(word), "+l"(acc)
+      : "l"(y[0]), "l"(y[1]), "l"(y[2]), "l"(y[3]), "l"(inv2));
+  return word;
+}
+
 // Value of each nibble of a code byte as two floats (exact).
 __device__ __forceinline__ F2 e2m1x2_decode(uint32_t byte) {
   uint32_t h;
@@ -187,6 +299,52 @@ __device__ __forceinline__ void ldg128x2(const void* p, uint32_t (&w)[8]) {
   uint4 a = __ldg(q), b = __ldg(q + 1);
   w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
   w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+}
+
+// ------------------------------------------------- mbarrier + bulk copy
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of the given parity; false once timeout_ns have passed.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try(bar, parity)) return true;
+    if ((i & 15u) == 0 && globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
+// Contiguous global -> shared copy on the async (bulk) path; completion is
+// counted in bytes on the mbarrier.  Addresses 16-byte aligned, size % 16 == 0.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
 }
 
 // ------------------------------------------------------------------- RHT
@@ -313,6 +471,58 @@ __device__ __forceinline__ float cand_sr16(const float (&y)[16], float inv, cons
   lo = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
   hi = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
   return __fadd_rn(acc.x, acc.y);
+}
+
+// RNE codes of one candidate for 16 values, from a per-tensor table entry:
+// same arithmetic as cand_rne16, 8 values per conversion group.
+__device__ __forceinline__ float cand_rne16_packed(const float (&y)[16], float inv, uint32_t& lo, uint32_t& hi) {
+  F2 acc{0.0f, 0.0f};
+  float q[8], r[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    F2 t = mul2(F2{y[2 * k], y[2 * k + 1]}, F2{inv, inv});
+    q[2 * k] = t.x;
+    q[2 * k + 1] = t.y;
+  }
+  lo = e2m1x8_residual(q, r);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) acc = fma2(F2{r[2 * k], r[2 * k + 1]}, F2{r[2 * k], r[2 * k + 1]}, acc);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    F2 t = mul2(F2{y[8 + 2 * k], y[9 + 2 * k]}, F2{inv, inv});
+    q[2 * k] = t.x;
+    q[2 * k + 1] = t.y;
+  }
+  hi = e2m1x8_residual(q, r);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) acc = fma2(F2{r[2 * k], r[2 * k + 1]}, F2{r[2 * k], r[2 * k + 1]}, acc);
+  return __fadd_rn(acc.x, acc.y);
+}
+
+// Per-tensor table over the 128 non-negative finite E4M3 bytes b (0x7F is NaN
+// and never produced): x = min(1/eff, FLT_MAX) (0 for b = 0) and y = eff*eff,
+// eff = float(b) * s_t -- the same roundings as candidates() and the error
+// scaling, computed once per CTA instead of twice per block.
+__device__ __forceinline__ void build_scale_table(float s_t, float2* tab) {
+  for (int b = threadIdx.x; b < 128; b += blockDim.x) {
+    const float v = e4m3x2_decode((uint32_t)b).x;
+    const float eff = __fmul_rn(v, s_t);
+    const float inv = b ? fminf(__frcp_rn(eff), FLT_MAX) : 0.0f;
+    tab[b] = make_float2(inv, __fmul_rn(eff, eff));
+  }
+}
+
+// max |x| of 16 bf16 values held as 8 words: max.xorsign.abs keeps the larger
+// magnitude of each half (its sign bit is junk and is dropped at the end).
+__device__ __forceinline__ float absmax16_bf16(const uint32_t (&w)[8]) {
+  uint32_t m[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m[k]) : "r"(w[2 * k]), "r"(w[2 * k + 1]));
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m[0]) : "r"(m[0]), "r"(m[1]));
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m[2]) : "r"(m[2]), "r"(m[3]));
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m[0]) : "r"(m[0]), "r"(m[2]));
+  return fmaxf(fabsf(__uint_as_float(m[0] << 16)), fabsf(__uint_as_float(m[0] & 0xFFFF0000u)));
 }
 
 // Scale-factor byte offset of block (r, c) of a matrix with nb scale columns.

@@ -36,6 +36,7 @@ struct QuantParams {
   int32_t n_partials;
   uint32_t sr_k0, sr_k1, hk0, hk1;  // SR and RHT seed words
   bool aligned32;
+  bool codes16;            // codes and ld_codes 16-byte aligned
 };
 
 struct DequantParams {
@@ -48,7 +49,7 @@ struct DequantParams {
 };
 
 int amax_grid(int64_t n_warp_tasks);
-int quant_grid(int64_t n_warp_tasks);
+int quant_grid(int64_t n_warp_tasks, int kind);
 cudaError_t launch_amax(const AmaxParams& p, bool hadamard, bool transpose, int grid, cudaStream_t s);
 // kind: 0 rows (1D), 1 cols (1D transposed), 2 2D, 3 2D transposed
 cudaError_t launch_quant(const QuantParams& p, int rule, int kind, bool rht, bool sr, int grid, cudaStream_t s);

@@ -4,7 +4,7 @@
 // arithmetic, not a contraction):
 //   amax_rows    max|y| of X (RHT along rows optional) -> one partial per CTA
 //   amax_cols    max|y| with the RHT running down columns (transposed input)
-//   quant_rows   1D blocks along rows: one thread owns one 16-value block
+//   quant_rows   1D blocks along rows: one lane owns 4 consecutive blocks
 //   quant_cols   1D blocks down columns (transposed output): one thread owns
 //                4 adjacent columns x 16 rows
 //   quant_2d     16x16 tiles: 16 lanes own the 16 source rows of a tile
@@ -192,90 +192,215 @@ __device__ __forceinline__ void quant_block(const float (&y)[16], float ab, cons
 
 template <bool SR>
 __device__ __forceinline__ void sr_words16(uint64_t i0, const QuantParams& p, uint32_t (&w)[16]) {
-  if (!SR) return;
+  if constexpr (SR) {
 #pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    U4 u = sr_words4(i0 + 4 * g, p.sr_k0, p.sr_k1);
-    w[4 * g] = u.x;
-    w[4 * g + 1] = u.y;
-    w[4 * g + 2] = u.z;
-    w[4 * g + 3] = u.w;
+    for (int g = 0; g < 4; ++g) {
+      U4 u = sr_words4(i0 + 4 * g, p.sr_k0, p.sr_k1);
+      w[4 * g] = u.x;
+      w[4 * g + 1] = u.y;
+      w[4 * g + 2] = u.z;
+      w[4 * g + 3] = u.w;
+    }
   }
 }
 
 // ------------------------------------------------------------ quant_rows
-// Warp task = one row and 32 consecutive blocks (512 values); lane = block.
-template <int RULE, bool RHT, bool SR>
-__global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
-  __shared__ float s_red[33];
-  const TensorConsts tc = quant_prologue(p, s_red);
-  const uint32_t rht_mask = RHT ? rht_sign_mask(p.hk0, p.hk1) : 0u;
-  const int lane = threadIdx.x & 31;
-  const int64_t nb = p.nb;
-  const int64_t wpr = (nb + 31) >> 5;
-  const int64_t n_tasks = p.R * wpr;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (t >= n_tasks) return;
-  int64_t r = t / wpr, ch = t - r * wpr;
-  const int64_t dr = nwarps / wpr, dch = nwarps - dr * wpr;
+// Warp task = one row and up to 128 consecutive blocks (2048 values, 4 KB of
+// bf16).  Each warp streams its tasks through a private ring of shared-memory
+// slots filled by bulk copies (issued kRowSlots tasks ahead by lane 0), so the
+// HBM reads stay in flight without holding registers.  Lane l owns blocks l,
+// l+32, l+64, l+96 of a task: its code stores and the warp's reads of the slot
+// are contiguous across lanes.  The two candidates' reciprocal and squared
+// effective scale come from a per-CTA table indexed by the E4M3 byte.
+constexpr int kRowWarps = 8;
+constexpr int kRowSlots = 2;
+constexpr int kRowSlotBytes = 128 * 32;
+constexpr int kRowSmemBytes = kRowWarps * kRowSlots * kRowSlotBytes;
+constexpr uint64_t kCopyTimeoutNs = 1000000000ull;  // a bulk copy that takes 1 s has failed
 
-  uint32_t wcur[8];
-  {
-    int64_t b = ch * 32 + lane;
-    if (b < nb) load_block16(p.x + r * p.ld + b * 16, p.aligned32, wcur);
+template <int RULE, bool SR>
+__device__ __forceinline__ void quant_block_tab(const uint64_t (&yp)[8], float ab, const TensorConsts& tc,
+                                                const float2* tab, const uint32_t (&w)[16], uint32_t& lo,
+                                                uint32_t& hi, uint32_t& sf, bool& four) {
+  const uint32_t pair = e4m3x2(__fmul_rn(ab, tc.k6), __fmul_rn(ab, tc.k4));
+  const uint32_t sf6 = pair & 0xFFu, sf4 = pair >> 8;
+  float y[16];
+  if (SR) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      F2 v = unpack_f2(yp[k]);
+      y[2 * k] = v.x;
+      y[2 * k + 1] = v.y;
+    }
   }
-  for (;;) {
-    // next task, and its prefetch
-    int64_t tn = t + nwarps, rn = r + dr, chn = ch + dch;
-    if (chn >= wpr) {
-      chn -= wpr;
-      ++rn;
+  uint32_t lo6 = 0, hi6 = 0, lo4 = 0, hi4 = 0;
+  float E6 = 0.0f, E4 = 0.0f;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    if (c == 0 && RULE == FOS_SCALE_4) continue;
+    if (c == 1 && RULE == FOS_SCALE_6) continue;
+    const float2 t = tab[c == 0 ? sf6 : sf4];
+    uint32_t l, h;
+    float S;
+    if (SR) {
+      S = cand_sr16(y, t.x, w, l, h);
+    } else {
+      const uint64_t inv2 = pack_f2(t.x, t.x);
+      uint64_t acc = 0ull;
+      const uint64_t a[4] = {yp[0], yp[1], yp[2], yp[3]}, b[4] = {yp[4], yp[5], yp[6], yp[7]};
+      l = cand_rne8(a, inv2, acc);
+      h = cand_rne8(b, inv2, acc);
+      const F2 e = unpack_f2(acc);
+      S = __fadd_rn(e.x, e.y);
     }
-    uint32_t wnext[8];
-    if (tn < n_tasks) {
-      int64_t bn = chn * 32 + lane;
-      if (bn < nb) load_block16(p.x + rn * p.ld + bn * 16, p.aligned32, wnext);
+    if (c == 0) {
+      lo6 = l; hi6 = h; E6 = __fmul_rn(S, t.y);
+    } else {
+      lo4 = l; hi4 = h; E4 = __fmul_rn(S, t.y);
     }
+  }
+  if (sf6 == 0u || sf4 == 0u) {
+    // a zero scale flushes the block to zero codes: its error is sum y^2
+    float z[16];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      F2 v = unpack_f2(yp[k]);
+      z[2 * k] = v.x;
+      z[2 * k + 1] = v.y;
+    }
+    const float zz = sumsq16(z);
+    if (sf6 == 0u) E6 = zz;
+    if (sf4 == 0u) E4 = zz;
+  }
+  four = (RULE == FOS_SCALE_4) || (RULE == FOS_SCALE_4OVER6 && E4 < E6);
+  lo = four ? lo4 : lo6;
+  hi = four ? hi4 : hi6;
+  sf = four ? sf4 : sf6;
+}
 
-    const int64_t b = ch * 32 + lane;
-    const bool valid = b < nb;
-    uint32_t lo = 0, hi = 0, sf = 0;
-    bool four = false;
-    if (valid) {
-      float y[16];
+template <int RULE, bool RHT, bool SR>
+__global__ void __launch_bounds__(256, SR ? 2 : 3) quant_rows_kernel(QuantParams p) {
+  extern __shared__ __align__(128) uint8_t q_smem[];
+  __shared__ float s_red[33];
+  __shared__ float2 s_tab[128];
+  __shared__ uint64_t s_bar[kRowWarps * kRowSlots];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x < kRowWarps * kRowSlots) mbar_init(smem_addr(&s_bar[threadIdx.x]), 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  const TensorConsts tc = quant_prologue(p, s_red);
+  build_scale_table(tc.s_t, s_tab);
+  __syncthreads();
+  const uint32_t rht_mask = RHT ? rht_sign_mask(p.hk0, p.hk1) : 0u;
+  const int64_t nb = p.nb;
+  const int64_t wpr = (nb + 127) >> 7;  // warp tasks per row
+  const int64_t nwarps = (int64_t)gridDim.x * kRowWarps;
+  const int64_t gw = (int64_t)blockIdx.x * kRowWarps + warp;
+  // tasks t = gw, gw + nwarps, ... as (row, chunk) pairs advanced without division
+  const int64_t dr = nwarps / wpr, dch = nwarps - dr * wpr;
+  const bool swz = p.sf_layout == FOS_SF_SWIZZLED_128x4;
+  const int64_t n_ct = (nb + 3) >> 2;
+  uint8_t* slots = q_smem + warp * (kRowSlots * kRowSlotBytes);
+  const uint32_t bar0 = smem_addr(&s_bar[warp * kRowSlots]);
+
+  // producer cursor (lane 0): the next task to fetch
+  int64_t pr = gw / wpr, pch = gw - pr * wpr;
+  auto issue_next = [&](int slot) -> bool {
+    if (pr >= p.R) return false;
+    const int64_t c0 = pch * 128;
+    const int64_t nblk = nb - c0 < 128 ? nb - c0 : 128;
+    bulk_g2s(smem_addr(slots + slot * kRowSlotBytes), p.x + pr * p.ld + c0 * 16, (uint32_t)(nblk * 32),
+             bar0 + 8u * slot);
+    pr += dr;
+    pch += dch;
+    if (pch >= wpr) {
+      pch -= wpr;
+      ++pr;
+    }
+    return true;
+  };
+  int issued = 0, consumed = 0;
+  if (lane == 0)
+    for (int k = 0; k < kRowSlots; ++k) issued += issue_next(k) ? 1 : 0;
+
+  int slot = 0;
+  uint32_t ph = 0;
+  bool failed = false;
+  int64_t r = gw / wpr, ch = gw - r * wpr;
+  for (; r < p.R; r += dr, ch += dch) {
+    if (ch >= wpr) {
+      ch -= wpr;
+      if (++r >= p.R) break;
+    }
+    const int64_t c0 = ch * 128;
+    const int nblk = nb - c0 < 128 ? (int)(nb - c0) : 128;
+    // every lane observes the copy's completion itself; the verdict is made
+    // warp-uniform so the warp stays converged
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait_for(bar0 + 8u * slot, ph, kCopyTimeoutNs))) {
+      failed = true;
+      break;
+    }
+    const uint8_t* src = slots + slot * kRowSlotBytes + lane * 32;
+    const int64_t b_lane = c0 + lane;
+    uint8_t* code_dst = p.codes + r * p.ld_codes + b_lane * 8;
+    const int64_t sf_lane = swz ? ((((r >> 7) * n_ct + (b_lane >> 2)) << 9) + ((r & 31) << 4) +
+                                   (((r >> 5) & 3) << 2) + (b_lane & 3))
+                                : r * nb + b_lane;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (lane + 32 * j >= nblk) break;
+      uint32_t wv[8];
+      {
+        const uint4 a = *reinterpret_cast<const uint4*>(src + 1024 * j);
+        const uint4 b = *reinterpret_cast<const uint4*>(src + 1024 * j + 16);
+        wv[0] = a.x; wv[1] = a.y; wv[2] = a.z; wv[3] = a.w;
+        wv[4] = b.x; wv[5] = b.y; wv[6] = b.z; wv[7] = b.w;
+      }
+      uint64_t yp[8];
       float ab;
       if (RHT) {
-        unpack16(wcur, rht_mask, y);
+        float y[16];
+        unpack16(wv, rht_mask, y);
         hadamard16(y);
         ab = absmax16(y);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) yp[k] = pack_f2(y[2 * k], y[2 * k + 1]);
       } else {
-        unpack16(wcur, 0u, y);
-        ab = absmax16_bits(wcur);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) yp[k] = bf16x2_to_f32x2(wv[k]);
+        ab = absmax16_bf16(wv);
       }
       uint32_t w[16];
-      sr_words16<SR>((uint64_t)r * (uint64_t)p.cols + (uint64_t)b * 16, p, w);
-      quant_block<RULE, SR>(y, ab, tc, w, lo, hi, sf, four);
-      *reinterpret_cast<uint2*>(p.codes + r * p.ld_codes + b * 8) = make_uint2(lo, hi);
-      if (p.choice) p.choice[r * nb + b] = four ? 1 : 0;
+      sr_words16<SR>((uint64_t)r * (uint64_t)p.cols + (uint64_t)(b_lane + 32 * j) * 16, p, w);
+      uint32_t lo, hi, sf;
+      bool four;
+      quant_block_tab<RULE, SR>(yp, ab, tc, s_tab, w, lo, hi, sf, four);
+      *reinterpret_cast<uint2*>(code_dst + 256 * j) = make_uint2(lo, hi);
+      // 32 blocks further along a row: 8 swizzled tiles (4096 bytes) further
+      p.sf[sf_lane + (swz ? 4096 * j : 32 * j)] = (uint8_t)sf;
+      if (p.choice) p.choice[r * nb + b_lane + 32 * j] = four ? 1 : 0;
     }
-    if (p.sf_layout == FOS_SF_SWIZZLED_128x4) {
-      // four consecutive blocks of a row are four consecutive bytes
-      uint32_t v = sf;
-      v |= __shfl_down_sync(0xFFFFFFFFu, sf, 1) << 8;
-      v |= __shfl_down_sync(0xFFFFFFFFu, sf, 2) << 16;
-      v |= __shfl_down_sync(0xFFFFFFFFu, sf, 3) << 24;
-      if (valid && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(p.sf + sf_off(r, b, nb, 0)) = v;
-    } else if (valid) {
-      p.sf[r * nb + b] = (uint8_t)sf;
+    __syncwarp();
+    ++consumed;
+    if (lane == 0) {
+      // the warp's reads of this slot are done: refill it
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issued += issue_next(slot) ? 1 : 0;
     }
-
-    if (tn >= n_tasks) break;
-    t = tn;
-    r = rn;
-    ch = chn;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) wcur[k] = wnext[k];
+    if (++slot == kRowSlots) {
+      slot = 0;
+      ph ^= 1u;
+    }
+  }
+  if (lane == 0) {
+    if (failed) *p.tensor_scale = __int_as_float(0x7FC00000);  // NaN: the result is not valid
+    // let copies still in flight land before the CTA exits (bounded)
+    for (; consumed < issued; ++consumed) {
+      mbar_wait_for(bar0 + 8u * slot, ph, kCopyTimeoutNs);
+      if (++slot == kRowSlots) {
+        slot = 0;
+        ph ^= 1u;
+      }
+    }
   }
 }
 
@@ -543,7 +668,16 @@ cudaError_t launch_amax(const AmaxParams& p, bool hadamard, bool transpose, int 
 template <int RULE, bool RHT, bool SR>
 static void launch_q(const QuantParams& p, int kind, int grid, cudaStream_t s) {
   switch (kind) {
-    case 0: quant_rows_kernel<RULE, RHT, SR><<<grid, 256, 0, s>>>(p); break;
+    case 0: {
+      static bool attr = false;  // benign race: the attribute is idempotent
+      if (!attr) {
+        cudaFuncSetAttribute(quant_rows_kernel<RULE, RHT, SR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kRowSmemBytes);
+        attr = true;
+      }
+      quant_rows_kernel<RULE, RHT, SR><<<grid, 256, kRowSmemBytes, s>>>(p);
+      break;
+    }
     case 1: quant_cols_kernel<RULE, RHT, SR><<<grid, 256, 0, s>>>(p); break;
     case 2: quant_2d_kernel<RULE, RHT, SR, false><<<grid, 256, 0, s>>>(p); break;
     default: quant_2d_kernel<RULE, RHT, SR, true><<<grid, 256, 0, s>>>(p); break;
@@ -561,9 +695,10 @@ static void launch_q_rule(const QuantParams& p, int kind, bool rht, bool sr, int
   }
 }
 
-int quant_grid(int64_t n_warp_tasks) {
+int quant_grid(int64_t n_warp_tasks, int kind) {
   int64_t g = (n_warp_tasks + 7) / 8;
-  int64_t cap = (int64_t)sm_count() * 8;
+  // the row kernel keeps three CTAs per SM resident (its shared-memory ring)
+  int64_t cap = (int64_t)sm_count() * (kind == 0 ? 3 : 8);
   if (g > cap) g = cap;
   return (int)(g < 1 ? 1 : g);
 }
