@@ -121,8 +121,10 @@ fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
 
   const bool aligned32 = aligned(x, 32) && ld_x % 16 == 0;
   const bool cols_amax = rht && tr;
+  // 1D blocks along rows without a supplied amax: one launch does both passes
+  const bool fused = !tr && !two_d && !opt->tensor_amax;
   int n_partials = 0;
-  if (!opt->tensor_amax) {
+  if (!opt->tensor_amax && !fused) {
     fos::AmaxParams a{};
     a.x = static_cast<const uint16_t*>(x);
     a.rows = rows;
@@ -157,6 +159,10 @@ fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
   p.hk1 = (uint32_t)(opt->hadamard_seed >> 32);
   p.aligned32 = aligned32;
   p.codes16 = aligned(codes, 16) && ld_codes % 16 == 0;
+  if (fused) {
+    p.ws_partials = static_cast<float*>(workspace);
+    p.ws_barrier = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + fos::kBarrierOffset);
+  }
 
   int kind;
   int64_t tasks;
@@ -170,10 +176,13 @@ fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
     kind = 0;
     tasks = R * ((nb + 127) / 128);
   }
-  const int grid = fos::quant_grid(tasks, kind);
-  if (fos::launch_quant(p, opt->scale_rule, kind, rht, opt->rounding == FOS_ROUND_STOCHASTIC, grid, stream) !=
-      cudaSuccess)
-    return FOS_ERR_CUDA;
+  const bool sr = opt->rounding == FOS_ROUND_STOCHASTIC;
+  if (fused) {
+    if (fos::launch_quant_rows_fused(p, opt->scale_rule, rht, sr, tasks, stream) != cudaSuccess) return FOS_ERR_CUDA;
+  } else {
+    const int grid = fos::quant_grid(tasks, kind);
+    if (fos::launch_quant(p, opt->scale_rule, kind, rht, sr, grid, stream) != cudaSuccess) return FOS_ERR_CUDA;
+  }
   if (opt->sf_layout == FOS_SF_SWIZZLED_128x4 && (R % 128 != 0 || nb % 4 != 0)) {
     if (fos::launch_sf_pad(sf, sf_bytes_of(R, nb, opt->sf_layout), R, nb, stream) != cudaSuccess)
       return FOS_ERR_CUDA;

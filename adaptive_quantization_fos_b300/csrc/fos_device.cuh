@@ -347,6 +347,63 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
                : "memory");
 }
 
+// The same with an L2 eviction policy (from createpolicy) for the source lines.
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                              uint64_t policy) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// 32 bytes of read-only global data with an L2 eviction policy.
+__device__ __forceinline__ void ldg256_hint(const void* p, uint32_t (&w)[8], uint64_t policy) {
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+               : "l"(p), "l"(policy));
+}
+
+__device__ __forceinline__ void ldg128x2_hint(const void* p, uint32_t (&w)[8], uint64_t policy) {
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.b32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+               : "l"(p), "l"(policy));
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.b32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+               : "l"(static_cast<const char*>(p) + 16), "l"(policy));
+}
+
+// Grid-wide barrier for a launch whose CTAs are all resident (cooperative
+// launch) on an arrival counter that is zero when the launch starts (the host
+// clears it in stream order before the launch).  Called by one thread per
+// CTA; the wait gives up (returns false) after timeout_ns.
+__device__ __forceinline__ bool grid_barrier(unsigned int* word, unsigned int n, uint64_t timeout_ns) {
+  __threadfence();
+  atomicAdd(word, 1u);
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    unsigned int cur;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(cur) : "l"(word) : "memory");
+    if (cur >= n) break;
+    if ((i & 15u) == 15u && globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+  __threadfence();
+  return true;
+}
+
 // ------------------------------------------------------------------- RHT
 // In place on 16 values: sign flips (bit j of mask), butterflies of stride
 // 1, 2, 4, 8 -- (a, b) -> (a + b, a - b) -- then an exact scaling by 1/4.

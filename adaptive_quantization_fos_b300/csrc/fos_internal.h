@@ -12,7 +12,10 @@ namespace fos {
 // Upper bound on the number of CTAs of the amax pass (= partial maxima the
 // quantize kernels reduce in their prologue).
 constexpr int kMaxAmaxPartials = 2048;
-constexpr size_t kQuantWorkspaceBytes = kMaxAmaxPartials * sizeof(float);
+// Workspace: the partial maxima, then (at kBarrierOffset) the word of the
+// grid barrier of the one-launch row quantizer.
+constexpr size_t kBarrierOffset = kMaxAmaxPartials * sizeof(float);
+constexpr size_t kQuantWorkspaceBytes = kBarrierOffset + 256;
 
 struct AmaxParams {
   const uint16_t* x;
@@ -37,6 +40,9 @@ struct QuantParams {
   uint32_t sr_k0, sr_k1, hk0, hk1;  // SR and RHT seed words
   bool aligned32;
   bool codes16;            // codes and ld_codes 16-byte aligned
+  // one-launch row quantizer (amax pass, grid barrier, quantize pass)
+  float* ws_partials;      // one partial maximum per CTA
+  unsigned int* ws_barrier;
 };
 
 struct DequantParams {
@@ -53,6 +59,10 @@ int quant_grid(int64_t n_warp_tasks, int kind);
 cudaError_t launch_amax(const AmaxParams& p, bool hadamard, bool transpose, int grid, cudaStream_t s);
 // kind: 0 rows (1D), 1 cols (1D transposed), 2 2D, 3 2D transposed
 cudaError_t launch_quant(const QuantParams& p, int rule, int kind, bool rht, bool sr, int grid, cudaStream_t s);
+// Rows (1D) with the tensor amax computed in the same launch: a cooperative
+// launch of as many CTAs as fit on the GPU at once.
+cudaError_t launch_quant_rows_fused(const QuantParams& p, int rule, bool rht, bool sr, int64_t n_tasks,
+                                    cudaStream_t s);
 cudaError_t launch_sf_pad(uint8_t* sf, int64_t bytes, int64_t R, int64_t nb, cudaStream_t s);
 cudaError_t launch_dequant(const DequantParams& p, bool bf16, cudaStream_t s);
 cudaError_t launch_e2m1_encode(const float* x, int64_t n, uint8_t* out, cudaStream_t s);

@@ -10,8 +10,9 @@
 // library itself owns.
 //
 // Limits and behaviour a caller must know:
-//   - The array holds kNoAllocScratchFloats floats (8 KiB).  Every GPU that
-//     loads the library holds it until the process exits.
+//   - The array holds kNoAllocScratchFloats floats (8448 bytes: the partial
+//     maxima and the word of the one-launch quantizer's grid barrier).  Every
+//     GPU that loads the library holds it until the process exits.
 //   - The first call on each device looks up the array's device address (with
 //     that device current) and caches it.  Make that first call before any
 //     stream capture.
@@ -19,7 +20,9 @@
 //     example on two streams without ordering between them) race on it and
 //     may produce wrong scales.
 //   - Nothing in the array needs clearing between calls: each call's amax pass
-//     writes every slot its quantize pass later reads.
+//     writes every slot its quantize pass later reads, and each call clears
+//     the barrier word (a 4-byte cudaMemsetAsync on the caller's stream, which
+//     allocates nothing) before its launch.
 //   - A call whose scratch need exceeds the array is rejected with
 //     FOS_ERR_INVALID_ARG.  The amax pass never runs more than
 //     kMaxAmaxPartials CTAs, so every call fos_quantize accepts fits.
@@ -33,7 +36,7 @@
 
 namespace {
 
-constexpr int kNoAllocScratchFloats = fos::kMaxAmaxPartials;
+constexpr int kNoAllocScratchFloats = (int)(fos::kQuantWorkspaceBytes / sizeof(float));
 static_assert(kNoAllocScratchFloats * sizeof(float) >= fos::kQuantWorkspaceBytes,
               "the fixed scratch must cover the quantizer's workspace");
 

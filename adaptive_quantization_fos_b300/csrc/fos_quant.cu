@@ -278,18 +278,21 @@ __device__ __forceinline__ void quant_block_tab(const uint64_t (&yp)[8], float a
   sf = four ? sf4 : sf6;
 }
 
-template <int RULE, bool RHT, bool SR>
+// FUSED: the tensor amax is computed in the same launch.  Pass 1 reads every
+// task once for its block maxima (keeping the lines in L2), one partial per
+// CTA goes to the workspace, a grid barrier (all CTAs resident: cooperative
+// launch) publishes them, and pass 2 quantizes, re-reading the input mostly
+// from L2 when the matrix fits there.
+template <int RULE, bool RHT, bool SR, bool FUSED>
 __global__ void __launch_bounds__(256, SR ? 2 : 3) quant_rows_kernel(QuantParams p) {
   extern __shared__ __align__(128) uint8_t q_smem[];
   __shared__ float s_red[33];
   __shared__ float2 s_tab[128];
   __shared__ uint64_t s_bar[kRowWarps * kRowSlots];
+  __shared__ int s_ok;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x < kRowWarps * kRowSlots) mbar_init(smem_addr(&s_bar[threadIdx.x]), 1);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  const TensorConsts tc = quant_prologue(p, s_red);
-  build_scale_table(tc.s_t, s_tab);
-  __syncthreads();
   const uint32_t rht_mask = RHT ? rht_sign_mask(p.hk0, p.hk1) : 0u;
   const int64_t nb = p.nb;
   const int64_t wpr = (nb + 127) >> 7;  // warp tasks per row
@@ -297,6 +300,60 @@ __global__ void __launch_bounds__(256, SR ? 2 : 3) quant_rows_kernel(QuantParams
   const int64_t gw = (int64_t)blockIdx.x * kRowWarps + warp;
   // tasks t = gw, gw + nwarps, ... as (row, chunk) pairs advanced without division
   const int64_t dr = nwarps / wpr, dch = nwarps - dr * wpr;
+  TensorConsts tc;
+  if constexpr (FUSED) {
+    const uint64_t keep = l2_policy_evict_last();
+    float m = 0.0f;
+    int64_t r = gw / wpr, ch = gw - r * wpr;
+    for (; r < p.R; r += dr, ch += dch) {
+      if (ch >= wpr) {
+        ch -= wpr;
+        if (++r >= p.R) break;
+      }
+      const int64_t c0 = ch * 128;
+      const int nblk = nb - c0 < 128 ? (int)(nb - c0) : 128;
+      const uint16_t* src = p.x + r * p.ld + (c0 + lane) * 16;
+      uint32_t wv[4][8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (lane + 32 * j < nblk) {
+          if (p.aligned32)
+            ldg256_hint(src + 512 * j, wv[j], keep);
+          else
+            ldg128x2_hint(src + 512 * j, wv[j], keep);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (lane + 32 * j >= nblk) break;
+        if (RHT) {
+          float y[16];
+          unpack16(wv[j], rht_mask, y);
+          hadamard16(y);
+          m = fmaxf(m, absmax16(y));
+        } else {
+          m = fmaxf(m, absmax16_bf16(wv[j]));
+        }
+      }
+    }
+    m = block_max(m, s_red);
+    if (threadIdx.x == 0) {
+      p.ws_partials[blockIdx.x] = m;
+      s_ok = grid_barrier(p.ws_barrier, gridDim.x, kCopyTimeoutNs) ? 1 : 0;
+      if (!s_ok) *p.tensor_scale = __int_as_float(0x7FC00000);  // NaN: the result is not valid
+    }
+    __syncthreads();
+    if (!s_ok) return;
+    float mm = 0.0f;
+    for (int i = threadIdx.x; i < (int)gridDim.x; i += blockDim.x) mm = fmaxf(mm, __ldcg(p.ws_partials + i));
+    tc = tensor_consts(block_max(mm, s_red));
+    if (blockIdx.x == 0 && threadIdx.x == 0) *p.tensor_scale = tc.s_t;
+  } else {
+    tc = quant_prologue(p, s_red);
+  }
+  build_scale_table(tc.s_t, s_tab);
+  __syncthreads();
+  const uint64_t stream_once = l2_policy_evict_first();
   const bool swz = p.sf_layout == FOS_SF_SWIZZLED_128x4;
   const int64_t n_ct = (nb + 3) >> 2;
   uint8_t* slots = q_smem + warp * (kRowSlots * kRowSlotBytes);
@@ -308,8 +365,8 @@ __global__ void __launch_bounds__(256, SR ? 2 : 3) quant_rows_kernel(QuantParams
     if (pr >= p.R) return false;
     const int64_t c0 = pch * 128;
     const int64_t nblk = nb - c0 < 128 ? nb - c0 : 128;
-    bulk_g2s(smem_addr(slots + slot * kRowSlotBytes), p.x + pr * p.ld + c0 * 16, (uint32_t)(nblk * 32),
-             bar0 + 8u * slot);
+    bulk_g2s_hint(smem_addr(slots + slot * kRowSlotBytes), p.x + pr * p.ld + c0 * 16, (uint32_t)(nblk * 32),
+                  bar0 + 8u * slot, stream_once);
     pr += dr;
     pch += dch;
     if (pch >= wpr) {
@@ -671,11 +728,11 @@ static void launch_q(const QuantParams& p, int kind, int grid, cudaStream_t s) {
     case 0: {
       static bool attr = false;  // benign race: the attribute is idempotent
       if (!attr) {
-        cudaFuncSetAttribute(quant_rows_kernel<RULE, RHT, SR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(quant_rows_kernel<RULE, RHT, SR, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kRowSmemBytes);
         attr = true;
       }
-      quant_rows_kernel<RULE, RHT, SR><<<grid, 256, kRowSmemBytes, s>>>(p);
+      quant_rows_kernel<RULE, RHT, SR, false><<<grid, 256, kRowSmemBytes, s>>>(p);
       break;
     }
     case 1: quant_cols_kernel<RULE, RHT, SR><<<grid, 256, 0, s>>>(p); break;
@@ -701,6 +758,48 @@ int quant_grid(int64_t n_warp_tasks, int kind) {
   int64_t cap = (int64_t)sm_count() * (kind == 0 ? 3 : 8);
   if (g > cap) g = cap;
   return (int)(g < 1 ? 1 : g);
+}
+
+template <int RULE, bool RHT, bool SR>
+static cudaError_t launch_rows_fused(const QuantParams& p, int64_t n_tasks, cudaStream_t s) {
+  auto fn = quant_rows_kernel<RULE, RHT, SR, true>;
+  static int per_sm = 0;  // benign race: every thread computes the same value
+  if (per_sm == 0) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowSmemBytes);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, 256, kRowSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    per_sm = n;
+  }
+  int64_t grid = (int64_t)per_sm * sm_count();
+  const int64_t want = (n_tasks + kRowWarps - 1) / kRowWarps;
+  if (grid > want) grid = want;
+  if (grid > kMaxAmaxPartials) grid = kMaxAmaxPartials;
+  if (grid < 1) grid = 1;
+  QuantParams q = p;
+  void* args[] = {&q};
+  cudaError_t e = cudaMemsetAsync(p.ws_barrier, 0, sizeof(unsigned int), s);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fn), dim3((unsigned)grid), dim3(256), args,
+                                     kRowSmemBytes, s);
+}
+
+template <int RULE>
+static cudaError_t launch_rows_fused_rule(const QuantParams& p, bool rht, bool sr, int64_t n_tasks,
+                                          cudaStream_t s) {
+  if (rht) return sr ? launch_rows_fused<RULE, true, true>(p, n_tasks, s) : launch_rows_fused<RULE, true, false>(p, n_tasks, s);
+  return sr ? launch_rows_fused<RULE, false, true>(p, n_tasks, s) : launch_rows_fused<RULE, false, false>(p, n_tasks, s);
+}
+
+cudaError_t launch_quant_rows_fused(const QuantParams& p, int rule, bool rht, bool sr, int64_t n_tasks,
+                                    cudaStream_t s) {
+  switch (rule) {
+    case FOS_SCALE_6: return launch_rows_fused_rule<FOS_SCALE_6>(p, rht, sr, n_tasks, s);
+    case FOS_SCALE_4: return launch_rows_fused_rule<FOS_SCALE_4>(p, rht, sr, n_tasks, s);
+    default: return launch_rows_fused_rule<FOS_SCALE_4OVER6>(p, rht, sr, n_tasks, s);
+  }
 }
 
 cudaError_t launch_quant(const QuantParams& p, int rule, int kind, bool rht, bool sr, int grid, cudaStream_t s) {

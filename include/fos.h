@@ -150,8 +150,16 @@ fos_status fos_tensor_amax(const void* x, int64_t rows, int64_t cols, int64_t ld
  *   choice    optional device [R_out][C_out/16] bytes: 1 where the block kept
  *             the 4 candidate (NULL: not written).
  *   workspace device scratch of fos_quantize_workspace_size() bytes (may be
- *             NULL when opt->tensor_amax is given).
+ *             NULL when opt->tensor_amax is given); its contents need no
+ *             initialisation, and calls sharing one workspace must not
+ *             overlap on the GPU.
  * The RHT output is not undone: codes describe the transformed values.
+ * 1D blocks along rows without a supplied amax run as one cooperative launch
+ * (amax pass, grid barrier in the workspace -- its counter is cleared by a
+ * 4-byte cudaMemsetAsync on `stream` first -- and a quantize pass that
+ * re-reads the input mostly from L2).  A device wait that runs out (a copy or the grid
+ * barrier taking over a second) leaves *tensor_scale = NaN: the outputs are
+ * then not valid.
  */
 fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
                         const fos_quant_options* opt, uint8_t* codes, int64_t ld_codes, uint8_t* sf,
@@ -164,7 +172,7 @@ fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
  * only its inputs and outputs and forbid cudaMalloc after start-up).  The
  * pages have no counterpart; this is a library convenience.  Same arguments,
  * results and validation as fos_quantize, minus the workspace: the amax
- * pass's partial maxima go to a fixed 8 KiB array in device memory owned by
+ * pass's partial maxima go to a fixed 8448-byte array in device memory owned by
  * the library (held on every GPU that loads it until the process exits).
  *   - The first call on a device looks up the array's address; make it
  *     before any stream capture.
