@@ -83,6 +83,7 @@ def _load() -> ctypes.CDLL:
         "fos_e2m1_encode": (i32, [vp, i64, vp, vp]),
         "fos_e4m3_encode": (i32, [vp, i64, vp, vp]),
         "fos_philox4x32_10": (i32, [vp, i64, u64, vp, vp]),
+        "fos_selftest_wait_limits": (i32, [vp, sz, u64, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -94,7 +95,7 @@ def _load() -> ctypes.CDLL:
 _lib = _load()
 EXPORTED = ("fos_abi_version", "fos_status_string", "fos_sf_bytes", "fos_quantize_workspace_size",
             "fos_tensor_amax", "fos_quantize", "fos_quantize_noalloc", "fos_dequantize", "fos_gemm", "fos_e2m1_encode",
-            "fos_e4m3_encode", "fos_philox4x32_10")
+            "fos_e4m3_encode", "fos_philox4x32_10", "fos_selftest_wait_limits")
 
 
 def _check(status: int, what: str) -> None:
@@ -148,6 +149,10 @@ def fos_dequantize(q: fos_nvfp4_tensor, out, out_dtype, ld_out, stream) -> int:
 
 def fos_gemm(A: fos_nvfp4_tensor, B: fos_nvfp4_tensor, C, ldc, dev_status, stream) -> int:
     return int(_lib.fos_gemm(ctypes.byref(A), ctypes.byref(B), C, ldc, dev_status or None, stream))
+
+
+def fos_selftest_wait_limits(scratch, scratch_bytes, timeout_ns, result, stream) -> int:
+    return int(_lib.fos_selftest_wait_limits(scratch, scratch_bytes, timeout_ns, result, stream))
 
 
 def fos_e2m1_encode(x, n, codes, stream) -> int:

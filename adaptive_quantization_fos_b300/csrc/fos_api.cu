@@ -159,6 +159,7 @@ fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
   p.hk1 = (uint32_t)(opt->hadamard_seed >> 32);
   p.aligned32 = aligned32;
   p.codes16 = aligned(codes, 16) && ld_codes % 16 == 0;
+  p.timeout_ns = fos::kWaitTimeoutNs;
   if (fused) {
     p.ws_partials = static_cast<float*>(workspace);
     p.ws_barrier = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + fos::kBarrierOffset);
@@ -211,6 +212,49 @@ fos_status fos_dequantize(const fos_nvfp4_tensor* q, void* out, int32_t out_dtyp
   p.sf_layout = q->sf_layout;
   p.out = out;
   return cuda_status(fos::launch_dequant(p, out_dtype == FOS_DTYPE_BF16, stream));
+}
+
+fos_status fos_selftest_wait_limits(void* scratch, size_t scratch_bytes, uint64_t timeout_ns, int32_t* result,
+                                    cudaStream_t stream) {
+  constexpr size_t kNeed = 1 << 17;
+  if (!scratch || scratch_bytes < kNeed || !aligned(scratch, 256) || !result || !aligned(result, 4))
+    return FOS_ERR_INVALID_ARG;
+  if (timeout_ns == 0 || timeout_ns > fos::kWaitTimeoutNs) return FOS_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(result, 0, 2 * sizeof(int32_t), stream) != cudaSuccess) return FOS_ERR_CUDA;
+  // 1. the GEMM with a producer that never fills a stage
+  constexpr size_t kGemmPart = 80 << 10;
+  fos_status st = fos::gemm_stall_selftest(scratch, kGemmPart, timeout_ns, result, stream);
+  if (st != FOS_OK) return st;
+  // 2. the one-launch quantizer on a 16 x 64 zero matrix with a grid barrier
+  //    that waits for one CTA more than the launch has
+  char* b = static_cast<char*>(scratch) + kGemmPart;
+  uint16_t* x = reinterpret_cast<uint16_t*>(b);             // 2 KB
+  uint8_t* codes = reinterpret_cast<uint8_t*>(b + 4096);    // 512 B
+  uint8_t* sf = reinterpret_cast<uint8_t*>(b + 8192);       // 512 B
+  float* ts = reinterpret_cast<float*>(b + 12288);
+  void* ws = b + 16384;                                     // kQuantWorkspaceBytes
+  static_assert(kGemmPart + 16384 + fos::kQuantWorkspaceBytes <= kNeed, "self-test scratch layout");
+  if (cudaMemsetAsync(b, 0, 16384, stream) != cudaSuccess) return FOS_ERR_CUDA;
+  fos::QuantParams p{};
+  p.x = x;
+  p.rows = 16;
+  p.cols = 64;
+  p.ld = 64;
+  p.R = 16;
+  p.nb = 4;
+  p.codes = codes;
+  p.ld_codes = 32;
+  p.sf = sf;
+  p.sf_layout = FOS_SF_SWIZZLED_128x4;
+  p.tensor_scale = ts;
+  p.aligned32 = true;
+  p.codes16 = true;
+  p.ws_partials = static_cast<float*>(ws);
+  p.ws_barrier = reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + fos::kBarrierOffset);
+  p.barrier_extra = 1;
+  p.timeout_ns = timeout_ns;
+  if (fos::launch_quant_rows_fused(p, FOS_SCALE_4OVER6, false, false, 16, stream) != cudaSuccess) return FOS_ERR_CUDA;
+  return cuda_status(fos::launch_nan_to_status(ts, result + 1, stream));
 }
 
 fos_status fos_e2m1_encode(const float* x, int64_t n, uint8_t* codes, cudaStream_t stream) {

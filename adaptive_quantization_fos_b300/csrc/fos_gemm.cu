@@ -531,6 +531,21 @@ fos_status gemm_checked(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, vo
 
 }  // namespace
 
+namespace fos {
+fos_status gemm_stall_selftest(void* scratch, size_t scratch_bytes, uint64_t timeout_ns, int32_t* status,
+                               cudaStream_t s) {
+  // A [128 x 256] and B [128 x 256] codes (16 KB each), their scales (2 KB
+  // each), two tensor scales and C [128 x 128] bf16 (32 KB): 70 KB
+  if (scratch_bytes < (72u << 10)) return FOS_ERR_INVALID_ARG;
+  uint8_t* b = static_cast<uint8_t*>(scratch);
+  fos_nvfp4_tensor A{b, b + 32768, reinterpret_cast<float*>(b + 36864), 128, 256, 128, FOS_SF_SWIZZLED_128x4, 0};
+  fos_nvfp4_tensor B{b + 16384, b + 34816, reinterpret_cast<float*>(b + 36864), 128, 256, 128,
+                     FOS_SF_SWIZZLED_128x4, 0};
+  if (cudaMemsetAsync(b, 0, 40960, s) != cudaSuccess) return FOS_ERR_CUDA;
+  return launch_gemm<128>(&A, &B, b + 40960, 128, status, timeout_ns, 1, 1, s);
+}
+}  // namespace fos
+
 extern "C" fos_status fos_gemm(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* C, int64_t ldc,
                                int32_t* dev_status, cudaStream_t stream) {
   return gemm_checked(A, B, C, ldc, dev_status, kDefaultTimeoutNs, 0, stream);

@@ -43,7 +43,12 @@ struct QuantParams {
   // one-launch row quantizer (amax pass, grid barrier, quantize pass)
   float* ws_partials;      // one partial maximum per CTA
   unsigned int* ws_barrier;
+  unsigned int barrier_extra;  // arrivals beyond the grid the barrier waits for (0; 1 only in the self-test)
+  uint64_t timeout_ns;         // limit of every device wait (copies, the grid barrier)
 };
+
+// Default limit of a device wait: a copy or barrier that takes a second has failed.
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;
 
 struct DequantParams {
   const uint8_t* codes;
@@ -65,6 +70,13 @@ cudaError_t launch_quant_rows_fused(const QuantParams& p, int rule, bool rht, bo
                                     cudaStream_t s);
 cudaError_t launch_sf_pad(uint8_t* sf, int64_t bytes, int64_t R, int64_t nb, cudaStream_t s);
 cudaError_t launch_dequant(const DequantParams& p, bool bf16, cudaStream_t s);
+// The GEMM kernel on tiny dummy operands in `scratch` with a producer that
+// never fills a stage, so its waits run out after timeout_ns and it writes
+// FOS_ERR_TIMEOUT to *status.
+fos_status gemm_stall_selftest(void* scratch, size_t scratch_bytes, uint64_t timeout_ns, int32_t* status,
+                               cudaStream_t s);
+// *out = FOS_ERR_TIMEOUT if *tensor_scale is NaN, else FOS_OK.
+cudaError_t launch_nan_to_status(const float* tensor_scale, int32_t* out, cudaStream_t s);
 cudaError_t launch_e2m1_encode(const float* x, int64_t n, uint8_t* out, cudaStream_t s);
 cudaError_t launch_e4m3_encode(const float* x, int64_t n, uint8_t* out, cudaStream_t s);
 cudaError_t launch_philox(const uint32_t* ctr, int64_t n, uint64_t key, uint32_t* out, cudaStream_t s);

@@ -216,7 +216,6 @@ constexpr int kRowWarps = 8;
 constexpr int kRowSlots = 2;
 constexpr int kRowSlotBytes = 128 * 32;
 constexpr int kRowSmemBytes = kRowWarps * kRowSlots * kRowSlotBytes;
-constexpr uint64_t kCopyTimeoutNs = 1000000000ull;  // a bulk copy that takes 1 s has failed
 
 template <int RULE, bool SR>
 __device__ __forceinline__ void quant_block_tab(const uint64_t (&yp)[8], float ab, const TensorConsts& tc,
@@ -339,7 +338,7 @@ __global__ void __launch_bounds__(256, SR ? 2 : 3) quant_rows_kernel(QuantParams
     m = block_max(m, s_red);
     if (threadIdx.x == 0) {
       p.ws_partials[blockIdx.x] = m;
-      s_ok = grid_barrier(p.ws_barrier, gridDim.x, kCopyTimeoutNs) ? 1 : 0;
+      s_ok = grid_barrier(p.ws_barrier, gridDim.x + p.barrier_extra, p.timeout_ns) ? 1 : 0;
       if (!s_ok) *p.tensor_scale = __int_as_float(0x7FC00000);  // NaN: the result is not valid
     }
     __syncthreads();
@@ -392,7 +391,7 @@ __global__ void __launch_bounds__(256, SR ? 2 : 3) quant_rows_kernel(QuantParams
     const int nblk = nb - c0 < 128 ? (int)(nb - c0) : 128;
     // every lane observes the copy's completion itself; the verdict is made
     // warp-uniform so the warp stays converged
-    if (!__all_sync(0xFFFFFFFFu, mbar_wait_for(bar0 + 8u * slot, ph, kCopyTimeoutNs))) {
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait_for(bar0 + 8u * slot, ph, p.timeout_ns))) {
       failed = true;
       break;
     }
@@ -452,7 +451,7 @@ __global__ void __launch_bounds__(256, SR ? 2 : 3) quant_rows_kernel(QuantParams
     if (failed) *p.tensor_scale = __int_as_float(0x7FC00000);  // NaN: the result is not valid
     // let copies still in flight land before the CTA exits (bounded)
     for (; consumed < issued; ++consumed) {
-      mbar_wait_for(bar0 + 8u * slot, ph, kCopyTimeoutNs);
+      mbar_wait_for(bar0 + 8u * slot, ph, p.timeout_ns);
       if (++slot == kRowSlots) {
         slot = 0;
         ph ^= 1u;
@@ -815,6 +814,15 @@ cudaError_t launch_sf_pad(uint8_t* sf, int64_t bytes, int64_t R, int64_t nb, cud
   int64_t g = (bytes + 255) / 256;
   if (g > 1024) g = 1024;
   sf_pad_zero_kernel<<<(int)(g < 1 ? 1 : g), 256, 0, s>>>(sf, bytes, R, nb);
+  return cudaGetLastError();
+}
+
+__global__ void nan_to_status_kernel(const float* ts, int32_t* out) {
+  *out = isnan(*ts) ? (int32_t)FOS_ERR_TIMEOUT : (int32_t)FOS_OK;
+}
+
+cudaError_t launch_nan_to_status(const float* tensor_scale, int32_t* out, cudaStream_t s) {
+  nan_to_status_kernel<<<1, 1, 0, s>>>(tensor_scale, out);
   return cudaGetLastError();
 }
 

@@ -209,6 +209,25 @@ fos_status fos_dequantize(const fos_nvfp4_tensor* q, void* out, int32_t out_dtyp
 fos_status fos_gemm(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* C, int64_t ldc,
                     int32_t* dev_status, cudaStream_t stream);
 
+/*
+ * fos_selftest_wait_limits -- runs the library's bounded device waits into
+ * their limits on purpose and reports what the kernels recorded, so a caller
+ * (or a test) can check failure detection without faulting or hanging a GPU.
+ * The pages have no counterpart; this is a library self-test.
+ *   1. fos_gemm's kernel on dummy 128x128x256 operands whose producer never
+ *      fills a stage: every wait runs out after timeout_ns and the kernel
+ *      writes FOS_ERR_TIMEOUT to result[0], frees its tensor memory and exits.
+ *   2. The one-launch row quantizer on a 16 x 64 zero matrix with a grid
+ *      barrier that waits for one CTA more than the launch has: the barrier
+ *      gives up after timeout_ns, tensor_scale becomes NaN, and result[1]
+ *      receives FOS_ERR_TIMEOUT.
+ *   scratch     device, >= 128 KiB, 256-byte aligned (operands and outputs).
+ *   timeout_ns  1 .. 1e9; result device int32[2], cleared first.
+ * Enqueued on `stream`; reads nothing back.  The CUDA context stays usable.
+ */
+fos_status fos_selftest_wait_limits(void* scratch, size_t scratch_bytes, uint64_t timeout_ns, int32_t* result,
+                                    cudaStream_t stream);
+
 /* ---- element codecs (the conversions the quantizer uses), for testing ---- */
 
 /* codes[i] = E2M1 code (RNE, saturating, sign kept) of x[i]; one code per byte. */
