@@ -12,14 +12,15 @@
 //   warp 0      TMA producer: codes of A (128 x 256 values) and B (BN x 256)
 //               per stage with 128-byte swizzle, plus the stage's scale bytes
 //               (contiguous 512-byte chunks of the 128x4 layout) by bulk copy.
-//   warp 1      allocates tensor memory; one thread copies each stage's scale
-//               chunks into tensor memory (tcgen05.cp 32x128b.warpx4) and
-//               issues 4 MMAs of K = 64 per stage; tcgen05.commit frees the
-//               stage and, after the last stage, signals the accumulator.
-//   warps 2..   epilogue: each warp reads 32 accumulator lanes x 128 columns
-//               into registers, hands the accumulator back at once (so the
-//               next tile's MMAs start while it stores), scales, rounds to
-//               bf16 and stores.
+//   warp 1      allocates tensor memory; one thread issues 4 MMAs of K = 64 per
+//               stage once the stage's codes and scales are in place;
+//               tcgen05.commit frees the stage and, after the last stage,
+//               signals the accumulator.
+//   warps 2..   scales and epilogue: they write each stage's scale words into
+//               tensor memory (tcgen05.st), and at the end of a tile each
+//               reads 32 accumulator lanes x 128 columns into registers, hands
+//               the accumulator back at once (so the next tile's MMAs start
+//               while it stores), scales, rounds to bf16 and stores.
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel records
 // FOS_ERR_TIMEOUT, all roles stop, in-flight copies and MMAs are drained
 // (again bounded) and the tensor memory is freed before the CTA exits.
@@ -57,6 +58,7 @@ struct Cfg {
   static constexpr int kSfbColsPerMma = BN / 32;
   static constexpr int kSfStageCols = kSfaCols + 4 * kSfbColsPerMma;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
+  static_assert((4 * kStages + 5) * 8 <= 256, "barrier area");
   static_assert(kStageBytes % 1024 == 0, "stage buffers stay 1024-byte aligned");
   static_assert(BN + kStages * kSfStageCols <= (int)kTmemCols, "tensor memory budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -164,10 +166,6 @@ __host__ __device__ constexpr uint32_t mma_idesc(int m, int n) {
   return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                        uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
   asm volatile(
@@ -194,6 +192,32 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&v)[32], int o
 
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Registers -> tensor memory: lane L of the warp's quadrant writes its 8 (16)
+// words to columns taddr .. taddr+7 (+15) of lane L.
+__device__ __forceinline__ void tc_st8(uint32_t taddr, const uint4& a, const uint4& b) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(a.x),
+               "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint4& a, const uint4& b, const uint4& c,
+                                       const uint4& d) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w), "r"(c.x), "r"(c.y), "r"(c.z),
+      "r"(c.w), "r"(d.x), "r"(d.y), "r"(d.z), "r"(d.w)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
@@ -214,9 +238,11 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
-  // bars[0, S): stage full; [S, 2S): stage empty; 2S: acc full; 2S+1: acc empty; 2S+2: drain
-  volatile int* abort = reinterpret_cast<volatile int*>(bars + 2 * C::kStages + 3);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 4);
+  // bars[0, S): stage codes landed; [S, 2S): stage empty; 2S: acc full; 2S+1: acc empty;
+  // 2S+2: drain; [2S+3, 3S+3): stage scales in tensor memory; [3S+3, 4S+3): stage scale
+  // bytes landed
+  volatile int* abort = reinterpret_cast<volatile int*>(bars + 4 * C::kStages + 3);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4 * C::kStages + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t bar0 = smem_u32(bars);
@@ -225,6 +251,8 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   const uint32_t acc_full = bar0 + 8u * (2 * C::kStages);
   const uint32_t acc_empty = acc_full + 8u;
   const uint32_t drain_bar = acc_full + 16u;
+  auto sf_ready = [&](int s) { return acc_full + 24u + 8u * s; };
+  auto sf_full = [&](int s) { return acc_full + 24u + 8u * (C::kStages + s); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -234,6 +262,10 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, C::kEpiWarps);
     mbar_init(drain_bar, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(sf_ready(s), C::kEpiWarps);
+      mbar_init(sf_full(s), 1);
+    }
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -267,22 +299,23 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
           }
           if (!args.stall_test) {
             const int kkc = min(4, kmma_total - 4 * kb);
-            uint32_t tx = C::kABytes + C::kBBytes + kkc * kSfChunk;
             int halves = 0;
             for (int h = 0; h < BN / 128; ++h)
               if ((nb * (BN / 128) + h) * 128 < args.n) ++halves;
-            tx += halves * kkc * kSfChunk;
             const uint32_t st = smem_u32(smem + s * C::kStageBytes);
-            mbar_expect_tx(full_bar(s), tx);
-            tma_load_2d(st, &tm_a, kb * kBKBytes, mb * kBM, full_bar(s));
-            tma_load_2d(st + C::kABytes, &tm_b, kb * kBKBytes, nb * BN, full_bar(s));
+            // the small scale copies first, on their own barrier, so the
+            // scales reach tensor memory while the code tiles are in flight
             const uint32_t sfa_dst = st + C::kABytes + C::kBBytes;
+            mbar_expect_tx(sf_full(s), (1 + halves) * kkc * kSfChunk);
             bulk_load(sfa_dst, args.sfa + ((int64_t)mb * args.sf_ktiles + 4 * kb) * kSfChunk, kkc * kSfChunk,
-                      full_bar(s));
+                      sf_full(s));
             for (int h = 0; h < halves; ++h)
               bulk_load(sfa_dst + C::kSfaBytes + h * 4 * kSfChunk,
                         args.sfb + ((int64_t)(nb * (BN / 128) + h) * args.sf_ktiles + 4 * kb) * kSfChunk,
-                        kkc * kSfChunk, full_bar(s));
+                        kkc * kSfChunk, sf_full(s));
+            mbar_expect_tx(full_bar(s), C::kABytes + C::kBBytes);
+            tma_load_2d(st, &tm_a, kb * kBKBytes, mb * kBM, full_bar(s));
+            tma_load_2d(st + C::kABytes, &tm_b, kb * kBKBytes, nb * BN, full_bar(s));
             ++issued;
           }
           if (++s == C::kStages) {
@@ -299,6 +332,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
             ph ^= 1u;
           }
           mbar_wait(full_bar(s), ph, args.timeout_ns, nullptr);
+          mbar_wait(sf_full(s), ph, args.timeout_ns, nullptr);
         }
       }
     }
@@ -318,7 +352,9 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         }
         tc_fence_after();
         for (int kb = 0; kb < args.num_kb; ++kb) {
-          if (!mbar_wait(full_bar(s), ph, args.timeout_ns, abort)) {
+          // the stage's codes are in shared memory and its scales in tensor memory
+          if (!mbar_wait(full_bar(s), ph, args.timeout_ns, abort) ||
+              !mbar_wait(sf_ready(s), ph, args.timeout_ns, abort)) {
             raise_timeout(args, abort);
             ok = false;
             break;
@@ -326,15 +362,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
           tc_fence_after();
           const int kkc = min(4, kmma_total - 4 * kb);
           const uint32_t st = smem_u32(smem + s * C::kStageBytes);
-          const uint32_t sfa_s = st + C::kABytes + C::kBBytes, sfb_s = sfa_s + C::kSfaBytes;
           const uint32_t sf_col = tmem + BN + s * C::kSfStageCols;
-          for (int kk = 0; kk < kkc; ++kk) {
-            tc_cp_sf(sf_col + 4 * kk, smem_desc(sfa_s + kk * kSfChunk, 128, 128, 0));
-#pragma unroll
-            for (int h = 0; h < BN / 128; ++h)
-              tc_cp_sf(sf_col + C::kSfaCols + C::kSfbColsPerMma * kk + 4 * h,
-                       smem_desc(sfb_s + h * 4 * kSfChunk + kk * kSfChunk, 128, 128, 0));
-          }
           const uint64_t adesc = smem_desc(st, 16, 1024, 2);
           const uint64_t bdesc = smem_desc(st + C::kABytes, 16, 1024, 2);
           for (int kk = 0; kk < kkc; ++kk) {
@@ -358,20 +386,73 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------ epilogue
+    // ------------------------------------------------------ epilogue + scales
+    // Between tiles these warps put each stage's scale words into tensor
+    // memory with tcgen05.st (the tcgen05.cp route costs the MMA pipe a fixed
+    // time per copy): lane j of the warp on lane quadrant q reads row j of a
+    // 512-byte scale chunk (16 bytes = the 4-scale words of rows j, 32+j,
+    // 64+j, 96+j) and writes them as 4 columns of tensor-memory lane 32q+j --
+    // in every quadrant the image a 32x128b.warpx4 copy of that chunk makes.
+    // With 256-column tiles the two warps of a quadrant split a stage's chunks
+    // by K step; the MMA waits until all epilogue warps have signalled.
     const int q = warp & 3;                    // tensor-memory lane quadrant of this warp
     const int h = (warp - 2) / 4;              // which 128-column half of the tile
     const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + 128 * h;
+    const uint32_t quad = (uint32_t)(32 * q) << 16;
     const float alpha = __fmul_rn(__ldg(args.sta), __ldg(args.stb));
     uint32_t acc_ph = 0;
-    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    // scale-staging cursor: the next stage (tile, k block) in this CTA's sequence
+    int sf_s = 0, sf_t = blockIdx.x, sf_kb = 0;
+    uint32_t sf_ph = 0;
+    bool ok = true;
+    auto stage_scales = [&]() {
+      int go = 1;
+      if (lane == 0) go = mbar_wait(sf_full(sf_s), sf_ph, args.timeout_ns, abort) ? 1 : 0;
+      go = __shfl_sync(0xFFFFFFFFu, go, 0);
+      if (!go) {
+        if (lane == 0) raise_timeout(args, abort);
+        ok = false;
+        return;
+      }
+      const uint32_t st = smem_u32(smem + sf_s * C::kStageBytes);
+      const uint32_t sfa_s = st + C::kABytes + C::kBBytes + 16u * lane, sfb_s = sfa_s + C::kSfaBytes;
+      const uint32_t sf_col = tmem + quad + BN + sf_s * C::kSfStageCols;
+      if (BN == 256) {
+        // this warp: K steps 2h, 2h+1 of A (columns 8h..8h+7) and of both B halves
+        // (columns 16+16h .. 16+16h+15: [B0 k][B1 k][B0 k+1][B1 k+1])
+        const uint32_t k0 = 2u * h;
+        tc_st8(sf_col + 8 * h, lds128(sfa_s + k0 * kSfChunk), lds128(sfa_s + (k0 + 1) * kSfChunk));
+        tc_st16(sf_col + 16 + 16 * h, lds128(sfb_s + k0 * kSfChunk), lds128(sfb_s + 4 * kSfChunk + k0 * kSfChunk),
+                lds128(sfb_s + (k0 + 1) * kSfChunk), lds128(sfb_s + 4 * kSfChunk + (k0 + 1) * kSfChunk));
+      } else {
+        tc_st16(sf_col, lds128(sfa_s), lds128(sfa_s + kSfChunk), lds128(sfa_s + 2 * kSfChunk),
+                lds128(sfa_s + 3 * kSfChunk));
+        tc_st16(sf_col + 16, lds128(sfb_s), lds128(sfb_s + kSfChunk), lds128(sfb_s + 2 * kSfChunk),
+                lds128(sfb_s + 3 * kSfChunk));
+      }
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sf_ready(sf_s));
+      if (++sf_kb == args.num_kb) {
+        sf_kb = 0;
+        sf_t += gridDim.x;
+      }
+      if (++sf_s == C::kStages) {
+        sf_s = 0;
+        sf_ph ^= 1u;
+      }
+    };
+    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
       const int mb = t % args.tiles_m, nb = t / args.tiles_m;
+      while (ok && sf_t == t) stage_scales();  // the rest of this tile's stages
+      if (!ok) break;
       // one lane waits and the warp follows its verdict, so the warp stays
       // converged for the .sync.aligned tensor-memory loads
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait(acc_full, acc_ph, args.timeout_ns, abort) ? 1 : 0;
-      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-      if (!ok) {
+      int go = 1;
+      if (lane == 0) go = mbar_wait(acc_full, acc_ph, args.timeout_ns, abort) ? 1 : 0;
+      go = __shfl_sync(0xFFFFFFFFu, go, 0);
+      if (!go) {
         if (lane == 0) raise_timeout(args, abort);
         break;
       }
@@ -389,6 +470,11 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty);
       acc_ph ^= 1u;
+      // the next tile's first stages are (or soon will be) loaded: give the
+      // MMA their scales before spending time on the stores.  Only that tile:
+      // its stages depend on nothing but this tile's finished MMAs, while a
+      // later tile's would wait on an accumulator this warp has yet to free.
+      for (int i = 0; i < C::kStages && ok && sf_t < n_tiles && sf_t == t + (int)gridDim.x; ++i) stage_scales();
 
       const int row = mb * kBM + 32 * q + lane;
       const int col0 = nb * BN + 128 * h;
@@ -409,7 +495,9 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
                                 __fmul_rn(__uint_as_float(v[j][8 * g + 5]), alpha));
               o.w = pack_bf16x2(__fmul_rn(__uint_as_float(v[j][8 * g + 6]), alpha),
                                 __fmul_rn(__uint_as_float(v[j][8 * g + 7]), alpha));
-              *reinterpret_cast<uint4*>(dst + 32 * j + 8 * g) = o;
+              // streaming store: C is written once, and keeping it out of
+              // L2's way keeps the operand tiles there for the next tiles
+              __stcs(reinterpret_cast<uint4*>(dst + 32 * j + 8 * g), o);
             }
           }
         }

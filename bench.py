@@ -466,10 +466,11 @@ def linear_forward(torch, fos, dev, pk) -> dict:
     except fos.FosError as e:
         return {"status": f"gemm unavailable: {e}"}
     flops = 2.0 * 8192 * 12288 * 4096
-    t = _time_calls(torch, lambda: fos.gemm(a, w, out=C), 20)
+    with ClockSampler(dev.index) as clk:
+        t = _time_calls(torch, lambda: fos.gemm(a, w, out=C), 50)
     tf = flops / (t * 1e-3) / 1e12
     fp4_peak = pk["bf16_tflops"] * 6.0  # measured bf16 burst x nominal dense fp4/bf16 ratio (13.5 / 2.25)
-    return {"gemm_ms": round(t, 4), "tflops": round(tf, 1),
+    return {"gemm_ms": round(t, 4), "tflops": round(tf, 1), "clocks": clk.summary(),
             "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                          "frac": round(tf / fp4_peak, 4),
                          "peak_source": "measured bf16 burst x 6 (nominal dense fp4/bf16 ratio)"}}
