@@ -48,6 +48,20 @@ class fos_quant_options(ctypes.Structure):
     ]
 
 
+class fos_quant_job(ctypes.Structure):
+    _fields_ = [
+        ("x", ctypes.c_void_p),
+        ("rows", ctypes.c_int64),
+        ("cols", ctypes.c_int64),
+        ("ld_x", ctypes.c_int64),
+        ("codes", ctypes.c_void_p),
+        ("ld_codes", ctypes.c_int64),
+        ("sf", ctypes.c_void_p),
+        ("tensor_scale", ctypes.c_void_p),
+        ("choice", ctypes.c_void_p),
+    ]
+
+
 class fos_nvfp4_tensor(ctypes.Structure):
     _fields_ = [
         ("codes", ctypes.c_void_p),
@@ -84,6 +98,9 @@ def _load() -> ctypes.CDLL:
         "fos_e4m3_encode": (i32, [vp, i64, vp, vp]),
         "fos_philox4x32_10": (i32, [vp, i64, u64, vp, vp]),
         "fos_selftest_wait_limits": (i32, [vp, sz, u64, vp, vp]),
+        "fos_quantize_batch_workspace_size": (i32, [i32, ctypes.POINTER(sz)]),
+        "fos_quantize_batch": (i32, [ctypes.POINTER(fos_quant_job), i32, ctypes.POINTER(fos_quant_options), vp, sz,
+                                     vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -95,7 +112,8 @@ def _load() -> ctypes.CDLL:
 _lib = _load()
 EXPORTED = ("fos_abi_version", "fos_status_string", "fos_sf_bytes", "fos_quantize_workspace_size",
             "fos_tensor_amax", "fos_quantize", "fos_quantize_noalloc", "fos_dequantize", "fos_gemm", "fos_e2m1_encode",
-            "fos_e4m3_encode", "fos_philox4x32_10", "fos_selftest_wait_limits")
+            "fos_e4m3_encode", "fos_philox4x32_10", "fos_selftest_wait_limits", "fos_quantize_batch",
+            "fos_quantize_batch_workspace_size")
 
 
 def _check(status: int, what: str) -> None:
@@ -255,6 +273,54 @@ class Quantizer:
                           self.ws_bytes, _stream_ptr(stream))
         _check(st, "fos_quantize")
         return o
+
+
+def fos_quantize_batch_workspace_size(n_jobs: int) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.fos_quantize_batch_workspace_size(n_jobs, ctypes.byref(n)), "fos_quantize_batch_workspace_size")
+    return n.value
+
+
+def fos_quantize_batch(jobs, opt: fos_quant_options, workspace, workspace_bytes, stream) -> int:
+    """Raw call: jobs is a sequence of fos_quant_job; buffers are device addresses."""
+    arr = (fos_quant_job * len(jobs))(*jobs)
+    return int(_lib.fos_quantize_batch(arr, len(jobs), ctypes.byref(opt), workspace or None, workspace_bytes, stream))
+
+
+class BatchQuantizer:
+    """Reusable outputs and workspace for repeated quantization of a fixed set
+    of row-major matrices (e.g. one layer's weights) in one chained batch."""
+
+    def __init__(self, shapes, *, device="cuda", with_choice=False, **opts):
+        torch = _torch()
+        self.opt = options(**opts)
+        self.outs = []
+        for rows, cols in shapes:
+            layout = opts.get("sf_layout", FOS_SF_SWIZZLED_128x4)
+            ldc = max(8, ((cols // 2 + 15) // 16) * 16)
+            self.outs.append(NVFP4Tensor(
+                codes=torch.empty((rows, ldc), dtype=torch.uint8, device=device),
+                sf=torch.empty(max(1, fos_sf_bytes(rows, cols, layout)), dtype=torch.uint8, device=device),
+                tensor_scale=torch.empty(1, dtype=torch.float32, device=device),
+                rows=rows, cols=cols, sf_layout=layout,
+                choice=torch.empty((rows, cols // 16), dtype=torch.uint8, device=device) if with_choice else None))
+        self.ws_bytes = fos_quantize_batch_workspace_size(len(self.outs))
+        self.workspace = torch.empty(max(1, self.ws_bytes), dtype=torch.uint8, device=device)
+        self._jobs = None
+
+    def __call__(self, xs, stream=None):
+        assert len(xs) == len(self.outs)
+        jobs = []
+        for x, o in zip(xs, self.outs):
+            assert x.dtype == _torch().bfloat16 and x.shape == (o.rows, o.cols)
+            assert x.numel() == 0 or x.stride(1) == 1
+            ld = x.stride(0) if x.numel() else max(o.cols, 8)
+            jobs.append(fos_quant_job(x.data_ptr(), o.rows, o.cols, ld, o.codes.data_ptr(),
+                                      o.codes.stride(0), o.sf.data_ptr(), o.tensor_scale.data_ptr(),
+                                      o.choice.data_ptr() if o.choice is not None else None))
+        _check(fos_quantize_batch(jobs, self.opt, self.workspace.data_ptr(), self.ws_bytes, _stream_ptr(stream)),
+               "fos_quantize_batch")
+        return self.outs
 
 
 def quantize(x, *, with_choice=False, stream=None, **opts) -> NVFP4Tensor:

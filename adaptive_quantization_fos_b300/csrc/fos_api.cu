@@ -191,6 +191,96 @@ fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
   return FOS_OK;
 }
 
+fos_status fos_quantize_batch_workspace_size(int32_t n_jobs, size_t* bytes) {
+  if (!bytes || n_jobs < 0) return FOS_ERR_INVALID_ARG;
+  *bytes = (size_t)n_jobs * fos::kBarrierOffset;  // one slot of partial maxima per job
+  return FOS_OK;
+}
+
+fos_status fos_quantize_batch(const fos_quant_job* jobs, int32_t n_jobs, const fos_quant_options* opt,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!valid_options(opt) || n_jobs < 0 || (n_jobs > 0 && !jobs)) return FOS_ERR_INVALID_ARG;
+  if (opt->transpose || opt->block_2d || opt->tensor_amax) return FOS_ERR_UNSUPPORTED;
+  if (n_jobs == 0) return FOS_OK;
+  if (!workspace || workspace_bytes < (size_t)n_jobs * fos::kBarrierOffset || !aligned(workspace, 4))
+    return FOS_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < n_jobs; ++i) {
+    const fos_quant_job& j = jobs[i];
+    if (!valid_source(j.x, j.rows, j.cols, j.ld_x, false)) return FOS_ERR_INVALID_ARG;
+    const bool empty = j.rows == 0 || j.cols == 0;
+    if ((!empty && (!j.codes || !j.sf)) || !j.tensor_scale) return FOS_ERR_INVALID_ARG;
+    if (j.ld_codes < j.cols / 2 || j.ld_codes % 8 != 0 || !aligned(j.codes, 8) || !aligned(j.sf, 4))
+      return FOS_ERR_INVALID_ARG;
+  }
+  const bool rht = opt->hadamard != 0, sr = opt->rounding == FOS_ROUND_STOCHASTIC;
+  auto slot = [&](int32_t i) {
+    return reinterpret_cast<float*>(static_cast<char*>(workspace) + (size_t)i * fos::kBarrierOffset);
+  };
+  // job 0's block maxima: the amax pass on its own
+  int n_part;
+  {
+    const fos_quant_job& j = jobs[0];
+    fos::AmaxParams a{};
+    a.x = static_cast<const uint16_t*>(j.x);
+    a.rows = j.rows;
+    a.cols = j.cols;
+    a.ld = j.ld_x;
+    a.hk0 = (uint32_t)opt->hadamard_seed;
+    a.hk1 = (uint32_t)(opt->hadamard_seed >> 32);
+    a.aligned32 = aligned(j.x, 32) && j.ld_x % 16 == 0;
+    a.partials = slot(0);
+    n_part = amax_tasks_grid(j.rows, j.cols, false);
+    if (fos::launch_amax(a, rht, false, n_part, stream) != cudaSuccess) return FOS_ERR_CUDA;
+  }
+  for (int32_t i = 0; i < n_jobs; ++i) {
+    const fos_quant_job& j = jobs[i];
+    const int64_t nb = j.cols / 16;
+    fos::QuantParams p{};
+    p.x = static_cast<const uint16_t*>(j.x);
+    p.rows = j.rows;
+    p.cols = j.cols;
+    p.ld = j.ld_x;
+    p.R = j.rows;
+    p.nb = nb;
+    p.codes = j.codes;
+    p.ld_codes = j.ld_codes;
+    p.sf = j.sf;
+    p.sf_layout = opt->sf_layout;
+    p.choice = j.choice;
+    p.tensor_scale = j.tensor_scale;
+    p.amax_src = slot(i);
+    p.n_partials = n_part;
+    p.sr_k0 = (uint32_t)opt->sr_seed;
+    p.sr_k1 = (uint32_t)(opt->sr_seed >> 32);
+    p.hk0 = (uint32_t)opt->hadamard_seed;
+    p.hk1 = (uint32_t)(opt->hadamard_seed >> 32);
+    p.aligned32 = aligned(j.x, 32) && j.ld_x % 16 == 0;
+    p.codes16 = aligned(j.codes, 16) && j.ld_codes % 16 == 0;
+    p.timeout_ns = fos::kWaitTimeoutNs;
+    if (i + 1 < n_jobs) {
+      // quantize job i while taking job i+1's block maxima
+      const fos_quant_job& nx = jobs[i + 1];
+      p.next_x = static_cast<const uint16_t*>(nx.x);
+      p.next_rows = nx.rows;
+      p.next_cols = nx.cols;
+      p.next_ld = nx.ld_x;
+      p.next_partials = slot(i + 1);
+      const int g = fos::chained_grid();
+      if (fos::launch_quant_rows_chained(p, opt->scale_rule, rht, sr, g, stream) != cudaSuccess) return FOS_ERR_CUDA;
+      n_part = g;
+    } else {
+      const int64_t tasks = j.rows * ((nb + 127) / 128);
+      if (fos::launch_quant(p, opt->scale_rule, 0, rht, sr, fos::quant_grid(tasks, 0), stream) != cudaSuccess)
+        return FOS_ERR_CUDA;
+    }
+    if (opt->sf_layout == FOS_SF_SWIZZLED_128x4 && (j.rows % 128 != 0 || nb % 4 != 0)) {
+      if (fos::launch_sf_pad(j.sf, sf_bytes_of(j.rows, nb, opt->sf_layout), j.rows, nb, stream) != cudaSuccess)
+        return FOS_ERR_CUDA;
+    }
+  }
+  return FOS_OK;
+}
+
 fos_status fos_dequantize(const fos_nvfp4_tensor* q, void* out, int32_t out_dtype, int64_t ld_out,
                           cudaStream_t stream) {
   if (!q || !out || !q->codes || !q->sf || !q->tensor_scale) return FOS_ERR_INVALID_ARG;

@@ -45,6 +45,11 @@ struct QuantParams {
   unsigned int* ws_barrier;
   unsigned int barrier_extra;  // arrivals beyond the grid the barrier waits for (0; 1 only in the self-test)
   uint64_t timeout_ns;         // limit of every device wait (copies, the grid barrier)
+  // chained row quantizer: the next job of a batch, whose block maxima this
+  // launch also takes (one partial per CTA into next_partials)
+  const uint16_t* next_x;
+  int64_t next_rows, next_cols, next_ld;
+  float* next_partials;
 };
 
 // Default limit of a device wait: a copy or barrier that takes a second has failed.
@@ -64,6 +69,10 @@ int quant_grid(int64_t n_warp_tasks, int kind);
 cudaError_t launch_amax(const AmaxParams& p, bool hadamard, bool transpose, int grid, cudaStream_t s);
 // kind: 0 rows (1D), 1 cols (1D transposed), 2 2D, 3 2D transposed
 cudaError_t launch_quant(const QuantParams& p, int rule, int kind, bool rht, bool sr, int grid, cudaStream_t s);
+// Rows (1D) quantized from partials of an earlier launch while 2 extra warps
+// per CTA take the block maxima of the next job (p.next_*); grid = chained_grid().
+cudaError_t launch_quant_rows_chained(const QuantParams& p, int rule, bool rht, bool sr, int grid, cudaStream_t s);
+int chained_grid();
 // Rows (1D) with the tensor amax computed in the same launch: a cooperative
 // launch of as many CTAs as fit on the GPU at once.
 cudaError_t launch_quant_rows_fused(const QuantParams& p, int rule, bool rht, bool sr, int64_t n_tasks,

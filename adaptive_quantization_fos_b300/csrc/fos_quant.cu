@@ -216,6 +216,11 @@ constexpr int kRowWarps = 8;
 constexpr int kRowSlots = 2;
 constexpr int kRowSlotBytes = 128 * 32;
 constexpr int kRowSmemBytes = kRowWarps * kRowSlots * kRowSlotBytes;
+// chained mode: 2 more warps per CTA stream the next job's input for its
+// amax through rings of 4 slots each
+constexpr int kAmaxWarps = 2;
+constexpr int kAmaxSlots = 4;
+constexpr int kChainSmemBytes = kRowSmemBytes + kAmaxWarps * kAmaxSlots * kRowSlotBytes;
 
 template <int RULE, bool SR>
 __device__ __forceinline__ void quant_block_tab(const uint64_t (&yp)[8], float ab, const TensorConsts& tc,
@@ -277,20 +282,139 @@ __device__ __forceinline__ void quant_block_tab(const uint64_t (&yp)[8], float a
   sf = four ? sf4 : sf6;
 }
 
-// FUSED: the tensor amax is computed in the same launch.  Pass 1 reads every
-// task once for its block maxima (keeping the lines in L2), one partial per
-// CTA goes to the workspace, a grid barrier (all CTAs resident: cooperative
-// launch) publishes them, and pass 2 quantizes, re-reading the input mostly
-// from L2 when the matrix fits there.
-template <int RULE, bool RHT, bool SR, bool FUSED>
-__global__ void __launch_bounds__(256, SR ? 2 : 3) quant_rows_kernel(QuantParams p) {
+// Block maxima of the next job of a batch, by the kAmaxWarps extra warps of a
+// chained launch: tasks of 2048 values stream through each warp's ring of
+// bulk-copy slots; the CTA's maximum (as bits: non-negative floats order like
+// their bit patterns) goes to p.next_partials[blockIdx.x] once both warps are
+// done.  A copy that outlasts the time limit makes the partial NaN.
+template <bool RHT>
+__device__ __forceinline__ void next_job_amax(const QuantParams& p, uint8_t* ring, uint64_t* bars, int aw, int lane,
+                                              uint32_t rht_mask, unsigned int* s_max, unsigned int* s_done) {
+  const int64_t nb = p.next_cols >> 4;
+  const int64_t wpr = (nb + 127) >> 7;
+  const int64_t nwarps = (int64_t)gridDim.x * kAmaxWarps;
+  const int64_t gw = (int64_t)blockIdx.x * kAmaxWarps + aw;
+  const int64_t R = nb > 0 ? p.next_rows : 0;
+  const int64_t dr = nwarps / (wpr > 0 ? wpr : 1), dch = nwarps - dr * (wpr > 0 ? wpr : 1);
+  uint8_t* slots = ring + aw * (kAmaxSlots * kRowSlotBytes);
+  const uint32_t bar0 = smem_addr(&bars[aw * kAmaxSlots]);
+  const uint64_t keep = l2_policy_evict_last();  // the job's own launch reads it next
+  float m = 0.0f;
+  if (wpr > 0) {
+    int64_t pr = gw / wpr, pch = gw - pr * wpr;
+    auto issue_next = [&](int slot) -> bool {
+      if (pr >= R) return false;
+      const int64_t c0 = pch * 128;
+      const int64_t nblk = nb - c0 < 128 ? nb - c0 : 128;
+      bulk_g2s_hint(smem_addr(slots + slot * kRowSlotBytes), p.next_x + pr * p.next_ld + c0 * 16,
+                    (uint32_t)(nblk * 32), bar0 + 8u * slot, keep);
+      pr += dr;
+      pch += dch;
+      if (pch >= wpr) {
+        pch -= wpr;
+        ++pr;
+      }
+      return true;
+    };
+    int issued = 0, consumed = 0;
+    if (lane == 0)
+      for (int k = 0; k < kAmaxSlots; ++k) issued += issue_next(k) ? 1 : 0;
+    int slot = 0;
+    uint32_t ph = 0;
+    bool failed = false;
+    int64_t r = gw / wpr, ch = gw - r * wpr;
+    for (; r < R; r += dr, ch += dch) {
+      if (ch >= wpr) {
+        ch -= wpr;
+        if (++r >= R) break;
+      }
+      const int64_t c0 = ch * 128;
+      const int nblk = nb - c0 < 128 ? (int)(nb - c0) : 128;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait_for(bar0 + 8u * slot, ph, p.timeout_ns))) {
+        failed = true;
+        break;
+      }
+      uint32_t wv[4][8];
+      const uint8_t* src = slots + slot * kRowSlotBytes + lane * 32;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (lane + 32 * j < nblk) {
+          const uint4 a = *reinterpret_cast<const uint4*>(src + 1024 * j);
+          const uint4 b = *reinterpret_cast<const uint4*>(src + 1024 * j + 16);
+          wv[j][0] = a.x; wv[j][1] = a.y; wv[j][2] = a.z; wv[j][3] = a.w;
+          wv[j][4] = b.x; wv[j][5] = b.y; wv[j][6] = b.z; wv[j][7] = b.w;
+        }
+      }
+      __syncwarp();
+      ++consumed;
+      if (lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issued += issue_next(slot) ? 1 : 0;
+      }
+      if (++slot == kAmaxSlots) {
+        slot = 0;
+        ph ^= 1u;
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (lane + 32 * j >= nblk) break;
+        if (RHT) {
+          float y[16];
+          unpack16(wv[j], rht_mask, y);
+          hadamard16(y);
+          m = fmaxf(m, absmax16(y));
+        } else {
+          m = fmaxf(m, absmax16_bf16(wv[j]));
+        }
+      }
+    }
+    if (failed) m = __int_as_float(0x7FC00000);
+    if (lane == 0) {
+      for (; consumed < issued; ++consumed) {
+        mbar_wait_for(bar0 + 8u * slot, ph, p.timeout_ns);
+        if (++slot == kAmaxSlots) {
+          slot = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+  }
+  m = warp_max(m);
+  if (lane == 0) {
+    atomicMax(s_max, __float_as_uint(m));
+    __threadfence_block();
+    if (atomicAdd(s_done, 1u) == kAmaxWarps - 1) p.next_partials[blockIdx.x] = __uint_as_float(atomicMax(s_max, 0u));
+  }
+}
+
+// MODE kRowsPlain: the tensor amax is supplied, or reduced from partials a
+// previous launch wrote.
+// MODE kRowsFused: the tensor amax is computed in the same launch.  Pass 1
+// reads every task once for its block maxima (keeping the lines in L2), one
+// partial per CTA goes to the workspace, a grid barrier (all CTAs resident:
+// cooperative launch) publishes them, and pass 2 quantizes, re-reading the
+// input mostly from L2 when the matrix fits there.
+// MODE kRowsChained: as kRowsPlain, and 2 extra warps per CTA take the block
+// maxima of the NEXT job of a batch meanwhile (memory-bound work beside the
+// issue-bound quantization), leaving one partial per CTA for that job's launch.
+constexpr int kRowsPlain = 0, kRowsFused = 1, kRowsChained = 2;
+
+template <int RULE, bool RHT, bool SR, int MODE>
+__global__ void __launch_bounds__(MODE == kRowsChained ? 320 : 256, MODE == kRowsChained ? 2 : (SR ? 2 : 3))
+    quant_rows_kernel(QuantParams p) {
+  constexpr bool FUSED = MODE == kRowsFused;
   extern __shared__ __align__(128) uint8_t q_smem[];
   __shared__ float s_red[33];
   __shared__ float2 s_tab[128];
-  __shared__ uint64_t s_bar[kRowWarps * kRowSlots];
+  __shared__ uint64_t s_bar[kRowWarps * kRowSlots + kAmaxWarps * kAmaxSlots];
   __shared__ int s_ok;
+  __shared__ unsigned int s_next_max, s_next_done;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x < kRowWarps * kRowSlots) mbar_init(smem_addr(&s_bar[threadIdx.x]), 1);
+  if (threadIdx.x < kRowWarps * kRowSlots + kAmaxWarps * kAmaxSlots) mbar_init(smem_addr(&s_bar[threadIdx.x]), 1);
+  if (threadIdx.x == 0) {
+    s_next_max = 0u;
+    s_next_done = 0u;
+  }
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   const uint32_t rht_mask = RHT ? rht_sign_mask(p.hk0, p.hk1) : 0u;
   const int64_t nb = p.nb;
@@ -352,6 +476,11 @@ __global__ void __launch_bounds__(256, SR ? 2 : 3) quant_rows_kernel(QuantParams
   }
   build_scale_table(tc.s_t, s_tab);
   __syncthreads();
+  if (MODE == kRowsChained && warp >= kRowWarps) {
+    next_job_amax<RHT>(p, q_smem + kRowSmemBytes, &s_bar[kRowWarps * kRowSlots], warp - kRowWarps, lane, rht_mask,
+                       &s_next_max, &s_next_done);
+    return;
+  }
   const uint64_t stream_once = l2_policy_evict_first();
   const bool swz = p.sf_layout == FOS_SF_SWIZZLED_128x4;
   const int64_t n_ct = (nb + 3) >> 2;
@@ -727,11 +856,11 @@ static void launch_q(const QuantParams& p, int kind, int grid, cudaStream_t s) {
     case 0: {
       static bool attr = false;  // benign race: the attribute is idempotent
       if (!attr) {
-        cudaFuncSetAttribute(quant_rows_kernel<RULE, RHT, SR, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kRowSmemBytes);
+        cudaFuncSetAttribute(quant_rows_kernel<RULE, RHT, SR, kRowsPlain>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kRowSmemBytes);
         attr = true;
       }
-      quant_rows_kernel<RULE, RHT, SR, false><<<grid, 256, kRowSmemBytes, s>>>(p);
+      quant_rows_kernel<RULE, RHT, SR, kRowsPlain><<<grid, 256, kRowSmemBytes, s>>>(p);
       break;
     }
     case 1: quant_cols_kernel<RULE, RHT, SR><<<grid, 256, 0, s>>>(p); break;
@@ -761,7 +890,7 @@ int quant_grid(int64_t n_warp_tasks, int kind) {
 
 template <int RULE, bool RHT, bool SR>
 static cudaError_t launch_rows_fused(const QuantParams& p, int64_t n_tasks, cudaStream_t s) {
-  auto fn = quant_rows_kernel<RULE, RHT, SR, true>;
+  auto fn = quant_rows_kernel<RULE, RHT, SR, kRowsFused>;
   static int per_sm = 0;  // benign race: every thread computes the same value
   if (per_sm == 0) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowSmemBytes);
@@ -790,6 +919,36 @@ static cudaError_t launch_rows_fused_rule(const QuantParams& p, bool rht, bool s
                                           cudaStream_t s) {
   if (rht) return sr ? launch_rows_fused<RULE, true, true>(p, n_tasks, s) : launch_rows_fused<RULE, true, false>(p, n_tasks, s);
   return sr ? launch_rows_fused<RULE, false, true>(p, n_tasks, s) : launch_rows_fused<RULE, false, false>(p, n_tasks, s);
+}
+
+template <int RULE, bool RHT, bool SR>
+static cudaError_t launch_rows_chained(const QuantParams& p, int grid, cudaStream_t s) {
+  auto fn = quant_rows_kernel<RULE, RHT, SR, kRowsChained>;
+  static bool attr = false;  // benign race: the attribute is idempotent
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kChainSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  fn<<<grid, 32 * (kRowWarps + kAmaxWarps), kChainSmemBytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+int chained_grid() {
+  int g = sm_count() * 2;
+  return g > kMaxAmaxPartials ? kMaxAmaxPartials : g;
+}
+
+cudaError_t launch_quant_rows_chained(const QuantParams& p, int rule, bool rht, bool sr, int grid, cudaStream_t s) {
+#define FOS_CHAIN(R)                                                                                        \
+  return rht ? (sr ? launch_rows_chained<R, true, true>(p, grid, s) : launch_rows_chained<R, true, false>(p, grid, s)) \
+             : (sr ? launch_rows_chained<R, false, true>(p, grid, s) : launch_rows_chained<R, false, false>(p, grid, s))
+  switch (rule) {
+    case FOS_SCALE_6: FOS_CHAIN(FOS_SCALE_6);
+    case FOS_SCALE_4: FOS_CHAIN(FOS_SCALE_4);
+    default: FOS_CHAIN(FOS_SCALE_4OVER6);
+  }
+#undef FOS_CHAIN
 }
 
 cudaError_t launch_quant_rows_fused(const QuantParams& p, int rule, bool rht, bool sr, int64_t n_tasks,

@@ -45,7 +45,7 @@ WORKLOAD = ("qwen3-8b layer weights q,k,v,o,gate,up,down (192.9M bf16 values, St
 BYTES_PER_ELEM_QUANT = 2.0 + 0.5 + 1.0 / 16.0  # read bf16, write 4-bit code + 1/16 E4M3 scale
 CPU_SAMPLE_ROWS = 2048  # rows of each matrix timed on the host for the CPU baseline
 REF_SAMPLE_ROWS = 256  # rows of each matrix per step of the reference arm
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "quant_rows_one_launch_traffic.txt")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "quant_rows_chained_traffic.txt")
 
 
 def peaks() -> dict:
@@ -264,19 +264,22 @@ def run_fos(args, dist: Dist) -> None:
     pk = peaks()
 
     mats_np = workloads.qwen3_8b_weights()
-    mats = {k: _to_dev(torch, v, dev) for k, v in mats_np.items()}
-    qs = {k: fos.Quantizer(*v.shape, device=dev) for k, v in mats.items()}
+    # one batch per step, smallest matrix first (each launch takes the next
+    # matrix's amax beside the current matrix's quantization)
+    order = sorted(mats_np, key=lambda k: mats_np[k].size)
+    mats = {k: _to_dev(torch, mats_np[k], dev) for k in order}
+    bq = fos.BatchQuantizer([mats[k].shape for k in order], device=dev)
+    xs = [mats[k] for k in order]
     elems = sum(v.numel() for v in mats.values())
-    launches_per_step = 0
-    for k in qs:
+    launches_per_step = 1  # the first matrix's amax pass
+    for k in order:
         r, c = mats[k].shape
-        # one cooperative launch (amax pass + quantize pass), plus the pad fill
-        # of the scale layout when the shape leaves padding
+        # one quantize launch per matrix (chained), plus the pad fill of the
+        # scale layout when the shape leaves padding
         launches_per_step += 1 + (1 if (r % 128 or (c // 16) % 4) else 0)
 
     def step():
-        for k, q in qs.items():
-            q(mats[k])
+        bq(xs)
 
     for _ in range(args.warmup):
         step()
@@ -296,36 +299,37 @@ def run_fos(args, dist: Dist) -> None:
     ms_per_step = t_ms / args.steps
     value = dist.world * elems * args.steps / (t_ms * 1e-3) / 1e9
 
-    # the dominant kernel of the step (the one-launch quantizer: amax pass and
-    # quantize pass), one CUDA-event pair per launch on the launching stream,
-    # over a second run of the same steps right after the timed region
+    # the step's kernels (the batch: the first matrix's amax pass and one
+    # chained quantize launch per matrix), one CUDA-event pair per step on the
+    # launching stream, over a second run of the same steps right after the
+    # timed region
     reps = max(3, min(args.steps, 100))
-    ev = _events(torch, 2 * reps * len(mats))
-    i = 0
+    ev = _events(torch, 2 * reps)
     torch.cuda.synchronize()
-    for _ in range(reps):
-        for k, q in qs.items():
-            ev[i].record(stream)
-            q(mats[k])
-            ev[i + 1].record(stream)
-            i += 2
+    for i in range(reps):
+        ev[2 * i].record(stream)
+        step()
+        ev[2 * i + 1].record(stream)
     torch.cuda.synchronize()
     tot_t = sum(ev[j].elapsed_time(ev[j + 1]) for j in range(0, len(ev), 2))
     n_launch = reps * len(mats)
     achieved = elems * reps * BYTES_PER_ELEM_QUANT / (tot_t * 1e-3) / 1e9
     tpe = recorded_traffic_per_elem()
-    roofline = {"bound": "hbm", "kernel": "quant_rows_kernel<4/6, RNE, 1D, one launch> (amax pass + quantize pass)",
+    roofline = {"bound": "hbm",
+                "kernel": "quant_rows_kernel<4/6, RNE, 1D, chained> batch: per step 1 amax launch + 7 quantize "
+                          "launches, each taking the next matrix's amax beside its quantization",
                 "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / pk["hbm_gbs"], 4),
                 "peak_source": pk["source"] + " copy bandwidth (hbm_gbs), burst",
                 "bytes_per_elem": BYTES_PER_ELEM_QUANT,
                 "traffic": None if tpe is None else round(tpe * elems / len(mats)),
-                "traffic_note": "DRAM read+write bytes per launch (average over the 7 launches), scaled by values "
+                "traffic_note": "DRAM read+write bytes per quantize launch (average over the 7), scaled by values "
                                 "from the committed ncu capture of the same kernel" if tpe else "no current capture",
                 "algorithmic_bytes_per_launch": round(BYTES_PER_ELEM_QUANT * elems / len(mats)),
-                "avg_launch_us": round(tot_t / n_launch * 1e3, 2)}
+                "avg_launch_us": round(tot_t / n_launch * 1e3, 2),
+                "timed": "per step (the 8 launches of one batch), averaged over launches"}
 
-    # context: the quantize pass alone (amax supplied), same per-launch timing
+    # context: the quantize pass alone (amax supplied), per-launch timing
     amax = {k: fos.tensor_amax(v) for k, v in mats.items()}
     qk = {k: fos.Quantizer(*v.shape, device=dev, tensor_amax=amax[k]) for k, v in mats.items()}
     for k in mats:
@@ -521,7 +525,16 @@ def run_case(args) -> None:
     import adaptive_quantization_fos_b300 as fos
 
     dev = torch.device("cuda", 0)
-    if args.case == "quant_rows_one_launch":
+    if args.case == "quant_rows_chained":
+        # the Qwen3-8B layer weight set as one batch (smallest first): the
+        # chained quantize launches
+        mats = workloads.qwen3_8b_weights()
+        order = sorted(mats, key=lambda k: mats[k].size)
+        xs = [_to_dev(torch, mats[k], dev) for k in order]
+        bq = fos.BatchQuantizer([x.shape for x in xs], device=dev)
+        for _ in range(2):
+            bq(xs)
+    elif args.case == "quant_rows_one_launch":
         # 12288 x 4096 bf16 (100.7 MB, the gate/up projection shape), no amax
         # supplied: the one-launch quantizer (amax pass, barrier, quantize pass)
         x = _to_dev(torch, workloads.student_t(12288, 4096, seed=9002), dev)

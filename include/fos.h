@@ -166,6 +166,39 @@ fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
                         float* tensor_scale, uint8_t* choice, void* workspace, size_t workspace_bytes,
                         cudaStream_t stream);
 
+/* One matrix of a batch (fos_quantize_batch): source and outputs as in
+ * fos_quantize, with blocks along the rows (no transpose, no 2D tiles). */
+typedef struct fos_quant_job {
+  const void* x;        /* device bf16 [rows, cols], row stride ld_x elements */
+  int64_t rows, cols, ld_x;
+  uint8_t* codes;       /* device, rows x ld_codes bytes */
+  int64_t ld_codes;
+  uint8_t* sf;          /* device, fos_sf_bytes(rows, cols, opt->sf_layout) bytes */
+  float* tensor_scale;  /* device float: the job's s_t */
+  uint8_t* choice;      /* optional device [rows][cols/16] bytes, or NULL */
+} fos_quant_job;
+
+/* Device scratch fos_quantize_batch needs for n_jobs jobs (8 KiB per job). */
+fos_status fos_quantize_batch_workspace_size(int32_t n_jobs, size_t* bytes);
+
+/*
+ * fos_quantize_batch -- quantize n_jobs matrices (a layer's weight set, say)
+ * with the same options, each with its own tensor amax; results identical to
+ * one fos_quantize call per job.  The launches are chained so that each
+ * job's memory-bound amax pass runs beside the issue-bound quantization of
+ * the job before it: launch 0 takes job 0's block maxima, launch i+1
+ * quantizes job i while 2 extra warps per CTA take job i+1's block maxima,
+ * and the last launch quantizes the last job.  Order the jobs by size,
+ * smallest first, to overlap the most.
+ *   opt       shared options; transpose, block_2d and tensor_amax are not
+ *             supported here (FOS_ERR_UNSUPPORTED; use fos_quantize).
+ *   workspace device scratch of fos_quantize_batch_workspace_size() bytes,
+ *             4-byte aligned, no initialisation needed.
+ * Validation covers every job before anything is enqueued.
+ */
+fos_status fos_quantize_batch(const fos_quant_job* jobs, int32_t n_jobs, const fos_quant_options* opt,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /*
  * fos_quantize_noalloc -- fos_quantize for callers that cannot allocate
  * device memory (plugin hosts and inference runtimes that give an operator
