@@ -209,7 +209,7 @@ __device__ __forceinline__ uint32_t cand_rne8(const uint64_t (&y)[4], uint64_t i
       ".reg .b64 q0, q1, q2, q3, r0, r1, r2, r3;\n\t"
       ".reg .f32 x0, x1, x2, x3, x4, x5, x6, x7, e0, e1, e2, e3, e4, e5, e6, e7;\n\t"
       ".reg .b8 c0, c1, c2, c3;\n\t"
-      ".reg .b32 h0, h1, h2, h3, u0, u1, u2, u3, t0, t1;\n\t"
+      ".reg .b32 h0, h1, h2, h3;\n\t"
       ".reg .b16 l0, g0, l1, g1, l2, g2, l3, g3, m1;\n\t"
       "mul.rn.f32x2 q0, %2, %6;\n\t"
       "mul.rn.f32x2 q1, %3, %6;\n\t"
@@ -239,10 +239,7 @@ __device__ __forceinline__ uint32_t cand_rne8(const uint64_t (&y)[4], uint64_t i
       "fma.rn.f32x2 %1, r1, r1, %1;\n\t"
       "fma.rn.f32x2 %1, r2, r2, %1;\n\t"
       "fma.rn.f32x2 %1, r3, r3, %1;\n\t"
-      "cvt.u32.u8 u0, c0;\n\tcvt.u32.u8 u1, c1;\n\tcvt.u32.u8 u2, c2;\n\tcvt.u32.u8 u3, c3;\n\t"
-      "mad.lo.u32 t0, u1, 256, u0;\n\t"
-      "mad.lo.u32 t1, u3, 256, u2;\n\t"
-      "mad.lo.u32 %0, t1, 65536, t0;\n\t}"
+      "mov.b32 %0, {c0, c1, c2, c3};\n\t}"
       : "=r"(word), "+l"(acc)
       : "l"(y[0]), "l"(y[1]), "l"(y[2]), "l"(y[3]), "l"(inv2));
   return word;

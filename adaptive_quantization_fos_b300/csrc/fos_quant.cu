@@ -483,6 +483,8 @@ __global__ void __launch_bounds__(MODE == kRowsChained ? 320 : 256, MODE == kRow
   }
   const uint64_t stream_once = l2_policy_evict_first();
   const bool swz = p.sf_layout == FOS_SF_SWIZZLED_128x4;
+  const int64_t sf_step = swz ? 4096 : 32;
+  const bool want_choice = p.choice != nullptr;
   const int64_t n_ct = (nb + 3) >> 2;
   uint8_t* slots = q_smem + warp * (kRowSlots * kRowSlotBytes);
   const uint32_t bar0 = smem_addr(&s_bar[warp * kRowSlots]);
@@ -527,9 +529,10 @@ __global__ void __launch_bounds__(MODE == kRowsChained ? 320 : 256, MODE == kRow
     const uint8_t* src = slots + slot * kRowSlotBytes + lane * 32;
     const int64_t b_lane = c0 + lane;
     uint8_t* code_dst = p.codes + r * p.ld_codes + b_lane * 8;
-    const int64_t sf_lane = swz ? ((((r >> 7) * n_ct + (b_lane >> 2)) << 9) + ((r & 31) << 4) +
-                                   (((r >> 5) & 3) << 2) + (b_lane & 3))
-                                : r * nb + b_lane;
+    uint8_t* sf_dst = p.sf + (swz ? ((((r >> 7) * n_ct + (b_lane >> 2)) << 9) + ((r & 31) << 4) +
+                                     (((r >> 5) & 3) << 2) + (b_lane & 3))
+                                  : r * nb + b_lane);
+    uint8_t* choice_dst = want_choice ? p.choice + r * nb + b_lane : nullptr;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       if (lane + 32 * j >= nblk) break;
@@ -561,8 +564,8 @@ __global__ void __launch_bounds__(MODE == kRowsChained ? 320 : 256, MODE == kRow
       quant_block_tab<RULE, SR>(yp, ab, tc, s_tab, w, lo, hi, sf, four);
       *reinterpret_cast<uint2*>(code_dst + 256 * j) = make_uint2(lo, hi);
       // 32 blocks further along a row: 8 swizzled tiles (4096 bytes) further
-      p.sf[sf_lane + (swz ? 4096 * j : 32 * j)] = (uint8_t)sf;
-      if (p.choice) p.choice[r * nb + b_lane + 32 * j] = four ? 1 : 0;
+      sf_dst[sf_step * j] = (uint8_t)sf;
+      if (want_choice) choice_dst[32 * j] = four ? 1 : 0;
     }
     __syncwarp();
     ++consumed;
