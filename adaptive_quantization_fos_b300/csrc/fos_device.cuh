@@ -117,60 +117,6 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
   return r;
 }
 
-// One byte of two codes -> (residual lo, residual hi) = (qlo - g(lo code),
-// qhi - g(hi code)), each one FP32 rounding; also returns the byte.  The code
-// values are decoded exactly to f16 and subtracted with a mixed-precision FMA
-// (g * -1 + q).
-__device__ __forceinline__ uint32_t e2m1x2_residual(float qlo, float qhi, float& rlo, float& rhi) {
-  uint32_t byte;
-  asm("{\n\t.reg .b8 c;\n\t.reg .b32 h;\n\t.reg .b16 hl, hh, m1;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 c, %4, %3;\n\t"
-      "cvt.rn.f16x2.e2m1x2 h, c;\n\t"
-      "mov.b32 {hl, hh}, h;\n\t"
-      "mov.b16 m1, 0xBC00;\n\t"
-      "fma.rn.f32.f16 %0, hl, m1, %3;\n\t"
-      "fma.rn.f32.f16 %1, hh, m1, %4;\n\t"
-      "cvt.u32.u8 %2, c;\n\t}"
-      : "=f"(rlo), "=f"(rhi), "=r"(byte)
-      : "f"(qlo), "f"(qhi));
-  return byte;
-}
-
-// RNE codes of 8 consecutive values in one word, and their 8 residuals q - g (each exact: g is the nearest grid value or the
-// saturation bound, so the difference is representable).  Byte k of the word
-// holds the codes of q[2k] (low nibble) and q[2k+1].
-__device__ __forceinline__ uint32_t e2m1x8_residual(const float (&q)[8], float (&r)[8]) {
-  uint32_t word;
-  asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\t.reg .b32 h0, h1, h2, h3, t0, t1, u0, u1, u2, u3;\n\t"
-      ".reg .b16 l0, g0, l1, g1, l2, g2, l3, g3, m1;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 c0, %10, %9;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 c1, %12, %11;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 c2, %14, %13;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 c3, %16, %15;\n\t"
-      "cvt.rn.f16x2.e2m1x2 h0, c0;\n\t"
-      "cvt.rn.f16x2.e2m1x2 h1, c1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 h2, c2;\n\t"
-      "cvt.rn.f16x2.e2m1x2 h3, c3;\n\t"
-      "mov.b32 {l0, g0}, h0;\n\tmov.b32 {l1, g1}, h1;\n\tmov.b32 {l2, g2}, h2;\n\tmov.b32 {l3, g3}, h3;\n\t"
-      "mov.b16 m1, 0xBC00;\n\t"
-      "fma.rn.f32.f16 %1, l0, m1, %9;\n\t"
-      "fma.rn.f32.f16 %2, g0, m1, %10;\n\t"
-      "fma.rn.f32.f16 %3, l1, m1, %11;\n\t"
-      "fma.rn.f32.f16 %4, g1, m1, %12;\n\t"
-      "fma.rn.f32.f16 %5, l2, m1, %13;\n\t"
-      "fma.rn.f32.f16 %6, g2, m1, %14;\n\t"
-      "fma.rn.f32.f16 %7, l3, m1, %15;\n\t"
-      "fma.rn.f32.f16 %8, g3, m1, %16;\n\t"
-      "cvt.u32.u8 u0, c0;\n\tcvt.u32.u8 u1, c1;\n\tcvt.u32.u8 u2, c2;\n\tcvt.u32.u8 u3, c3;\n\t"
-      "prmt.b32 t0, u0, u1, 0x0040;\n\t"
-      "prmt.b32 t1, u2, u3, 0x0040;\n\t"
-      "prmt.b32 %0, t0, t1, 0x5410;\n\t}"
-      : "=r"(word), "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]),
-        "=f"(r[7])
-      : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
-  return word;
-}
-
 // ------------------------------------------------ float pairs in 64 bits
 // A value pair (element 2k in the low half) kept in one 64-bit register, the
 // operand form of the packed f32x2 instructions.
@@ -448,50 +394,11 @@ __device__ __forceinline__ TensorConsts tensor_consts(float amax) {
   return t;
 }
 
-// ------------------------------------------------------------ per block
-// The two candidate scales of a block with magnitude max `ab`.
-struct Cands {
-  uint32_t sf6, sf4;   // E4M3 bytes
-  float eff6, eff4;    // float(sf) * s_t
-  float inv6, inv4;    // min(1/eff, FLT_MAX), or 0 when sf == 0
-};
-
-__device__ __forceinline__ Cands candidates(float ab, const TensorConsts& tc) {
-  Cands c;
-  uint32_t pair = e4m3x2(__fmul_rn(ab, tc.k6), __fmul_rn(ab, tc.k4));
-  c.sf6 = pair & 0xFFu;
-  c.sf4 = pair >> 8;
-  F2 v = e4m3x2_decode(pair);
-  F2 e = mul2(v, F2{tc.s_t, tc.s_t});
-  c.eff6 = e.x;
-  c.eff4 = e.y;
-  c.inv6 = c.sf6 ? fminf(__frcp_rn(c.eff6), FLT_MAX) : 0.0f;
-  c.inv4 = c.sf4 ? fminf(__frcp_rn(c.eff4), FLT_MAX) : 0.0f;
-  return c;
-}
-
 // Fixed-order sum of 16 squares: FMA chains over even and odd positions, then one add.
 __device__ __forceinline__ float sumsq16(const float (&r)[16]) {
   F2 acc{0.0f, 0.0f};
 #pragma unroll
   for (int k = 0; k < 8; ++k) acc = fma2(F2{r[2 * k], r[2 * k + 1]}, F2{r[2 * k], r[2 * k + 1]}, acc);
-  return __fadd_rn(acc.x, acc.y);
-}
-
-// RNE codes of one candidate for 16 values: returns the scaled-domain sum of
-// squared residuals and the 8 code bytes in (lo, hi) words.
-__device__ __forceinline__ float cand_rne16(const float (&y)[16], float inv, uint32_t& lo, uint32_t& hi) {
-  F2 acc{0.0f, 0.0f};
-  uint32_t b[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    F2 q = mul2(F2{y[2 * k], y[2 * k + 1]}, F2{inv, inv});
-    F2 r;
-    b[k] = e2m1x2_residual(q.x, q.y, r.x, r.y);
-    acc = fma2(r, r, acc);
-  }
-  lo = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-  hi = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
   return __fadd_rn(acc.x, acc.y);
 }
 
@@ -527,36 +434,10 @@ __device__ __forceinline__ float cand_sr16(const float (&y)[16], float inv, cons
   return __fadd_rn(acc.x, acc.y);
 }
 
-// RNE codes of one candidate for 16 values, from a per-tensor table entry:
-// same arithmetic as cand_rne16, 8 values per conversion group.
-__device__ __forceinline__ float cand_rne16_packed(const float (&y)[16], float inv, uint32_t& lo, uint32_t& hi) {
-  F2 acc{0.0f, 0.0f};
-  float q[8], r[8];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    F2 t = mul2(F2{y[2 * k], y[2 * k + 1]}, F2{inv, inv});
-    q[2 * k] = t.x;
-    q[2 * k + 1] = t.y;
-  }
-  lo = e2m1x8_residual(q, r);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) acc = fma2(F2{r[2 * k], r[2 * k + 1]}, F2{r[2 * k], r[2 * k + 1]}, acc);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    F2 t = mul2(F2{y[8 + 2 * k], y[9 + 2 * k]}, F2{inv, inv});
-    q[2 * k] = t.x;
-    q[2 * k + 1] = t.y;
-  }
-  hi = e2m1x8_residual(q, r);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) acc = fma2(F2{r[2 * k], r[2 * k + 1]}, F2{r[2 * k], r[2 * k + 1]}, acc);
-  return __fadd_rn(acc.x, acc.y);
-}
-
 // Per-tensor table over the 128 non-negative finite E4M3 bytes b (0x7F is NaN
 // and never produced): x = min(1/eff, FLT_MAX) (0 for b = 0) and y = eff*eff,
-// eff = float(b) * s_t -- the same roundings as candidates() and the error
-// scaling, computed once per CTA instead of twice per block.
+// eff = float(b) * s_t, each one IEEE rounding -- the candidate's reciprocal
+// scale and the factor of its error, computed once per CTA instead of per block.
 __device__ __forceinline__ void build_scale_table(float s_t, float2* tab) {
   for (int b = threadIdx.x; b < 128; b += blockDim.x) {
     const float v = e4m3x2_decode((uint32_t)b).x;

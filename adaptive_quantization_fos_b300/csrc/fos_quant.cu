@@ -160,36 +160,6 @@ __device__ __forceinline__ TensorConsts quant_prologue(const QuantParams& p, flo
   return tc;
 }
 
-// One candidate's squared error given its row residual sum S (or the raw
-// sum of squares when its scale is 0).
-__device__ __forceinline__ float cand_err(float S, uint32_t sf, float eff, const float (&y)[16]) {
-  if (sf == 0) return sumsq16(y);
-  return __fmul_rn(S, __fmul_rn(eff, eff));
-}
-
-template <bool SR>
-__device__ __forceinline__ float cand16(const float (&y)[16], float inv, const uint32_t (&w)[16], uint32_t& lo,
-                                        uint32_t& hi) {
-  if (SR) return cand_sr16(y, inv, w, lo, hi);
-  return cand_rne16(y, inv, lo, hi);
-}
-
-// Quantize one 1D block of 16 transformed values: result codes/scale/choice.
-template <int RULE, bool SR>
-__device__ __forceinline__ void quant_block(const float (&y)[16], float ab, const TensorConsts& tc,
-                                            const uint32_t (&w)[16], uint32_t& lo, uint32_t& hi, uint32_t& sf,
-                                            bool& four) {
-  Cands c = candidates(ab, tc);
-  uint32_t lo6 = 0, hi6 = 0, lo4 = 0, hi4 = 0;
-  float E6 = 0.0f, E4 = 0.0f;
-  if (RULE != FOS_SCALE_4) E6 = cand_err(cand16<SR>(y, c.inv6, w, lo6, hi6), c.sf6, c.eff6, y);
-  if (RULE != FOS_SCALE_6) E4 = cand_err(cand16<SR>(y, c.inv4, w, lo4, hi4), c.sf4, c.eff4, y);
-  four = (RULE == FOS_SCALE_4) || (RULE == FOS_SCALE_4OVER6 && E4 < E6);
-  lo = four ? lo4 : lo6;
-  hi = four ? hi4 : hi6;
-  sf = four ? c.sf4 : c.sf6;
-}
-
 template <bool SR>
 __device__ __forceinline__ void sr_words16(uint64_t i0, const QuantParams& p, uint32_t (&w)[16]) {
   if constexpr (SR) {
@@ -598,7 +568,10 @@ __global__ void __launch_bounds__(MODE == kRowsChained ? 320 : 256, MODE == kRow
 template <int RULE, bool RHT, bool SR>
 __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
   __shared__ float s_red[33];
+  __shared__ float2 s_tab[128];
   const TensorConsts tc = quant_prologue(p, s_red);
+  build_scale_table(tc.s_t, s_tab);
+  __syncthreads();
   const uint32_t rht_mask = RHT ? rht_sign_mask(p.hk0, p.hk1) : 0u;
   const int lane = threadIdx.x & 31;
   const int64_t ngroups = (p.cols + 127) >> 7;
@@ -611,6 +584,13 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
     uint2 d[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) d[i] = __ldg(reinterpret_cast<const uint2*>(p.x + (rb * 16 + i) * p.ld + c0));
+    // stochastic rounding: the 4 columns of a source row share one Philox call
+    U4 u4[SR ? 16 : 1];
+    if (SR) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        u4[i] = sr_words4((uint64_t)(rb * 16 + i) * (uint64_t)p.cols + (uint64_t)c0, p.sr_k0, p.sr_k1);
+    }
 #pragma unroll 1
     for (int k = 0; k < 4; ++k) {
       float y[16];
@@ -626,13 +606,16 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
       if (SR) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          U4 u = sr_words4((uint64_t)(rb * 16 + i) * (uint64_t)p.cols + (uint64_t)c0, p.sr_k0, p.sr_k1);
+          const U4& u = u4[SR ? i : 0];
           w[i] = k == 0 ? u.x : (k == 1 ? u.y : (k == 2 ? u.z : u.w));
         }
       }
+      uint64_t yp[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) yp[j] = pack_f2(y[2 * j], y[2 * j + 1]);
       uint32_t lo, hi, sf;
       bool four;
-      quant_block<RULE, SR>(y, ab, tc, w, lo, hi, sf, four);
+      quant_block_tab<RULE, SR>(yp, ab, tc, s_tab, w, lo, hi, sf, four);
       const int64_t orow = c0 + k;
       *reinterpret_cast<uint2*>(p.codes + orow * p.ld_codes + rb * 8) = make_uint2(lo, hi);
       p.sf[sf_off(orow, rb, nb, p.sf_layout)] = (uint8_t)sf;
@@ -660,7 +643,10 @@ __device__ __forceinline__ float half_tree_sum(float v) {
 template <int RULE, bool RHT, bool SR, bool TRANS>
 __global__ void __launch_bounds__(256) quant_2d_kernel(QuantParams p) {
   __shared__ float s_red[33];
+  __shared__ float2 s_tab[128];
   const TensorConsts tc = quant_prologue(p, s_red);
+  build_scale_table(tc.s_t, s_tab);
+  __syncthreads();
   const uint32_t rht_mask = RHT ? rht_sign_mask(p.hk0, p.hk1) : 0u;
   const int lane = threadIdx.x & 31, i = lane & 15, half = lane >> 4;
   const int64_t ntc = p.cols >> 4;               // tiles along source columns
@@ -706,23 +692,43 @@ __global__ void __launch_bounds__(256) quant_2d_kernel(QuantParams p) {
     const float ab = half_max(absmax16(y));
     uint32_t w[16];
     sr_words16<SR>((uint64_t)r * (uint64_t)p.cols + (uint64_t)c0, p, w);
-    Cands c = candidates(ab, tc);
+    const uint32_t pair = e4m3x2(__fmul_rn(ab, tc.k6), __fmul_rn(ab, tc.k4));
+    const uint32_t sf6 = pair & 0xFFu, sf4 = pair >> 8;
+    uint64_t yp[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) yp[j] = pack_f2(y[2 * j], y[2 * j + 1]);
     uint32_t lo6 = 0, hi6 = 0, lo4 = 0, hi4 = 0;
     float E6 = 0.0f, E4 = 0.0f;
-    if (RULE != FOS_SCALE_4) {
-      float S = cand16<SR>(y, c.inv6, w, lo6, hi6);
-      if (c.sf6 == 0) S = sumsq16(y);
+#pragma unroll
+    for (int cnd = 0; cnd < 2; ++cnd) {
+      if (cnd == 0 && RULE == FOS_SCALE_4) continue;
+      if (cnd == 1 && RULE == FOS_SCALE_6) continue;
+      const uint32_t sfc = cnd == 0 ? sf6 : sf4;
+      const float2 tb = s_tab[sfc];
+      uint32_t l, h;
+      float S;
+      if (SR) {
+        S = cand_sr16(y, tb.x, w, l, h);
+      } else {
+        const uint64_t inv2 = pack_f2(tb.x, tb.x);
+        uint64_t acc = 0ull;
+        const uint64_t a[4] = {yp[0], yp[1], yp[2], yp[3]}, b[4] = {yp[4], yp[5], yp[6], yp[7]};
+        l = cand_rne8(a, inv2, acc);
+        h = cand_rne8(b, inv2, acc);
+        const F2 e = unpack_f2(acc);
+        S = __fadd_rn(e.x, e.y);
+      }
+      if (sfc == 0) S = sumsq16(y);  // a zero scale flushes the row: its error is sum y^2
       S = half_tree_sum(S);
-      E6 = c.sf6 ? __fmul_rn(S, __fmul_rn(c.eff6, c.eff6)) : S;
-    }
-    if (RULE != FOS_SCALE_6) {
-      float S = cand16<SR>(y, c.inv4, w, lo4, hi4);
-      if (c.sf4 == 0) S = sumsq16(y);
-      S = half_tree_sum(S);
-      E4 = c.sf4 ? __fmul_rn(S, __fmul_rn(c.eff4, c.eff4)) : S;
+      const float E = sfc ? __fmul_rn(S, tb.y) : S;
+      if (cnd == 0) {
+        lo6 = l; hi6 = h; E6 = E;
+      } else {
+        lo4 = l; hi4 = h; E4 = E;
+      }
     }
     const bool four = (RULE == FOS_SCALE_4) || (RULE == FOS_SCALE_4OVER6 && E4 < E6);
-    const uint32_t lo = four ? lo4 : lo6, hi = four ? hi4 : hi6, sf = four ? c.sf4 : c.sf6;
+    const uint32_t lo = four ? lo4 : lo6, hi = four ? hi4 : hi6, sf = four ? sf4 : sf6;
     if (!TRANS) {
       if (valid) {
         *reinterpret_cast<uint2*>(p.codes + r * p.ld_codes + tcol * 8) = make_uint2(lo, hi);
