@@ -405,14 +405,19 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     int sf_s = 0, sf_t = blockIdx.x, sf_kb = 0;
     uint32_t sf_ph = 0;
     bool ok = true;
-    auto stage_scales = [&]() {
+    // stage the next stage in sequence; with only_if_ready, return false at
+    // once (staging nothing) when its scale bytes have not landed yet
+    auto stage_scales = [&](bool only_if_ready) -> bool {
       int go = 1;
-      if (lane == 0) go = mbar_wait(sf_full(sf_s), sf_ph, args.timeout_ns, abort) ? 1 : 0;
+      if (lane == 0)
+        go = only_if_ready ? (mbar_try(sf_full(sf_s), sf_ph) ? 1 : 0)
+                           : (mbar_wait(sf_full(sf_s), sf_ph, args.timeout_ns, abort) ? 1 : 0);
       go = __shfl_sync(0xFFFFFFFFu, go, 0);
       if (!go) {
+        if (only_if_ready) return false;
         if (lane == 0) raise_timeout(args, abort);
         ok = false;
-        return;
+        return false;
       }
       const uint32_t st = smem_u32(smem + sf_s * C::kStageBytes);
       const uint32_t sfa_s = st + C::kABytes + C::kBBytes + 16u * lane, sfb_s = sfa_s + C::kSfaBytes;
@@ -442,10 +447,11 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         sf_s = 0;
         sf_ph ^= 1u;
       }
+      return true;
     };
     for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
       const int mb = t % args.tiles_m, nb = t / args.tiles_m;
-      while (ok && sf_t == t) stage_scales();  // the rest of this tile's stages
+      while (ok && sf_t == t) stage_scales(false);  // the rest of this tile's stages
       if (!ok) break;
       // one lane waits and the warp follows its verdict, so the warp stays
       // converged for the .sync.aligned tensor-memory loads
@@ -474,14 +480,21 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       // MMA their scales before spending time on the stores.  Only that tile:
       // its stages depend on nothing but this tile's finished MMAs, while a
       // later tile's would wait on an accumulator this warp has yet to free.
-      for (int i = 0; i < C::kStages && ok && sf_t < n_tiles && sf_t == t + (int)gridDim.x; ++i) stage_scales();
+      for (int i = 0; i < C::kStages && ok && sf_t < n_tiles && sf_t == t + (int)gridDim.x; ++i)
+        stage_scales(false);
+      // between store groups, stage any further stage of the next tile whose
+      // scale bytes have landed, so the MMA is not kept waiting by the stores
+      auto stage_ready_ones = [&]() {
+        while (ok && sf_t < n_tiles && sf_t == t + (int)gridDim.x && stage_scales(true)) {
+        }
+      };
 
       const int row = mb * kBM + 32 * q + lane;
       const int col0 = nb * BN + 128 * h;
-      if (row < args.m) {
-        uint16_t* dst = args.c + (int64_t)row * args.ldc + col0;
+      uint16_t* dst = args.c + (int64_t)row * args.ldc + col0;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 4; ++j) {
+        if (row < args.m) {
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             const int col = col0 + 32 * j + 8 * g;
@@ -501,6 +514,8 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
             }
           }
         }
+        __syncwarp();
+        stage_ready_ones();  // warp-uniform: outside the per-lane row test
       }
     }
   }
