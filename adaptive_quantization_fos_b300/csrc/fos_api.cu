@@ -216,6 +216,17 @@ fos_status fos_quantize_batch(const fos_quant_job* jobs, int32_t n_jobs, const f
   auto slot = [&](int32_t i) {
     return reinterpret_cast<float*>(static_cast<char*>(workspace) + (size_t)i * fos::kBarrierOffset);
   };
+  // The scale pads first (bytes no quantize launch writes), so that the
+  // quantize launches follow one another directly: each may then start while
+  // its predecessor finishes (programmatic dependent launch).
+  for (int32_t i = 0; i < n_jobs; ++i) {
+    const fos_quant_job& j = jobs[i];
+    const int64_t nb = j.cols / 16;
+    if (opt->sf_layout == FOS_SF_SWIZZLED_128x4 && (j.rows % 128 != 0 || nb % 4 != 0)) {
+      if (fos::launch_sf_pad(j.sf, sf_bytes_of(j.rows, nb, opt->sf_layout), j.rows, nb, stream) != cudaSuccess)
+        return FOS_ERR_CUDA;
+    }
+  }
   // job 0's block maxima: the amax pass on its own
   int n_part;
   {
@@ -270,11 +281,7 @@ fos_status fos_quantize_batch(const fos_quant_job* jobs, int32_t n_jobs, const f
       n_part = g;
     } else {
       const int64_t tasks = j.rows * ((nb + 127) / 128);
-      if (fos::launch_quant(p, opt->scale_rule, 0, rht, sr, fos::quant_grid(tasks, 0), stream) != cudaSuccess)
-        return FOS_ERR_CUDA;
-    }
-    if (opt->sf_layout == FOS_SF_SWIZZLED_128x4 && (j.rows % 128 != 0 || nb % 4 != 0)) {
-      if (fos::launch_sf_pad(j.sf, sf_bytes_of(j.rows, nb, opt->sf_layout), j.rows, nb, stream) != cudaSuccess)
+      if (fos::launch_quant(p, opt->scale_rule, 0, rht, sr, fos::quant_grid(tasks, 0), stream, true) != cudaSuccess)
         return FOS_ERR_CUDA;
     }
   }

@@ -68,7 +68,10 @@ int amax_grid(int64_t n_warp_tasks);
 int quant_grid(int64_t n_warp_tasks, int kind);
 cudaError_t launch_amax(const AmaxParams& p, bool hadamard, bool transpose, int grid, cudaStream_t s);
 // kind: 0 rows (1D), 1 cols (1D transposed), 2 2D, 3 2D transposed
-cudaError_t launch_quant(const QuantParams& p, int rule, int kind, bool rht, bool sr, int grid, cudaStream_t s);
+// pdl (row kernel only): the launch may overlap the stream's previous kernel,
+// which must be a row-kernel or amax launch whose outputs it waits for.
+cudaError_t launch_quant(const QuantParams& p, int rule, int kind, bool rht, bool sr, int grid, cudaStream_t s,
+                         bool pdl = false);
 // Rows (1D) quantized from partials of an earlier launch while 2 extra warps
 // per CTA take the block maxima of the next job (p.next_*); grid = chained_grid().
 cudaError_t launch_quant_rows_chained(const QuantParams& p, int rule, bool rht, bool sr, int grid, cudaStream_t s);

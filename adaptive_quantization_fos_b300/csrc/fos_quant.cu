@@ -47,6 +47,36 @@ __device__ __forceinline__ float block_max(float v, float* s_red) {
   return r;
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel of
+// the stream (launched with programmatic stream serialization) be scheduled
+// once every CTA of this grid has executed it or exited; wait blocks until
+// the grids this one depends on have completed and their writes are visible.
+// Both are no-ops for a grid launched without that attribute.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Named barrier 1 over the CTA's first n threads.
+__device__ __forceinline__ void bar_sync_first(int n) { asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory"); }
+
+// block_max over the first NW warps of the CTA only (named barrier 1), for
+// kernels whose other warps have gone their own way.
+template <int NW>
+__device__ __forceinline__ float group_max(float v, float* s_red) {
+  v = warp_max(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) s_red[warp] = v;
+  bar_sync_first(32 * NW);
+  if (warp == 0) {
+    float u = lane < NW ? s_red[lane] : 0.0f;
+    u = warp_max(u);
+    if (lane == 0) s_red[32] = u;
+  }
+  bar_sync_first(32 * NW);
+  const float r = s_red[32];
+  bar_sync_first(32 * NW);
+  return r;
+}
+
 __device__ __forceinline__ void load_block16(const uint16_t* p, bool aligned32, uint32_t (&w)[8]) {
   if (aligned32)
     ldg256(p, w);
@@ -87,6 +117,7 @@ __device__ __forceinline__ float absmax16(const float (&y)[16]) {
 template <bool RHT>
 __global__ void __launch_bounds__(256) amax_rows_kernel(AmaxParams p) {
   __shared__ float s_red[33];
+  pdl_launch_dependents();  // the next launch may start its own reads meanwhile
   const int lane = threadIdx.x & 31;
   const uint32_t rht_mask = RHT ? rht_sign_mask(p.hk0, p.hk1) : 0u;
   const int64_t nb = p.cols >> 4;
@@ -191,6 +222,24 @@ constexpr int kRowSmemBytes = kRowWarps * kRowSlots * kRowSlotBytes;
 constexpr int kAmaxWarps = 2;
 constexpr int kAmaxSlots = 4;
 constexpr int kChainSmemBytes = kRowSmemBytes + kAmaxWarps * kAmaxSlots * kRowSlotBytes;
+
+// The row kernel's prologue, run by its kRowWarps quantize warps alone: the
+// tensor amax from the supplied value or from the partial maxima a previous
+// launch wrote (read through L2: that launch may have been running when this
+// one started), then the tensor constants.
+__device__ __forceinline__ TensorConsts quant_prologue_rows(const QuantParams& p, float* s_red) {
+  float amax;
+  if (p.n_partials == 0) {
+    amax = __ldcg(p.amax_src);
+  } else {
+    float m = 0.0f;
+    for (int i = threadIdx.x; i < p.n_partials; i += 32 * kRowWarps) m = fmaxf(m, __ldcg(p.amax_src + i));
+    amax = group_max<kRowWarps>(m, s_red);
+  }
+  TensorConsts tc = tensor_consts(amax);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *p.tensor_scale = tc.s_t;
+  return tc;
+}
 
 template <int RULE, bool SR>
 __device__ __forceinline__ void quant_block_tab(const uint64_t (&yp)[8], float ab, const TensorConsts& tc,
@@ -386,6 +435,10 @@ __global__ void __launch_bounds__(MODE == kRowsChained ? 320 : 256, MODE == kRow
     s_next_done = 0u;
   }
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  if constexpr (!FUSED) {
+    __syncthreads();  // the barriers are initialised before the roles split
+    pdl_launch_dependents();
+  }
   const uint32_t rht_mask = RHT ? rht_sign_mask(p.hk0, p.hk1) : 0u;
   const int64_t nb = p.nb;
   const int64_t wpr = (nb + 127) >> 7;  // warp tasks per row
@@ -441,12 +494,9 @@ __global__ void __launch_bounds__(MODE == kRowsChained ? 320 : 256, MODE == kRow
     for (int i = threadIdx.x; i < (int)gridDim.x; i += blockDim.x) mm = fmaxf(mm, __ldcg(p.ws_partials + i));
     tc = tensor_consts(block_max(mm, s_red));
     if (blockIdx.x == 0 && threadIdx.x == 0) *p.tensor_scale = tc.s_t;
-  } else {
-    tc = quant_prologue(p, s_red);
   }
-  build_scale_table(tc.s_t, s_tab);
-  __syncthreads();
   if (MODE == kRowsChained && warp >= kRowWarps) {
+    // the next job's block maxima need nothing from earlier launches
     next_job_amax<RHT>(p, q_smem + kRowSmemBytes, &s_bar[kRowWarps * kRowSlots], warp - kRowWarps, lane, rht_mask,
                        &s_next_max, &s_next_done);
     return;
@@ -478,6 +528,18 @@ __global__ void __launch_bounds__(MODE == kRowsChained ? 320 : 256, MODE == kRow
   int issued = 0, consumed = 0;
   if (lane == 0)
     for (int k = 0; k < kRowSlots; ++k) issued += issue_next(k) ? 1 : 0;
+  if constexpr (FUSED) {
+    build_scale_table(tc.s_t, s_tab);
+    __syncthreads();
+  } else {
+    // The input is read-only, so its first copies are in flight already; the
+    // partial maxima come from the launch before this one, which may still be
+    // running.  Everything from here on waits for it.
+    pdl_wait();
+    tc = quant_prologue_rows(p, s_red);
+    build_scale_table(tc.s_t, s_tab);
+    bar_sync_first(32 * kRowWarps);
+  }
 
   int slot = 0;
   uint32_t ph = 0;
@@ -859,8 +921,26 @@ cudaError_t launch_amax(const AmaxParams& p, bool hadamard, bool transpose, int 
   return cudaGetLastError();
 }
 
+// Launch fn(p); with pdl, the launch may begin while the stream's previous
+// kernel is still running (programmatic stream serialization): fn must then
+// wait (griddepcontrol.wait) before it reads anything that kernel writes.
+static cudaError_t launch_params(void (*fn)(QuantParams), int grid, int block, int smem, bool pdl,
+                                 const QuantParams& p, cudaStream_t s) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
 template <int RULE, bool RHT, bool SR>
-static void launch_q(const QuantParams& p, int kind, int grid, cudaStream_t s) {
+static void launch_q(const QuantParams& p, int kind, int grid, cudaStream_t s, bool pdl) {
   switch (kind) {
     case 0: {
       static bool attr = false;  // benign race: the attribute is idempotent
@@ -869,7 +949,7 @@ static void launch_q(const QuantParams& p, int kind, int grid, cudaStream_t s) {
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kRowSmemBytes);
         attr = true;
       }
-      quant_rows_kernel<RULE, RHT, SR, kRowsPlain><<<grid, 256, kRowSmemBytes, s>>>(p);
+      launch_params(quant_rows_kernel<RULE, RHT, SR, kRowsPlain>, grid, 256, kRowSmemBytes, pdl, p, s);
       break;
     }
     case 1: quant_cols_kernel<RULE, RHT, SR><<<grid, 256, 0, s>>>(p); break;
@@ -879,13 +959,13 @@ static void launch_q(const QuantParams& p, int kind, int grid, cudaStream_t s) {
 }
 
 template <int RULE>
-static void launch_q_rule(const QuantParams& p, int kind, bool rht, bool sr, int grid, cudaStream_t s) {
+static void launch_q_rule(const QuantParams& p, int kind, bool rht, bool sr, int grid, cudaStream_t s, bool pdl) {
   if (rht) {
-    if (sr) launch_q<RULE, true, true>(p, kind, grid, s);
-    else launch_q<RULE, true, false>(p, kind, grid, s);
+    if (sr) launch_q<RULE, true, true>(p, kind, grid, s, pdl);
+    else launch_q<RULE, true, false>(p, kind, grid, s, pdl);
   } else {
-    if (sr) launch_q<RULE, false, true>(p, kind, grid, s);
-    else launch_q<RULE, false, false>(p, kind, grid, s);
+    if (sr) launch_q<RULE, false, true>(p, kind, grid, s, pdl);
+    else launch_q<RULE, false, false>(p, kind, grid, s, pdl);
   }
 }
 
@@ -939,8 +1019,8 @@ static cudaError_t launch_rows_chained(const QuantParams& p, int grid, cudaStrea
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  fn<<<grid, 32 * (kRowWarps + kAmaxWarps), kChainSmemBytes, s>>>(p);
-  return cudaGetLastError();
+  // always the successor of a launch of the same batch: overlap its tail
+  return launch_params(fn, grid, 32 * (kRowWarps + kAmaxWarps), kChainSmemBytes, true, p, s);
 }
 
 int chained_grid() {
@@ -969,11 +1049,12 @@ cudaError_t launch_quant_rows_fused(const QuantParams& p, int rule, bool rht, bo
   }
 }
 
-cudaError_t launch_quant(const QuantParams& p, int rule, int kind, bool rht, bool sr, int grid, cudaStream_t s) {
+cudaError_t launch_quant(const QuantParams& p, int rule, int kind, bool rht, bool sr, int grid, cudaStream_t s,
+                         bool pdl) {
   switch (rule) {
-    case FOS_SCALE_6: launch_q_rule<FOS_SCALE_6>(p, kind, rht, sr, grid, s); break;
-    case FOS_SCALE_4: launch_q_rule<FOS_SCALE_4>(p, kind, rht, sr, grid, s); break;
-    default: launch_q_rule<FOS_SCALE_4OVER6>(p, kind, rht, sr, grid, s); break;
+    case FOS_SCALE_6: launch_q_rule<FOS_SCALE_6>(p, kind, rht, sr, grid, s, pdl); break;
+    case FOS_SCALE_4: launch_q_rule<FOS_SCALE_4>(p, kind, rht, sr, grid, s, pdl); break;
+    default: launch_q_rule<FOS_SCALE_4OVER6>(p, kind, rht, sr, grid, s, pdl); break;
   }
   return cudaGetLastError();
 }

@@ -189,7 +189,11 @@ fos_status fos_quantize_batch_workspace_size(int32_t n_jobs, size_t* bytes);
  * the job before it: launch 0 takes job 0's block maxima, launch i+1
  * quantizes job i while 2 extra warps per CTA take job i+1's block maxima,
  * and the last launch quantizes the last job.  Order the jobs by size,
- * smallest first, to overlap the most.
+ * smallest first, to overlap the most.  The quantize launches use
+ * programmatic dependent launch: each may start (its input copies and the
+ * next job's maxima) while its predecessor finishes, and waits for it before
+ * reading the maxima it left.  Scale-pad clears, when a shape needs them,
+ * are enqueued before all of these.
  *   opt       shared options; transpose, block_2d and tensor_amax are not
  *             supported here (FOS_ERR_UNSUPPORTED; use fos_quantize).
  *   workspace device scratch of fos_quantize_batch_workspace_size() bytes,
