@@ -75,6 +75,19 @@ class fos_nvfp4_tensor(ctypes.Structure):
     ]
 
 
+class fos_backward_options(ctypes.Structure):
+    _fields_ = [
+        ("struct_size", ctypes.c_uint32),
+        ("scale_rule", ctypes.c_int32),
+        ("grad_rounding", ctypes.c_int32),
+        ("wgrad_hadamard", ctypes.c_int32),
+        ("weight_2d", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("sr_seed", ctypes.c_uint64),
+        ("hadamard_seed", ctypes.c_uint64),
+    ]
+
+
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(
@@ -101,6 +114,10 @@ def _load() -> ctypes.CDLL:
         "fos_quantize_batch_workspace_size": (i32, [i32, ctypes.POINTER(sz)]),
         "fos_quantize_batch": (i32, [ctypes.POINTER(fos_quant_job), i32, ctypes.POINTER(fos_quant_options), vp, sz,
                                      vp]),
+        "fos_linear_backward_workspace_size": (i32, [i64, i64, i64, ctypes.POINTER(sz)]),
+        "fos_linear_backward_operands": (i32, [i64, i64, i64, vp, sz, ctypes.POINTER(fos_nvfp4_tensor)]),
+        "fos_linear_backward": (i32, [vp, i64, vp, i64, vp, i64, i64, i64, i64, ctypes.POINTER(fos_backward_options),
+                                      vp, i64, vp, i64, vp, sz, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -113,7 +130,8 @@ _lib = _load()
 EXPORTED = ("fos_abi_version", "fos_status_string", "fos_sf_bytes", "fos_quantize_workspace_size",
             "fos_tensor_amax", "fos_quantize", "fos_quantize_noalloc", "fos_dequantize", "fos_gemm", "fos_e2m1_encode",
             "fos_e4m3_encode", "fos_philox4x32_10", "fos_selftest_wait_limits", "fos_quantize_batch",
-            "fos_quantize_batch_workspace_size")
+            "fos_quantize_batch_workspace_size", "fos_linear_backward", "fos_linear_backward_workspace_size",
+            "fos_linear_backward_operands")
 
 
 def _check(status: int, what: str) -> None:
@@ -357,3 +375,93 @@ def gemm(A: NVFP4Tensor, B: NVFP4Tensor, out=None, status=None, stream=None):
     _check(fos_gemm(A.as_c(), B.as_c(), out.data_ptr(), out.stride(0),
                     status.data_ptr() if status is not None else 0, _stream_ptr(stream)), "fos_gemm")
     return out
+
+
+# ------------------------------------------------------- linear backward
+
+
+def fos_linear_backward_workspace_size(M: int, N: int, K: int) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.fos_linear_backward_workspace_size(M, N, K, ctypes.byref(n)), "fos_linear_backward_workspace_size")
+    return n.value
+
+
+def fos_linear_backward_operands(M: int, N: int, K: int, workspace, workspace_bytes: int):
+    """Raw call: the four fos_nvfp4_tensor descriptors inside a workspace."""
+    ops = (fos_nvfp4_tensor * 4)()
+    _check(_lib.fos_linear_backward_operands(M, N, K, workspace, workspace_bytes, ops),
+           "fos_linear_backward_operands")
+    return list(ops)
+
+
+def fos_linear_backward(dy, ld_dy, x, ld_x, w, ld_w, M, N, K, opt: fos_backward_options, dx, ld_dx, dw, ld_dw,
+                        workspace, workspace_bytes, dev_status, stream) -> int:
+    return int(_lib.fos_linear_backward(dy, ld_dy, x or None, ld_x, w or None, ld_w, M, N, K, ctypes.byref(opt),
+                                        dx or None, ld_dx, dw or None, ld_dw, workspace, workspace_bytes,
+                                        dev_status or None, stream))
+
+
+def backward_options(*, scale_rule=FOS_SCALE_4OVER6, grad_rounding=FOS_ROUND_STOCHASTIC, wgrad_hadamard=True,
+                     weight_2d=False, sr_seed=0, hadamard_seed=0) -> fos_backward_options:
+    """Defaults follow the FP4 training recipe: stochastic rounding of dY and
+    the RHT on the weight-gradient operands."""
+    o = fos_backward_options()
+    o.struct_size = ctypes.sizeof(fos_backward_options)
+    o.scale_rule = scale_rule
+    o.grad_rounding = grad_rounding
+    o.wgrad_hadamard = int(bool(wgrad_hadamard))
+    o.weight_2d = int(bool(weight_2d))
+    o.reserved = 0
+    o.sr_seed = sr_seed
+    o.hadamard_seed = hadamard_seed
+    return o
+
+
+class LinearBackward:
+    """dX = dY W and dW = dY^T X for Y = X W^T, through fos_linear_backward,
+    with a reusable workspace for one M x N x K shape."""
+
+    def __init__(self, M: int, N: int, K: int, *, device="cuda", **opts):
+        torch = _torch()
+        self.M, self.N, self.K = M, N, K
+        self.opt = backward_options(**opts)
+        self.ws_bytes = fos_linear_backward_workspace_size(M, N, K)
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+
+    def __call__(self, dy, x, w, *, dx=None, dw=None, need_dx=True, need_dw=True, status=None, stream=None):
+        torch = _torch()
+        M, N, K = self.M, self.N, self.K
+        for t, shape in ((dy, (M, N)), (x, (M, K)), (w, (N, K))):
+            assert t is None or (t.dtype == torch.bfloat16 and tuple(t.shape) == shape and t.stride(1) == 1)
+        dev = dy.device
+        if need_dx and dx is None:
+            dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+        if need_dw and dw is None:
+            dw = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+        dx = dx if need_dx else None
+        dw = dw if need_dw else None
+        st = fos_linear_backward(dy.data_ptr(), dy.stride(0), x.data_ptr() if x is not None else 0,
+                                 x.stride(0) if x is not None else 0, w.data_ptr() if w is not None else 0,
+                                 w.stride(0) if w is not None else 0, M, N, K, self.opt,
+                                 dx.data_ptr() if dx is not None else 0, dx.stride(0) if dx is not None else 0,
+                                 dw.data_ptr() if dw is not None else 0, dw.stride(0) if dw is not None else 0,
+                                 self.workspace.data_ptr(), self.ws_bytes,
+                                 status.data_ptr() if status is not None else 0, _stream_ptr(stream))
+        _check(st, "fos_linear_backward")
+        return dx, dw
+
+    def operands(self):
+        """[dY, W^T, dY^T, X^T] as NVFP4Tensor views into the workspace."""
+        torch = _torch()
+        base = self.workspace.data_ptr()
+        out = []
+        for d in fos_linear_backward_operands(self.M, self.N, self.K, base, self.ws_bytes):
+            c0 = d.codes - base
+            s0 = d.sf - base
+            t0 = d.tensor_scale - base
+            sfb = fos_sf_bytes(d.rows, d.cols, d.sf_layout)
+            out.append(NVFP4Tensor(
+                codes=self.workspace[c0:c0 + d.rows * d.ld_codes].view(d.rows, d.ld_codes),
+                sf=self.workspace[s0:s0 + sfb], tensor_scale=self.workspace[t0:t0 + 4].view(torch.float32),
+                rows=d.rows, cols=d.cols, sf_layout=d.sf_layout))
+        return out

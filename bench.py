@@ -475,7 +475,43 @@ def secondary(torch, fos, dev, pk) -> dict:
     measure("gradient_rne_2d", grad, block_2d=True)
     del grad
     res["linear_forward"] = linear_forward(torch, fos, dev, pk)
+    res["linear_backward"] = linear_backward(torch, fos, dev, pk)
     return res
+
+
+def linear_backward(torch, fos, dev, pk) -> dict:
+    """dX = dY W and dW = dY^T X for the linear forward's layer (X 8192 x 4096
+    activations, W 12288 x 4096 weights) with dY 8192 x 12288 from the
+    gradient recipe, through fos_linear_backward with the training recipe
+    (SR on dY, RHT along M on the weight-gradient operands): four
+    quantizations and two NVFP4 GEMMs per call."""
+    M, N, K = 8192, 12288, 4096
+    dy = _to_dev(torch, workloads.gradients(M, N, seed=6001), dev)
+    x = _to_dev(torch, workloads.activations(M, K, seed=6002), dev)
+    w = _to_dev(torch, workloads.student_t(N, K, seed=6003), dev)
+    bw = fos.LinearBackward(M, N, K, device=dev, sr_seed=11, hadamard_seed=12)
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    dw = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+    try:
+        bw(dy, x, w, dx=dx, dw=dw)
+    except fos.FosError as e:
+        return {"status": f"backward unavailable: {e}"}
+    # the operands' quantization alone, to split the time
+    qs = [fos.Quantizer(M, N, device=dev, rounding=fos.FOS_ROUND_STOCHASTIC, sr_seed=11),
+          fos.Quantizer(N, K, device=dev, transpose=True),
+          fos.Quantizer(M, N, device=dev, rounding=fos.FOS_ROUND_STOCHASTIC, sr_seed=11, transpose=True,
+                        hadamard=True, hadamard_seed=12),
+          fos.Quantizer(M, K, device=dev, transpose=True, hadamard=True, hadamard_seed=12)]
+    srcs = [dy, w, dy, x]
+    with ClockSampler(dev.index) as clk:
+        t = _time_calls(torch, lambda: bw(dy, x, w, dx=dx, dw=dw), 20)
+        tq = _time_calls(torch, lambda: [q(s) for q, s in zip(qs, srcs)], 20)
+    flops = 2 * 2.0 * M * N * K
+    return {"ms": round(t, 4), "quantize_ms": round(tq, 4), "gemm_ms": round(t - tq, 4),
+            "tflops_effective": round(flops / (t * 1e-3) / 1e12, 1),
+            "gemm_tflops": round(flops / ((t - tq) * 1e-3) / 1e12, 1), "clocks": clk.summary(),
+            "shape": {"M": M, "N": N, "K": K},
+            "options": "SR on dY (both copies), RHT along M on dY^T and X^T, W^T 1D"}
 
 
 def linear_forward(torch, fos, dev, pk) -> dict:

@@ -237,14 +237,77 @@ fos_status fos_dequantize(const fos_nvfp4_tensor* q, void* out, int32_t out_dtyp
  * quantized along K.  Products and FP32 accumulation run on the tcgen05
  * tensor cores (block-scaled MMA, 16-value E4M3 scales); the result is
  * scaled once in FP32 and rounded to bf16.
- *   A, B      K % 256 == 0 (same K), FOS_SF_SWIZZLED_128x4 scales, codes 16-byte
- *             aligned with ld_codes % 16 == 0; M % 128 == 0, N % 256 == 0.
- *   C         device bf16 [M][ldc], ldc % 8 == 0, 16-byte aligned.
+ *   A, B      the same K, K % 64 == 0 (one MMA step); FOS_SF_SWIZZLED_128x4
+ *             scales, 16-byte aligned; codes 16-byte aligned with
+ *             ld_codes % 16 == 0.  M (= A->rows) is any size >= 0 (ragged
+ *             tiles are clipped on store); N (= B->rows) % 8 == 0.
+ *   C         device bf16 [M][ldc], ldc >= N, ldc % 8 == 0, 16-byte aligned.
  *   dev_status optional device int32: a kernel whose bounded pipeline wait
  *             runs out writes FOS_ERR_TIMEOUT there and leaves C incomplete.
  */
 fos_status fos_gemm(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* C, int64_t ldc,
                     int32_t* dev_status, cudaStream_t stream);
+
+/* ---- quantized linear backward ---- */
+
+/*
+ * Options of fos_linear_backward.  The "Four Over Six" page ("Training")
+ * states that its quantized linear layer has a backward pass; the FP4
+ * glossary page ("FP4 ile Çıkarım ve Eğitim") describes the training recipe
+ * this follows: random Hadamard transforms against outliers and stochastic
+ * rounding for gradients.
+ */
+typedef struct fos_backward_options {
+  uint32_t struct_size;   /* sizeof(fos_backward_options) */
+  int32_t scale_rule;     /* fos_scale_rule of all four operands */
+  int32_t grad_rounding;  /* fos_rounding of both copies of dY (stochastic in the training recipe) */
+  int32_t wgrad_hadamard; /* 1: RHT along M on dY^T and X^T, one sign vector (their product is unchanged) */
+  int32_t weight_2d;      /* 1: W^T with 16x16 tiles (the exact transpose of a 2D forward W) */
+  int32_t reserved;       /* must be 0 */
+  uint64_t sr_seed;       /* stochastic rounding key; both copies of dY use it (source index) */
+  uint64_t hadamard_seed; /* RHT sign-vector key */
+} fos_backward_options;
+
+/* Device scratch of fos_linear_backward for M x N x K (see its layout). */
+fos_status fos_linear_backward_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
+
+/*
+ * fos_linear_backward_operands -- the four quantized operands as they lie in
+ * a fos_linear_backward workspace (valid after a call on that workspace):
+ *   ops[0] dY   [M, N] blocks along N   (dgrad A)
+ *   ops[1] W^T  [K, N] blocks along N   (dgrad B)
+ *   ops[2] dY^T [N, M] blocks along M   (wgrad A)
+ *   ops[3] X^T  [K, M] blocks along M   (wgrad B)
+ * Codes rows are padded to 16-byte strides; scales are FOS_SF_SWIZZLED_128x4.
+ * The workspace holds, each section 256-byte aligned and in this order, the
+ * codes then the scales of ops[0..3], the four tensor scales, and the
+ * quantizer's scratch.
+ */
+fos_status fos_linear_backward_operands(int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+                                        fos_nvfp4_tensor ops[4]);
+
+/*
+ * fos_linear_backward -- the NVFP4 backward of Y = X W^T (X [M,K], W [N,K],
+ * dY [M,N], all bf16 row-major):
+ *   dX = dY . W       [M, K]: dY quantized along N, W quantized along N
+ *                     (transposed input), one fos_gemm;
+ *   dW = dY^T . X     [N, K]: dY and X quantized along M (transposed input,
+ *                     optional RHT), one fos_gemm.
+ * Each quantization is exactly fos_quantize's; each product is fos_gemm's.
+ *   M % 64 == 0, N % 64 == 0 (the contraction lengths), K % 16 == 0; all > 0.
+ *   dy, x, w  device bf16, 16-byte aligned, ld % 8 == 0, ld >= the row length.
+ *   dx, dw    device bf16 outputs [M][ld_dx], [N][ld_dw] (ld >= K, ld % 8 == 0,
+ *             16-byte aligned); either may be NULL to skip that half (its
+ *             operands are then not produced).
+ *   dev_status optional device int32 for the GEMMs' FOS_ERR_TIMEOUT.  A
+ *             quantizer that gives up leaves a NaN tensor scale, which makes
+ *             the product that uses it NaN.
+ * Everything is enqueued on `stream` in the order dgrad, wgrad.
+ */
+fos_status fos_linear_backward(const void* dy, int64_t ld_dy, const void* x, int64_t ld_x, const void* w,
+                               int64_t ld_w, int64_t M, int64_t N, int64_t K, const fos_backward_options* opt,
+                               void* dx, int64_t ld_dx, void* dw, int64_t ld_dw, void* workspace,
+                               size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream);
 
 /*
  * fos_selftest_wait_limits -- runs the library's bounded device waits into

@@ -319,3 +319,36 @@ def mae_nearest_grid(x, block: int) -> float:
     a = np.ascontiguousarray(x, dtype=np.float32)
     assert a.size % block == 0
     return float(lib().orc_mae_nearest_grid(_p(a), a.size, block))
+
+
+def linear_backward_operands(dy, x, w, *, scale_rule: int = SCALE_4OVER6, grad_rounding: int = ROUND_SR,
+                             wgrad_hadamard: bool = True, weight_2d: bool = False, sr_seed: int = 0,
+                             hadamard_seed: int = 0) -> list[QResult]:
+    """The four quantized operands of the quantized linear layer's backward for
+    Y = X W^T (dy [M, N], x [M, K], w [N, K] as bf16 bit patterns).
+
+    "Four Over Six" ("Training") gives its quantized linear layer a backward
+    pass; the FP4 glossary page ("FP4 ile Çıkarım ve Eğitim") names the recipe:
+    random Hadamard transforms against outliers, stochastic rounding for
+    gradients.  Each product contracts over one dimension, and both of its
+    operands are blocked along that dimension:
+      dX = dY W     over N: [dY along N, W^T along N]
+      dW = dY^T X   over M: [dY^T along M, X^T along M] (RHT along M on both)
+    Returns [dY, W^T, dY^T, X^T]."""
+    return [
+        quantize(dy, scale_rule=scale_rule, rounding=grad_rounding, sr_seed=sr_seed),
+        quantize(w, scale_rule=scale_rule, transpose=True, block_2d=weight_2d),
+        quantize(dy, scale_rule=scale_rule, rounding=grad_rounding, transpose=True, hadamard=wgrad_hadamard,
+                 sr_seed=sr_seed, hadamard_seed=hadamard_seed),
+        quantize(x, scale_rule=scale_rule, transpose=True, hadamard=wgrad_hadamard, hadamard_seed=hadamard_seed),
+    ]
+
+
+def linear_backward_rows(ops: list[QResult], dx_rows, dw_rows, matmul: bool = False):
+    """FP64 references (and the sum |a||b| bounds) of the sampled rows of
+    dX = dY_hat W^T_hat^T and dW = dY^T_hat X^T_hat^T from the dequantized
+    operands of ``linear_backward_operands``."""
+    f = gemm_rows_matmul if matmul else gemm_rows
+    dx = f(dequantize(ops[0]), dequantize(ops[1]), dx_rows)
+    dw = f(dequantize(ops[2]), dequantize(ops[3]), dw_rows)
+    return dx, dw

@@ -120,6 +120,48 @@ def test_gemm_validation(fos):
     assert fos.fos_gemm(A, B, fake, 256, 0, 0) == fos.FOS_OK  # empty: nothing to launch
 
 
+def test_linear_backward_validation(fos):
+    """Every argument check of fos_linear_backward fails before anything is
+    enqueued (fake device addresses; nothing here reaches a launch)."""
+    INVALID = fos.FOS_ERR_INVALID_ARG
+    fake = 1 << 20
+    M, N, K = 128, 192, 80
+    ws = fos.fos_linear_backward_workspace_size(M, N, K)
+    assert ws > 0
+    opt = fos.backward_options()
+
+    def call(M=M, N=N, K=K, dy=fake, ld_dy=N, x=fake, ld_x=K, w=fake, ld_w=K, o=opt, dx=fake, ld_dx=K, dw=fake,
+             ld_dw=K, wsp=fake, wsb=ws, status=0):
+        return fos.fos_linear_backward(dy, ld_dy, x, ld_x, w, ld_w, M, N, K, o, dx, ld_dx, dw, ld_dw, wsp, wsb,
+                                       status, 0)
+
+    assert call(M=96) == INVALID  # M % 64 (the weight-gradient contraction)
+    assert call(N=160) == INVALID  # N % 64 (the data-gradient contraction)
+    assert call(K=72) == INVALID  # K % 16
+    assert call(M=0) == INVALID
+    assert call(dy=0) == INVALID
+    assert call(ld_dy=N - 8) == INVALID
+    assert call(ld_x=K + 4) == INVALID  # ld % 8
+    assert call(w=fake + 8) == INVALID  # 16-byte alignment
+    assert call(dx=fake + 2) == INVALID
+    assert call(ld_dw=K - 16) == INVALID
+    assert call(wsb=ws - 1) == INVALID
+    assert call(wsp=fake + 128) == INVALID  # workspace 256-byte aligned
+    assert call(status=fake + 2) == INVALID
+    assert call(x=0) == INVALID  # the weight gradient needs X
+    assert call(w=0) == INVALID  # the data gradient needs W
+    for field, value in (("scale_rule", 5), ("grad_rounding", 2), ("wgrad_hadamard", 2), ("weight_2d", 3),
+                         ("reserved", 1), ("struct_size", 8)):
+        bad = fos.backward_options()
+        setattr(bad, field, value)
+        assert call(o=bad) == INVALID, field
+    ops = fos.fos_linear_backward_operands(M, N, K, fake, ws)
+    assert [(o.rows, o.cols) for o in ops] == [(M, N), (K, N), (N, M), (K, M)]
+    assert all(o.ld_codes % 16 == 0 and o.codes % 256 == 0 and o.sf % 256 == 0 for o in ops)
+    with pytest.raises(fos.FosError):
+        fos.fos_linear_backward_workspace_size(100, N, K)
+
+
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     import importlib.util
 

@@ -406,3 +406,55 @@ def test_outlier_matrix_four_over_six_lowers_error(orc):
     d6 = orc.dequantize(orc.quantize(x, scale_rule=orc.SCALE_6)).astype(np.float64)
     assert np.abs(d46 - y).mean() < np.abs(d6 - y).mean()
     assert ((d46 - y) ** 2).sum() < ((d6 - y) ** 2).sum()
+
+
+# ------------------------------------------------- quantized linear backward
+
+
+def _grid_matrix(rng, rows, cols, sign_of_six=1.0):
+    """Values on the E2M1 grid, with a 6 wherever (i + j) % 16 == 0, so every
+    16-run along a row or a column (and every 16 x 16 tile) has amax 6."""
+    g = np.array([0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    v = rng.choice(g, (rows, cols)) * rng.choice([-1.0, 1.0], (rows, cols))
+    i, j = np.indices((rows, cols))
+    v[(i + j) % 16 == 0] = 6.0 * sign_of_six
+    return v
+
+
+@pytest.mark.parametrize("weight_2d", [False, True])
+def test_linear_backward_on_grid_inputs_recovers_exact_products(orc, weight_2d):
+    """Inputs already on the NVFP4 grid (block amax 6 in every orientation)
+    quantize losslessly up to the FP32 rounding of eff = 448 * (6/2688), so
+    the backward's operands must dequantize to dY, W^T, dY^T, X^T and its
+    products to dY W and dY^T X.  A transposed or swapped operand fails."""
+    rng = np.random.default_rng(31)
+    M, N, K = 64, 128, 48
+    dy, x, w = _grid_matrix(rng, M, N), _grid_matrix(rng, M, K, -1.0), _grid_matrix(rng, N, K)
+    ops = orc.linear_backward_operands(workloads.bf16_bits(dy), workloads.bf16_bits(x), workloads.bf16_bits(w),
+                                       grad_rounding=orc.ROUND_RNE, wgrad_hadamard=False, weight_2d=weight_2d)
+    for q, ref in zip(ops, (dy, w.T, dy.T, x.T)):
+        assert (q.rows, q.cols) == ref.shape
+        assert np.allclose(orc.dequantize(q), ref, rtol=1e-6, atol=0)
+    (dx, dxb), (dw, dwb) = orc.linear_backward_rows(ops, np.arange(M), np.arange(N))
+    assert np.all(np.abs(dx - dy @ w) <= 1e-6 * dxb)
+    assert np.all(np.abs(dw - dy.T @ x) <= 1e-6 * dwb)
+
+
+def test_linear_backward_recipe_preserves_weight_gradient(orc):
+    """With SR on dY and the RHT along M on both weight-gradient operands, the
+    transform cancels in dY^T X: the reference stays within NVFP4 error of the
+    exact product, while an RHT on one operand only would leave it unrelated."""
+    rng = np.random.default_rng(32)
+    M, N, K = 256, 64, 32
+    dy = rng.laplace(0, 1e-3, (M, N))
+    x = rng.standard_normal((M, K))
+    dyb, xb, wb = workloads.bf16_bits(dy), workloads.bf16_bits(x), workloads.bf16_bits(rng.standard_normal((N, K)))
+    dy, x = workloads.bf16_to_f32(dyb).astype(np.float64), workloads.bf16_to_f32(xb).astype(np.float64)
+    exact = dy.T @ x
+    ops = orc.linear_backward_operands(dyb, xb, wb, sr_seed=5, hadamard_seed=9)
+    _, (dw, _) = orc.linear_backward_rows(ops, np.arange(0), np.arange(N))
+    rel = np.linalg.norm(dw - exact) / np.linalg.norm(exact)
+    assert rel < 0.3
+    one_sided = orc.quantize(xb, transpose=True)  # X^T without the transform
+    bad, _ = orc.gemm_rows(orc.dequantize(ops[2]), orc.dequantize(one_sided), np.arange(N))
+    assert np.linalg.norm(bad - exact) / np.linalg.norm(exact) > 0.8
