@@ -402,16 +402,40 @@ __device__ __forceinline__ float sumsq16(const float (&r)[16]) {
   return __fadd_rn(acc.x, acc.y);
 }
 
-// Stochastic rounding of one value to an E2M1 grid magnitude: lo <= a < hi,
-// up iff u < (a - lo) / (hi - lo) with u = (w >> 8) * 2^-24 (all exact).
-__device__ __forceinline__ float sr_mag(float a, uint32_t w) {
-  float step = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
-  float inv_step = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
-  float lo = a < 4.0f ? __fmul_rn(floorf(__fmul_rn(a, inv_step)), step) : 4.0f;
-  float p = __fmul_rn(__fsub_rn(a, lo), inv_step);
-  float u = __fmul_rn((float)(w >> 8), 5.9604644775390625e-8f);  // 2^-24
-  float g = (u < p) ? __fadd_rn(lo, step) : lo;
-  return a >= 6.0f ? 6.0f : g;
+// Stochastic rounding to E2M1 grid magnitudes, two values at a time.
+//
+// For a in [0, 6] let step be the grid spacing of a's interval (0.5 below 2,
+// 1 in [2, 4), 2 in [4, 6]) and t = a / step (exact: step is a power of 2),
+// so the interval's ends are lo = floor(t) * step and hi = lo + step.  The
+// rule "up iff u < p" with p = t - floor(t) and u = n * 2^-24 (n = w >> 8)
+// picks ceil(t - u) * step: t - u lies in (floor(t), floor(t) + 1) when
+// u < p, and in (floor(t) - 1, floor(t)] otherwise.  t - u is evaluated as
+// one FMA rounded toward +inf, fma.rp(-n, 2^-24, t), and ceil(.) as the
+// round-up addition of M = 1.5 * 2^23, then M subtracted: t - u lies in
+// (-1, 3], so M + (t - u) stays inside [2^23, 2^24), where the spacing of
+// floats is exactly 1.  Both roundings are exact for ceil's purpose:
+// rounding up never passes an integer, and the integers involved are floats.
+// a >= 6 is clamped to 6 first (t = 3 gives 6 for every u), as the rule
+// saturates; step is read off the exponent of max(a, 1): 2^e / 2, with
+// 1/step = 2 / 2^e, both formed on the exponent bits.
+__device__ __forceinline__ F2 sr_mag2(F2 aq, F2 negn) {
+  const float a0 = fminf(aq.x, 6.0f), a1 = fminf(aq.y, 6.0f);
+  const uint32_t p0 = __float_as_uint(fmaxf(a0, 1.0f)) & 0x7F800000u;
+  const uint32_t p1 = __float_as_uint(fmaxf(a1, 1.0f)) & 0x7F800000u;
+  const F2 inv{__uint_as_float(0x7F800000u - p0), __uint_as_float(0x7F800000u - p1)};
+  const F2 step{__uint_as_float(p0 - 0x00800000u), __uint_as_float(p1 - 0x00800000u)};
+  const F2 t = mul2(F2{a0, a1}, inv);
+  F2 c;
+  asm("{\n\t.reg .b64 rn, rs, rt, rd, rm, rc;\n\t"
+      "mov.b64 rn, {%2, %3};\n\tmov.b64 rs, {%4, %4};\n\tmov.b64 rt, {%5, %6};\n\t"
+      "fma.rp.f32x2 rd, rn, rs, rt;\n\t"
+      "mov.b64 rm, {%7, %7};\n\t"
+      "add.rp.f32x2 rc, rd, rm;\n\t"
+      "sub.rn.f32x2 rc, rc, rm;\n\t"
+      "mov.b64 {%0, %1}, rc;\n\t}"
+      : "=f"(c.x), "=f"(c.y)
+      : "f"(negn.x), "f"(negn.y), "f"(5.9604644775390625e-8f), "f"(t.x), "f"(t.y), "f"(12582912.0f));
+  return mul2(c, step);
 }
 
 // Stochastic-rounding codes of one candidate (w: the 16 elements' words).
@@ -421,12 +445,13 @@ __device__ __forceinline__ float cand_sr16(const float (&y)[16], float inv, cons
   uint32_t b[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    F2 q = mul2(F2{y[2 * k], y[2 * k + 1]}, F2{inv, inv});
-    float a0 = fabsf(q.x), a1 = fabsf(q.y);
-    float g0 = sr_mag(a0, w[2 * k]), g1 = sr_mag(a1, w[2 * k + 1]);
+    const F2 q = mul2(F2{y[2 * k], y[2 * k + 1]}, F2{inv, inv});
+    const F2 aq{fabsf(q.x), fabsf(q.y)};
+    const F2 negn{-(float)(w[2 * k] >> 8), -(float)(w[2 * k + 1] >> 8)};
+    const F2 g = sr_mag2(aq, negn);
     // the grid value with q's sign converts exactly
-    b[k] = e2m1x2(copysignf(g0, q.x), copysignf(g1, q.y));
-    F2 r = sub2(F2{a0, a1}, F2{g0, g1});
+    b[k] = e2m1x2(copysignf(g.x, q.x), copysignf(g.y, q.y));
+    const F2 r = sub2(aq, g);
     acc = fma2(r, r, acc);
   }
   lo = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
