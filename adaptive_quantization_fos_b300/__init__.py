@@ -115,6 +115,10 @@ def _load() -> ctypes.CDLL:
         "fos_quantize_batch": (i32, [ctypes.POINTER(fos_quant_job), i32, ctypes.POINTER(fos_quant_options), vp, sz,
                                      vp]),
         "fos_linear_backward_workspace_size": (i32, [i64, i64, i64, ctypes.POINTER(sz)]),
+        "fos_linear_forward_workspace_size": (i32, [i64, i64, ctypes.POINTER(sz)]),
+        "fos_linear_forward_operand": (i32, [i64, i64, vp, sz, ctypes.POINTER(fos_nvfp4_tensor)]),
+        "fos_linear_forward": (i32, [vp, i64, i64, i64, ctypes.POINTER(fos_quant_options),
+                                     ctypes.POINTER(fos_nvfp4_tensor), vp, i64, vp, sz, vp, vp]),
         "fos_linear_backward_operands": (i32, [i64, i64, i64, vp, sz, ctypes.POINTER(fos_nvfp4_tensor)]),
         "fos_linear_backward": (i32, [vp, i64, vp, i64, vp, i64, i64, i64, i64, ctypes.POINTER(fos_backward_options),
                                       vp, i64, vp, i64, vp, sz, vp, vp]),
@@ -131,7 +135,8 @@ EXPORTED = ("fos_abi_version", "fos_status_string", "fos_sf_bytes", "fos_quantiz
             "fos_tensor_amax", "fos_quantize", "fos_quantize_noalloc", "fos_dequantize", "fos_gemm", "fos_e2m1_encode",
             "fos_e4m3_encode", "fos_philox4x32_10", "fos_selftest_wait_limits", "fos_quantize_batch",
             "fos_quantize_batch_workspace_size", "fos_linear_backward", "fos_linear_backward_workspace_size",
-            "fos_linear_backward_operands")
+            "fos_linear_backward_operands", "fos_linear_forward", "fos_linear_forward_workspace_size",
+            "fos_linear_forward_operand")
 
 
 def _check(status: int, what: str) -> None:
@@ -465,3 +470,60 @@ class LinearBackward:
                 sf=self.workspace[s0:s0 + sfb], tensor_scale=self.workspace[t0:t0 + 4].view(torch.float32),
                 rows=d.rows, cols=d.cols, sf_layout=d.sf_layout))
         return out
+
+
+# ------------------------------------------------------- linear forward
+
+
+def fos_linear_forward_workspace_size(M: int, K: int) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.fos_linear_forward_workspace_size(M, K, ctypes.byref(n)), "fos_linear_forward_workspace_size")
+    return n.value
+
+
+def fos_linear_forward_operand(M: int, K: int, workspace, workspace_bytes: int) -> fos_nvfp4_tensor:
+    t = fos_nvfp4_tensor()
+    _check(_lib.fos_linear_forward_operand(M, K, workspace, workspace_bytes, ctypes.byref(t)),
+           "fos_linear_forward_operand")
+    return t
+
+
+def fos_linear_forward(x, ld_x, M, K, x_opt: fos_quant_options, w: fos_nvfp4_tensor, y, ld_y, workspace,
+                       workspace_bytes, dev_status, stream) -> int:
+    return int(_lib.fos_linear_forward(x, ld_x, M, K, ctypes.byref(x_opt), ctypes.byref(w), y, ld_y, workspace,
+                                       workspace_bytes, dev_status or None, stream))
+
+
+class LinearForward:
+    """Y = X W^T through fos_linear_forward: X [M, K] quantized with the given
+    options, then multiplied by W, an NVFP4Tensor quantized beforehand along K
+    (with the same RHT seed when hadamard is set)."""
+
+    def __init__(self, M: int, K: int, *, device="cuda", **opts):
+        torch = _torch()
+        self.M, self.K = M, K
+        self.opt = options(**opts)
+        self.ws_bytes = fos_linear_forward_workspace_size(M, K)
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+
+    def __call__(self, x, w: NVFP4Tensor, out=None, status=None, stream=None):
+        torch = _torch()
+        assert x.dtype == torch.bfloat16 and tuple(x.shape) == (self.M, self.K) and x.stride(1) == 1
+        if out is None:
+            out = torch.empty((self.M, w.rows), dtype=torch.bfloat16, device=x.device)
+        st = fos_linear_forward(x.data_ptr(), x.stride(0), self.M, self.K, self.opt, w.as_c(), out.data_ptr(),
+                                out.stride(0), self.workspace.data_ptr(), self.ws_bytes,
+                                status.data_ptr() if status is not None else 0, _stream_ptr(stream))
+        _check(st, "fos_linear_forward")
+        return out
+
+    def operand(self) -> NVFP4Tensor:
+        """X's quantized operand as a view into the workspace."""
+        torch = _torch()
+        base = self.workspace.data_ptr()
+        d = fos_linear_forward_operand(self.M, self.K, base, self.ws_bytes)
+        c0, s0, t0 = d.codes - base, d.sf - base, d.tensor_scale - base
+        sfb = fos_sf_bytes(d.rows, d.cols, d.sf_layout)
+        return NVFP4Tensor(codes=self.workspace[c0:c0 + d.rows * d.ld_codes].view(d.rows, d.ld_codes),
+                           sf=self.workspace[s0:s0 + sfb], tensor_scale=self.workspace[t0:t0 + 4].view(torch.float32),
+                           rows=d.rows, cols=d.cols, sf_layout=d.sf_layout)

@@ -438,8 +438,15 @@ __device__ __forceinline__ F2 sr_mag2(F2 aq, F2 negn) {
   return mul2(c, step);
 }
 
-// Stochastic-rounding codes of one candidate (w: the 16 elements' words).
-__device__ __forceinline__ float cand_sr16(const float (&y)[16], float inv, const uint32_t (&w)[16], uint32_t& lo,
+// -n = -(w >> 8) of the 16 elements' words, once per block: both
+// candidates round with the same u = n * 2^-24.
+__device__ __forceinline__ void sr_negn16(const uint32_t (&w)[16], float (&negn)[16]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) negn[j] = -(float)(w[j] >> 8);
+}
+
+// Stochastic-rounding codes of one candidate (negn from sr_negn16).
+__device__ __forceinline__ float cand_sr16(const float (&y)[16], float inv, const float (&negn)[16], uint32_t& lo,
                                            uint32_t& hi) {
   F2 acc{0.0f, 0.0f};
   uint32_t b[8];
@@ -447,8 +454,7 @@ __device__ __forceinline__ float cand_sr16(const float (&y)[16], float inv, cons
   for (int k = 0; k < 8; ++k) {
     const F2 q = mul2(F2{y[2 * k], y[2 * k + 1]}, F2{inv, inv});
     const F2 aq{fabsf(q.x), fabsf(q.y)};
-    const F2 negn{-(float)(w[2 * k] >> 8), -(float)(w[2 * k + 1] >> 8)};
-    const F2 g = sr_mag2(aq, negn);
+    const F2 g = sr_mag2(aq, F2{negn[2 * k], negn[2 * k + 1]});
     // the grid value with q's sign converts exactly
     b[k] = e2m1x2(copysignf(g.x, q.x), copysignf(g.y, q.y));
     const F2 r = sub2(aq, g);

@@ -224,6 +224,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Programmatic dependent launch: wait until the kernel this launch depends on
+// (the stream's previous one, when launched with programmatic serialization)
+// has completed and its writes are visible; a no-op otherwise.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void raise_timeout(const GemmArgs& a, volatile int* abort) {
   *abort = 1;
   if (a.status) atomicExch(a.status, (int)FOS_ERR_TIMEOUT);
@@ -289,9 +294,44 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       uint32_t ph = 0;
       int issued = 0;
       bool ok = true;
+      // B's codes and scales for the first tile's first stages need nothing
+      // from an earlier kernel, so they are requested before this CTA waits
+      // for the previous kernel of the stream (A's producer, under
+      // programmatic dependent launch); A and its scales follow the wait.
+      // Stage slots start empty, so these stages need no empty-barrier wait.
+      const int pre = (!args.stall_test && (int)blockIdx.x < n_tiles) ? min(C::kStages, args.num_kb) : 0;
+      {
+        const int mb = (int)blockIdx.x % args.tiles_m, nb = (int)blockIdx.x / args.tiles_m;
+        int halves = 0;
+        for (int h = 0; h < BN / 128; ++h)
+          if ((nb * (BN / 128) + h) * 128 < args.n) ++halves;
+        for (int kb = 0; kb < pre; ++kb) {
+          const int kkc = min(4, kmma_total - 4 * kb);
+          const uint32_t st = smem_u32(smem + kb * C::kStageBytes);
+          const uint32_t sfa_dst = st + C::kABytes + C::kBBytes;
+          mbar_expect_tx(sf_full(kb), (1 + halves) * kkc * kSfChunk);
+          for (int h = 0; h < halves; ++h)
+            bulk_load(sfa_dst + C::kSfaBytes + h * 4 * kSfChunk,
+                      args.sfb + ((int64_t)(nb * (BN / 128) + h) * args.sf_ktiles + 4 * kb) * kSfChunk,
+                      kkc * kSfChunk, sf_full(kb));
+          mbar_expect_tx(full_bar(kb), C::kABytes + C::kBBytes);
+          tma_load_2d(st + C::kABytes, &tm_b, kb * kBKBytes, nb * BN, full_bar(kb));
+        }
+        pdl_wait();
+        for (int kb = 0; kb < pre; ++kb) {
+          const int kkc = min(4, kmma_total - 4 * kb);
+          const uint32_t st = smem_u32(smem + kb * C::kStageBytes);
+          bulk_load(st + C::kABytes + C::kBBytes, args.sfa + ((int64_t)mb * args.sf_ktiles + 4 * kb) * kSfChunk,
+                    kkc * kSfChunk, sf_full(kb));
+          tma_load_2d(st, &tm_a, kb * kBKBytes, mb * kBM, full_bar(kb));
+          ++issued;
+        }
+        s = pre % C::kStages;
+        ph = pre == C::kStages ? 1u : 0u;
+      }
       for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
         const int mb = t % args.tiles_m, nb = t / args.tiles_m;
-        for (int kb = 0; kb < args.num_kb; ++kb) {
+        for (int kb = t == (int)blockIdx.x ? pre : 0; kb < args.num_kb; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u, args.timeout_ns, abort)) {
             raise_timeout(args, abort);
             ok = false;
@@ -399,7 +439,8 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     const int h = (warp - 2) / 4;              // which 128-column half of the tile
     const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + 128 * h;
     const uint32_t quad = (uint32_t)(32 * q) << 16;
-    const float alpha = __fmul_rn(__ldg(args.sta), __ldg(args.stb));
+    pdl_wait();  // A's tensor scale comes from the previous kernel under programmatic launch
+    const float alpha = __fmul_rn(__ldcg(args.sta), __ldcg(args.stb));
     uint32_t acc_ph = 0;
     // scale-staging cursor: the next stage (tile, k block) in this CTA's sequence
     int sf_s = 0, sf_t = blockIdx.x, sf_kb = 0;
@@ -583,7 +624,8 @@ int sm_count() {
 
 template <int BN>
 fos_status launch_gemm(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* Cout, int64_t ldc,
-                       int32_t* dev_status, uint64_t timeout_ns, int stall_test, int grid_cap, cudaStream_t stream) {
+                       int32_t* dev_status, uint64_t timeout_ns, int stall_test, int grid_cap, bool pdl,
+                       cudaStream_t stream) {
   using C = Cfg<BN>;
   CUtensorMap ta, tb;
   const int64_t kbytes = A->cols / 2;
@@ -615,12 +657,21 @@ fos_status launch_gemm(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, voi
   if (cudaFuncSetAttribute(gemm_nvfp4_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
       cudaSuccess)
     return FOS_ERR_CUDA;
-  gemm_nvfp4_kernel<BN><<<grid, C::kThreads, C::kSmemBytes, stream>>>(ta, tb, a);
-  return cudaGetLastError() == cudaSuccess ? FOS_OK : FOS_ERR_CUDA;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)C::kThreads);
+  cfg.dynamicSmemBytes = (size_t)C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gemm_nvfp4_kernel<BN>, ta, tb, a) == cudaSuccess ? FOS_OK : FOS_ERR_CUDA;
 }
 
 fos_status gemm_checked(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* C, int64_t ldc,
-                        int32_t* dev_status, uint64_t timeout_ns, int stall_test, cudaStream_t stream) {
+                        int32_t* dev_status, uint64_t timeout_ns, int stall_test, bool pdl, cudaStream_t stream) {
   if (!valid_operand(A) || !valid_operand(B) || !C) return FOS_ERR_INVALID_ARG;
   if (A->cols != B->cols || B->rows % 8 != 0) return FOS_ERR_INVALID_ARG;
   if (ldc < B->rows || ldc % 8 != 0 || !aligned(C, 16)) return FOS_ERR_INVALID_ARG;
@@ -628,8 +679,8 @@ fos_status gemm_checked(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, vo
   if (A->rows == 0 || B->rows == 0) return FOS_OK;
   // 256-column tiles unless the last one would be half empty
   if (B->rows % 256 == 0 || B->rows % 256 > 128)
-    return launch_gemm<256>(A, B, C, ldc, dev_status, timeout_ns, stall_test, 0, stream);
-  return launch_gemm<128>(A, B, C, ldc, dev_status, timeout_ns, stall_test, 0, stream);
+    return launch_gemm<256>(A, B, C, ldc, dev_status, timeout_ns, stall_test, 0, pdl, stream);
+  return launch_gemm<128>(A, B, C, ldc, dev_status, timeout_ns, stall_test, 0, pdl, stream);
 }
 
 }  // namespace
@@ -645,11 +696,16 @@ fos_status gemm_stall_selftest(void* scratch, size_t scratch_bytes, uint64_t tim
   fos_nvfp4_tensor B{b + 16384, b + 34816, reinterpret_cast<float*>(b + 36864), 128, 256, 128,
                      FOS_SF_SWIZZLED_128x4, 0};
   if (cudaMemsetAsync(b, 0, 40960, s) != cudaSuccess) return FOS_ERR_CUDA;
-  return launch_gemm<128>(&A, &B, b + 40960, 128, status, timeout_ns, 1, 1, s);
+  return launch_gemm<128>(&A, &B, b + 40960, 128, status, timeout_ns, 1, 1, false, s);
+}
+
+fos_status gemm_after_producer_of_a(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* C, int64_t ldc,
+                                    int32_t* dev_status, cudaStream_t stream) {
+  return gemm_checked(A, B, C, ldc, dev_status, kDefaultTimeoutNs, 0, true, stream);
 }
 }  // namespace fos
 
 extern "C" fos_status fos_gemm(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* C, int64_t ldc,
                                int32_t* dev_status, cudaStream_t stream) {
-  return gemm_checked(A, B, C, ldc, dev_status, kDefaultTimeoutNs, 0, stream);
+  return gemm_checked(A, B, C, ldc, dev_status, kDefaultTimeoutNs, 0, false, stream);
 }

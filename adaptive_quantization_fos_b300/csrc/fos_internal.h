@@ -87,6 +87,12 @@ cudaError_t launch_dequant(const DequantParams& p, bool bf16, cudaStream_t s);
 // FOS_ERR_TIMEOUT to *status.
 fos_status gemm_stall_selftest(void* scratch, size_t scratch_bytes, uint64_t timeout_ns, int32_t* status,
                                cudaStream_t s);
+// fos_gemm launched with programmatic dependent launch for a stream whose
+// previous kernel produces A (its codes, scales and tensor scale) and writes
+// nothing B depends on: each CTA loads B's first stages before waiting for
+// that kernel, then A.  Only for that pairing: B is read before the wait.
+fos_status gemm_after_producer_of_a(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* C, int64_t ldc,
+                                    int32_t* dev_status, cudaStream_t stream);
 // *out = FOS_ERR_TIMEOUT if *tensor_scale is NaN, else FOS_OK.
 cudaError_t launch_nan_to_status(const float* tensor_scale, int32_t* out, cudaStream_t s);
 cudaError_t launch_e2m1_encode(const float* x, int64_t n, uint8_t* out, cudaStream_t s);

@@ -1,5 +1,5 @@
-// The quantized linear layer's backward pass as a composition of the
-// library's own calls: four quantizations (fos_quantize) and two block-scaled
+// The quantized linear layer's forward and backward passes as compositions of
+// the library's own calls: quantizations (fos_quantize) and block-scaled
 // products (fos_gemm), all enqueued on the caller's stream.
 //
 // "Four Over Six" ("Training"): the quantized linear layer carries a backward
@@ -62,6 +62,35 @@ Layout layout(int64_t M, int64_t N, int64_t K) {
 bool valid_bf16(const void* p, int64_t ld, int64_t row_len) {
   return p && aligned(p, 16) && ld >= row_len && ld % 8 == 0;
 }
+
+}  // namespace
+
+// ------------------------------------------------------------ forward
+// Y = X W^T with W already quantized (offline, along K; with the RHT of the
+// same seed when X gets it, so that the transform cancels in the product):
+// X is quantized into the workspace, then the GEMM runs as the quantizer's
+// programmatic dependent, loading W's first stages during the quantizer's
+// tail.  The quantizer is not folded into the GEMM's producer: every 128-row
+// tile of X feeds all N/256 output-column tiles, so it would be quantized
+// that many times over.
+
+namespace {
+
+struct FwdLayout {
+  size_t codes, sf, scale, scratch, total;
+};
+
+FwdLayout fwd_layout(int64_t M, int64_t K) {
+  FwdLayout L{};
+  L.codes = 0;
+  L.sf = up((size_t)(M * codes_ld(K)));
+  L.scale = up(L.sf + (size_t)sf_bytes(M, K));
+  L.scratch = up(L.scale + sizeof(float));
+  L.total = L.scratch + fos::kQuantWorkspaceBytes;
+  return L;
+}
+
+bool valid_fwd_shape(int64_t M, int64_t K) { return M > 0 && K > 0 && K % 64 == 0 && M <= INT32_MAX && K <= INT32_MAX; }
 
 }  // namespace
 
@@ -149,6 +178,52 @@ fos_status fos_linear_backward(const void* dy, int64_t ld_dy, const void* x, int
     if ((st = fos_gemm(&ops[2], &ops[3], dw, ld_dw, dev_status, stream)) != FOS_OK) return st;
   }
   return FOS_OK;
+}
+
+
+fos_status fos_linear_forward_workspace_size(int64_t M, int64_t K, size_t* bytes) {
+  if (!bytes || !valid_fwd_shape(M, K)) return FOS_ERR_INVALID_ARG;
+  *bytes = fwd_layout(M, K).total;
+  return FOS_OK;
+}
+
+fos_status fos_linear_forward_operand(int64_t M, int64_t K, void* workspace, size_t workspace_bytes,
+                                      fos_nvfp4_tensor* xq) {
+  if (!xq || !workspace || !valid_fwd_shape(M, K) || !aligned(workspace, kAlign)) return FOS_ERR_INVALID_ARG;
+  const FwdLayout L = fwd_layout(M, K);
+  if (workspace_bytes < L.total) return FOS_ERR_INVALID_ARG;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  xq->codes = base + L.codes;
+  xq->sf = base + L.sf;
+  xq->tensor_scale = reinterpret_cast<const float*>(base + L.scale);
+  xq->rows = M;
+  xq->cols = K;
+  xq->ld_codes = codes_ld(K);
+  xq->sf_layout = FOS_SF_SWIZZLED_128x4;
+  xq->reserved = 0;
+  return FOS_OK;
+}
+
+fos_status fos_linear_forward(const void* x, int64_t ld_x, int64_t M, int64_t K, const fos_quant_options* x_opt,
+                              const fos_nvfp4_tensor* w, void* y, int64_t ld_y, void* workspace,
+                              size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream) {
+  if (!x_opt || !w || x_opt->transpose || x_opt->sf_layout != FOS_SF_SWIZZLED_128x4) return FOS_ERR_INVALID_ARG;
+  if (w->cols != K || w->sf_layout != FOS_SF_SWIZZLED_128x4) return FOS_ERR_INVALID_ARG;
+  if (!valid_bf16(y, ld_y, w->rows) || (dev_status && !aligned(dev_status, 4))) return FOS_ERR_INVALID_ARG;
+  fos_nvfp4_tensor xq;
+  fos_status st = fos_linear_forward_operand(M, K, workspace, workspace_bytes, &xq);
+  if (st != FOS_OK) return st;
+  // the GEMM's own checks, on the operand the quantizer is about to write
+  if (!w->codes || !w->sf || !w->tensor_scale || w->rows <= 0 || w->rows % 8 != 0 || w->ld_codes % 16 != 0 ||
+      w->ld_codes < K / 2 || !aligned(w->codes, 16) || !aligned(w->sf, 16))
+    return FOS_ERR_INVALID_ARG;
+  const FwdLayout L = fwd_layout(M, K);
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  st = fos_quantize(x, M, K, ld_x, x_opt, base + L.codes, xq.ld_codes, base + L.sf,
+                    reinterpret_cast<float*>(base + L.scale), nullptr, base + L.scratch, fos::kQuantWorkspaceBytes,
+                    stream);
+  if (st != FOS_OK) return st;
+  return fos::gemm_after_producer_of_a(&xq, w, y, ld_y, dev_status, stream);
 }
 
 }  // extern "C"

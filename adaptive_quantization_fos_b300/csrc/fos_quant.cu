@@ -247,7 +247,7 @@ __device__ __forceinline__ void quant_block_tab(const uint64_t (&yp)[8], float a
                                                 uint32_t& hi, uint32_t& sf, bool& four) {
   const uint32_t pair = e4m3x2(__fmul_rn(ab, tc.k6), __fmul_rn(ab, tc.k4));
   const uint32_t sf6 = pair & 0xFFu, sf4 = pair >> 8;
-  float y[16];
+  float y[16], negn[16];
   if (SR) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -255,6 +255,7 @@ __device__ __forceinline__ void quant_block_tab(const uint64_t (&yp)[8], float a
       y[2 * k] = v.x;
       y[2 * k + 1] = v.y;
     }
+    sr_negn16(w, negn);
   }
   uint32_t lo6 = 0, hi6 = 0, lo4 = 0, hi4 = 0;
   float E6 = 0.0f, E4 = 0.0f;
@@ -266,7 +267,7 @@ __device__ __forceinline__ void quant_block_tab(const uint64_t (&yp)[8], float a
     uint32_t l, h;
     float S;
     if (SR) {
-      S = cand_sr16(y, t.x, w, l, h);
+      S = cand_sr16(y, t.x, negn, l, h);
     } else {
       const uint64_t inv2 = pack_f2(t.x, t.x);
       uint64_t acc = 0ull;
@@ -435,10 +436,8 @@ __global__ void __launch_bounds__(MODE == kRowsChained ? 320 : 256, MODE == kRow
     s_next_done = 0u;
   }
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  if constexpr (!FUSED) {
-    __syncthreads();  // the barriers are initialised before the roles split
-    pdl_launch_dependents();
-  }
+  if constexpr (!FUSED) __syncthreads();  // the barriers are initialised before the roles split
+  pdl_launch_dependents();
   const uint32_t rht_mask = RHT ? rht_sign_mask(p.hk0, p.hk1) : 0u;
   const int64_t nb = p.nb;
   const int64_t wpr = (nb + 127) >> 7;  // warp tasks per row
@@ -754,6 +753,8 @@ __global__ void __launch_bounds__(256) quant_2d_kernel(QuantParams p) {
     const float ab = half_max(absmax16(y));
     uint32_t w[16];
     sr_words16<SR>((uint64_t)r * (uint64_t)p.cols + (uint64_t)c0, p, w);
+    float negn[16];
+    if (SR) sr_negn16(w, negn);
     const uint32_t pair = e4m3x2(__fmul_rn(ab, tc.k6), __fmul_rn(ab, tc.k4));
     const uint32_t sf6 = pair & 0xFFu, sf4 = pair >> 8;
     uint64_t yp[8];
@@ -770,7 +771,7 @@ __global__ void __launch_bounds__(256) quant_2d_kernel(QuantParams p) {
       uint32_t l, h;
       float S;
       if (SR) {
-        S = cand_sr16(y, tb.x, w, l, h);
+        S = cand_sr16(y, tb.x, negn, l, h);
       } else {
         const uint64_t inv2 = pack_f2(tb.x, tb.x);
         uint64_t acc = 0ull;

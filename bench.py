@@ -516,7 +516,9 @@ def linear_backward(torch, fos, dev, pk) -> dict:
 
 def linear_forward(torch, fos, dev, pk) -> dict:
     """Quantize A (8192 x 4096 activations) and W (12288 x 4096 weights) with
-    4/6 1D RNE, then C = A W^T in NVFP4 on the tensor cores."""
+    4/6 1D RNE, then C = A W^T in NVFP4 on the tensor cores.  Also the whole
+    layer through fos_linear_forward (A quantized, then the GEMM) against W
+    quantized once beforehand."""
     A = _to_dev(torch, workloads.activations(8192, 4096, seed=5001), dev)
     W = _to_dev(torch, workloads.student_t(12288, 4096, seed=5002), dev)
     qa, qw = fos.Quantizer(*A.shape, device=dev), fos.Quantizer(*W.shape, device=dev)
@@ -527,11 +529,18 @@ def linear_forward(torch, fos, dev, pk) -> dict:
     except fos.FosError as e:
         return {"status": f"gemm unavailable: {e}"}
     flops = 2.0 * 8192 * 12288 * 4096
+    layer = fos.LinearForward(8192, 4096, device=dev)
     with ClockSampler(dev.index) as clk:
         t = _time_calls(torch, lambda: fos.gemm(a, w, out=C), 50)
+        # the whole layer: X quantized (one-launch quantizer), then the GEMM as
+        # its programmatic dependent; and the same two steps as separate calls
+        t_layer = _time_calls(torch, lambda: layer(A, w, out=C), 50)
+        t_two = _time_calls(torch, lambda: (qa(A), fos.gemm(a, w, out=C)), 50)
     tf = flops / (t * 1e-3) / 1e12
     fp4_peak = pk["bf16_tflops"] * 6.0  # measured bf16 burst x nominal dense fp4/bf16 ratio (13.5 / 2.25)
     return {"gemm_ms": round(t, 4), "tflops": round(tf, 1), "clocks": clk.summary(),
+            "layer_forward_ms": round(t_layer, 4), "layer_forward_tflops": round(flops / (t_layer * 1e-3) / 1e12, 1),
+            "quantize_then_gemm_ms": round(t_two, 4),
             "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                          "frac": round(tf / fp4_peak, 4),
                          "peak_source": "measured bf16 burst x 6 (nominal dense fp4/bf16 ratio)"}}
@@ -603,6 +612,23 @@ def run_case(args) -> None:
         x = _to_dev(torch, workloads.student_t(12288, 8192, seed=9001), dev)
         amax = fos.tensor_amax(x)
         q = fos.Quantizer(*x.shape, device=dev, tensor_amax=amax)
+        for _ in range(3):
+            q(x)
+    elif args.case == "quant_rows_sr":
+        # 8192 x 12288 gradient (201 MB > L2), stochastic rounding, amax
+        # supplied: only the row quantize kernel runs
+        x = _to_dev(torch, workloads.gradients(8192, 12288, seed=4001), dev)
+        amax = fos.tensor_amax(x)
+        q = fos.Quantizer(*x.shape, device=dev, tensor_amax=amax, rounding=fos.FOS_ROUND_STOCHASTIC, sr_seed=4002)
+        for _ in range(3):
+            q(x)
+    elif args.case == "quant_cols_sr_rht":
+        # the same gradient transposed (blocks along its rows) with SR and the
+        # RHT, amax supplied: only the transposed quantize kernel runs
+        x = _to_dev(torch, workloads.gradients(8192, 12288, seed=4001), dev)
+        amax = fos.tensor_amax(x, hadamard=True, transpose=True, hadamard_seed=12)
+        q = fos.Quantizer(*x.shape, device=dev, tensor_amax=amax, rounding=fos.FOS_ROUND_STOCHASTIC, sr_seed=11,
+                          transpose=True, hadamard=True, hadamard_seed=12)
         for _ in range(3):
             q(x)
     elif args.case == "gemm":

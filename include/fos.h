@@ -309,6 +309,39 @@ fos_status fos_linear_backward(const void* dy, int64_t ld_dy, const void* x, int
                                void* dx, int64_t ld_dx, void* dw, int64_t ld_dw, void* workspace,
                                size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream);
 
+/* ---- quantized linear forward ---- */
+
+/* Device scratch of fos_linear_forward for X [M, K] (K % 64 == 0). */
+fos_status fos_linear_forward_workspace_size(int64_t M, int64_t K, size_t* bytes);
+
+/* X's quantized operand [M, K] as it lies in a fos_linear_forward workspace
+ * (valid after a call on it): codes with 16-byte-padded rows, then
+ * FOS_SF_SWIZZLED_128x4 scales, then s_t, then the quantizer's scratch, each
+ * 256-byte aligned. */
+fos_status fos_linear_forward_operand(int64_t M, int64_t K, void* workspace, size_t workspace_bytes,
+                                      fos_nvfp4_tensor* xq);
+
+/*
+ * fos_linear_forward -- Y = X W^T for the quantized linear layer ("Four Over
+ * Six": the layer quantizes its input, then contracts in NVFP4): X bf16
+ * [M, K] is quantized with x_opt into the workspace (exactly fos_quantize),
+ * then multiplied by the already quantized W [N, K] (exactly fos_gemm).
+ * The GEMM is launched as a programmatic dependent of the quantizer: its CTAs
+ * start during the quantizer's tail and load W's first stages, and wait for
+ * the quantizer before touching X's operand.  W may come from work enqueued
+ * before this call (that work completes before the quantizer starts, and the
+ * quantizer writes only X's operand).  Quantize W once, offline, with the
+ * same RHT seed along K as x_opt when x_opt->hadamard is set.
+ *   x_opt     transpose must be 0 and sf_layout FOS_SF_SWIZZLED_128x4;
+ *             block_2d, hadamard, stochastic rounding and a supplied
+ *             tensor_amax (delayed scaling) are allowed.
+ *   w         K-major NVFP4 operand, w->cols == K (see fos_gemm).
+ *   y         device bf16 [M][ld_y], ld_y >= w->rows, ld_y % 8 == 0.
+ */
+fos_status fos_linear_forward(const void* x, int64_t ld_x, int64_t M, int64_t K, const fos_quant_options* x_opt,
+                              const fos_nvfp4_tensor* w, void* y, int64_t ld_y, void* workspace,
+                              size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream);
+
 /*
  * fos_selftest_wait_limits -- runs the library's bounded device waits into
  * their limits on purpose and reports what the kernels recorded, so a caller

@@ -162,6 +162,40 @@ def test_linear_backward_validation(fos):
         fos.fos_linear_backward_workspace_size(100, N, K)
 
 
+def test_linear_forward_validation(fos):
+    """fos_linear_forward's argument checks (fake device addresses; nothing here
+    reaches a launch)."""
+    INVALID = fos.FOS_ERR_INVALID_ARG
+    fake = 1 << 20
+    M, K, N = 256, 512, 384
+    ws = fos.fos_linear_forward_workspace_size(M, K)
+    W = fos.fos_nvfp4_tensor(codes=fake, sf=fake, tensor_scale=fake, rows=N, cols=K, ld_codes=K // 2)
+
+    def call(x=fake, ld_x=K, M=M, K=K, o=None, w=W, y=fake, ld_y=N, wsp=fake, wsb=ws, status=0):
+        return fos.fos_linear_forward(x, ld_x, M, K, o if o is not None else fos.options(), w, y, ld_y, wsp, wsb,
+                                      status, 0)
+
+    assert call(K=480) == INVALID  # K % 64 (one MMA step)
+    assert call(M=0) == INVALID
+    assert call(o=fos.options(transpose=True)) == INVALID
+    assert call(o=fos.options(sf_layout=fos.FOS_SF_ROWMAJOR)) == INVALID
+    assert call(ld_y=N - 8) == INVALID
+    assert call(y=fake + 4) == INVALID
+    assert call(wsb=ws - 1) == INVALID
+    assert call(wsp=fake + 64) == INVALID
+    assert call(status=fake + 1) == INVALID
+    W.cols = K + 64
+    assert call() == INVALID  # W's K differs
+    W.cols, W.rows = K, N - 4
+    assert call() == INVALID  # N % 8
+    W.rows, W.ld_codes = N, K // 2 + 8
+    assert call() == INVALID  # ld_codes % 16
+    W.ld_codes, W.sf_layout = K // 2, fos.FOS_SF_ROWMAJOR
+    assert call() == INVALID
+    d = fos.fos_linear_forward_operand(M, K, fake, ws)
+    assert (d.rows, d.cols, d.ld_codes) == (M, K, K // 2) and d.sf % 256 == 0 and d.tensor_scale % 256 == 0
+
+
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     import importlib.util
 
