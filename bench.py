@@ -45,7 +45,7 @@ WORKLOAD = ("qwen3-8b layer weights q,k,v,o,gate,up,down (192.9M bf16 values, St
 BYTES_PER_ELEM_QUANT = 2.0 + 0.5 + 1.0 / 16.0  # read bf16, write 4-bit code + 1/16 E4M3 scale
 CPU_SAMPLE_ROWS = 2048  # rows of each matrix timed on the host for the CPU baseline
 REF_SAMPLE_ROWS = 256  # rows of each matrix per step of the reference arm
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "quant_rows_chained_traffic.txt")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "quant_batch_step_traffic.txt")
 
 
 def peaks() -> dict:
@@ -323,8 +323,9 @@ def run_fos(args, dist: Dist) -> None:
                 "peak_source": pk["source"] + " copy bandwidth (hbm_gbs), burst",
                 "bytes_per_elem": BYTES_PER_ELEM_QUANT,
                 "traffic": None if tpe is None else round(tpe * elems / len(mats)),
-                "traffic_note": "DRAM read+write bytes per quantize launch (average over the 7), scaled by values "
-                                "from the committed ncu capture of the same kernel" if tpe else "no current capture",
+                "traffic_note": "DRAM read+write bytes per quantize launch (a step's total over its 7 quantize "
+                                "launches), from the committed warm-cache ncu capture of one batch call (all 8 "
+                                "launches, amax re-reads included), scaled by values" if tpe else "no current capture",
                 "algorithmic_bytes_per_launch": round(BYTES_PER_ELEM_QUANT * elems / len(mats)),
                 "avg_launch_us": round(tot_t / n_launch * 1e3, 2),
                 "timed": "per step (the 8 launches of one batch), averaged over launches"}
