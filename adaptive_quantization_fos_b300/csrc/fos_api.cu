@@ -172,7 +172,9 @@ fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
     tasks = (rows / 16) * ((cols / 16 + 1) / 2);
   } else if (tr) {
     kind = 1;
-    tasks = (rows / 16) * ((cols + 127) / 128);
+    // warp tasks of 64 source rows x 128 (RNE) or 64 (stochastic) source columns
+    tasks = ((rows / 16 + 3) / 4) * ((cols + (opt->rounding == FOS_ROUND_STOCHASTIC ? 63 : 127)) /
+                                     (opt->rounding == FOS_ROUND_STOCHASTIC ? 64 : 128));
   } else {
     kind = 0;
     tasks = R * ((nb + 127) / 128);

@@ -626,61 +626,155 @@ __global__ void __launch_bounds__(MODE == kRowsChained ? 320 : 256, MODE == kRow
 // ------------------------------------------------------------ quant_cols
 // Transposed output: a lane owns source columns c0..c0+3 (output rows) and
 // the 16 source rows of output block rb.
+// Transposed input (blocks run down X's columns; output row c of the result
+// is source column c).  A lane owns CPL adjacent source columns (4 with RNE,
+// 2 with stochastic rounding, whose words take registers); warp task = 64
+// source rows (4 block-rows) x 32*CPL source columns.  Each block-row of the
+// task (16 rows x 64*CPL bytes) is one slot of the warp's ring of bulk copies,
+// one copy per row issued by lanes 0..15 (the slot's barrier counts their 16
+// arrivals); a lane reads each row's 2*CPL bytes from shared memory.
+// Stochastic rounding: the Philox call for (row, 4-column group j) serves
+// lanes 2j and 2j+1; lane 2j computes rows 0-7 of the block-row and lane
+// 2j+1 rows 8-15, and each pair swaps the two words the other needs.  Each
+// block's 8 code bytes and scale byte are stored as soon as it is done; the
+// task's 4 block-rows fill 32 contiguous code bytes of each output row, which
+// L2 merges.
+constexpr int kColWarps = 8;
+constexpr int kColWarpSmem = 8192;  // ring bytes per warp: 4 slots x 2 KB (CPL 2) or 2 x 4 KB (CPL 4)
+constexpr int kColSmemBytes = kColWarps * kColWarpSmem;
+
 template <int RULE, bool RHT, bool SR>
-__global__ void __launch_bounds__(256) quant_cols_kernel(QuantParams p) {
+__global__ void __launch_bounds__(256, 2) quant_cols_kernel(QuantParams p) {
+  constexpr int CPL = SR ? 2 : 4;                 // source columns per lane
+  constexpr int kCW = 32 * CPL;                   // source columns per task
+  constexpr int kColSlotBytes = 16 * 2 * kCW;     // one block-row of the task
+  constexpr int kColSlots = kColWarpSmem / kColSlotBytes;
+  extern __shared__ __align__(128) uint8_t c_smem[];
   __shared__ float s_red[33];
   __shared__ float2 s_tab[128];
+  __shared__ uint64_t s_bar[kColWarps * 4];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x < kColWarps * kColSlots) mbar_init(smem_addr(&s_bar[threadIdx.x]), 16);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   const TensorConsts tc = quant_prologue(p, s_red);
   build_scale_table(tc.s_t, s_tab);
   __syncthreads();
   const uint32_t rht_mask = RHT ? rht_sign_mask(p.hk0, p.hk1) : 0u;
-  const int lane = threadIdx.x & 31;
-  const int64_t ngroups = (p.cols + 127) >> 7;
-  const int64_t n_tasks = (p.rows >> 4) * ngroups;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  const int64_t nb = p.nb;  // = rows / 16
-  for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n_tasks; t += nwarps) {
-    const int64_t rb = t / ngroups, c0 = (t - rb * ngroups) * 128 + 4 * lane;
-    if (c0 >= p.cols) continue;
-    uint2 d[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) d[i] = __ldg(reinterpret_cast<const uint2*>(p.x + (rb * 16 + i) * p.ld + c0));
-    // stochastic rounding: the 4 columns of a source row share one Philox call
-    U4 u4[SR ? 16 : 1];
-    if (SR) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        u4[i] = sr_words4((uint64_t)(rb * 16 + i) * (uint64_t)p.cols + (uint64_t)c0, p.sr_k0, p.sr_k1);
+  const int64_t nbr = p.rows >> 4;            // block-rows of the source = blocks per output row
+  const int64_t ngr = (nbr + 3) >> 2;          // task rows (4 block-rows each)
+  const int64_t nch = (p.cols + kCW - 1) / kCW;  // task columns (kCW source columns each)
+  const int64_t n_tasks = ngr * nch;
+  const int64_t nwarps = (int64_t)gridDim.x * kColWarps;
+  const int64_t gw = (int64_t)blockIdx.x * kColWarps + warp;
+  const uint64_t stream_once = l2_policy_evict_first();
+  uint8_t* slots = c_smem + warp * (kColSlots * kColSlotBytes);
+  const uint32_t bar0 = smem_addr(&s_bar[warp * kColSlots]);
+
+  // producer cursor (all lanes): the next (task, block-row) to fetch
+  int64_t pt = gw;
+  int psub = 0;
+  auto issue_next = [&](int slot) -> bool {
+    if (pt >= n_tasks) return false;
+    const int64_t g = pt / nch, ch = pt - g * nch;
+    const int64_t rb = 4 * g + psub;
+    const int64_t c0 = ch * kCW;
+    const uint32_t bytes = (uint32_t)((p.cols - c0 < kCW ? p.cols - c0 : kCW) * 2);
+    if (lane < 16)
+      bulk_g2s_hint(smem_addr(slots + slot * kColSlotBytes + lane * (2 * kCW)), p.x + (rb * 16 + lane) * p.ld + c0,
+                    bytes, bar0 + 8u * slot, stream_once);
+    if (++psub == 4 || 4 * g + psub >= nbr) {
+      psub = 0;
+      pt += nwarps;
     }
-#pragma unroll 1
-    for (int k = 0; k < 4; ++k) {
-      float y[16];
+    return true;
+  };
+  int issued = 0, consumed = 0;
+  for (int k = 0; k < kColSlots; ++k) issued += issue_next(k) ? 1 : 0;
+
+  int slot = 0;
+  uint32_t ph = 0;
+  bool failed = false;
+  for (int64_t t = gw; t < n_tasks && !failed; t += nwarps) {
+    const int64_t g = t / nch, ch = t - g * nch;
+    const int64_t c0 = ch * kCW;
+    const int nsub = nbr - 4 * g < 4 ? (int)(nbr - 4 * g) : 4;
+    for (int sub = 0; sub < nsub; ++sub) {
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait_for(bar0 + 8u * slot, ph, p.timeout_ns))) {
+        failed = true;
+        break;
+      }
+      uint32_t v[CPL / 2][16];  // word h of row i: columns 2h, 2h+1 of the lane
+      const uint8_t* src = slots + slot * kColSlotBytes + 2 * CPL * lane;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        uint32_t wv = (k < 2) ? d[i].x : d[i].y;
-        uint32_t s = RHT ? (((rht_mask >> i) & 1u) << 31) : 0u;
-        y[i] = __uint_as_float(((k & 1) ? (wv & 0xFFFF0000u) : (wv << 16)) ^ s);
-      }
-      if (RHT) hadamard16(y);
-      const float ab = absmax16(y);
-      uint32_t w[16];
-      if (SR) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const U4& u = u4[SR ? i : 0];
-          w[i] = k == 0 ? u.x : (k == 1 ? u.y : (k == 2 ? u.z : u.w));
+        if constexpr (CPL == 2) {
+          v[0][i] = *reinterpret_cast<const uint32_t*>(src + 2 * kCW * i);
+        } else {
+          const uint2 d = *reinterpret_cast<const uint2*>(src + 2 * kCW * i);
+          v[0][i] = d.x;
+          v[CPL / 2 - 1][i] = d.y;
         }
       }
-      uint64_t yp[8];
+      __syncwarp();
+      ++consumed;
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issued += issue_next(slot) ? 1 : 0;
+      if (++slot == kColSlots) {
+        slot = 0;
+        ph ^= 1u;
+      }
+      const int64_t rb = 4 * g + sub;
+      // the two columns' stochastic-rounding words
+      uint32_t w0[16], w1[16];
+      if (SR) {
+        const bool odd = lane & 1;
+        const uint64_t grp = (uint64_t)(c0 + 4 * (lane >> 1));
 #pragma unroll
-      for (int j = 0; j < 8; ++j) yp[j] = pack_f2(y[2 * j], y[2 * j + 1]);
-      uint32_t lo, hi, sf;
-      bool four;
-      quant_block_tab<RULE, SR>(yp, ab, tc, s_tab, w, lo, hi, sf, four);
-      const int64_t orow = c0 + k;
-      *reinterpret_cast<uint2*>(p.codes + orow * p.ld_codes + rb * 8) = make_uint2(lo, hi);
-      p.sf[sf_off(orow, rb, nb, p.sf_layout)] = (uint8_t)sf;
-      if (p.choice) p.choice[orow * nb + rb] = four ? 1 : 0;
+        for (int q = 0; q < 8; ++q) {
+          const uint64_t r = (uint64_t)(rb * 16 + (odd ? q + 8 : q));
+          const U4 u = sr_words4(r * (uint64_t)p.cols + grp, p.sr_k0, p.sr_k1);
+          const uint32_t r0 = __shfl_xor_sync(0xFFFFFFFFu, odd ? u.x : u.z, 1);
+          const uint32_t r1 = __shfl_xor_sync(0xFFFFFFFFu, odd ? u.y : u.w, 1);
+          if (odd) {
+            w0[q] = r0; w1[q] = r1; w0[q + 8] = u.z; w1[q + 8] = u.w;
+          } else {
+            w0[q] = u.x; w1[q] = u.y; w0[q + 8] = r0; w1[q + 8] = r1;
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < CPL; ++k) {
+        float y[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t s = RHT ? (((rht_mask >> i) & 1u) << 31) : 0u;
+          const uint32_t wv = v[k >> 1][i];
+          y[i] = __uint_as_float(((k & 1) ? (wv & 0xFFFF0000u) : (wv << 16)) ^ s);
+        }
+        if (RHT) hadamard16(y);
+        const float ab = absmax16(y);
+        uint64_t yp[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) yp[j] = pack_f2(y[2 * j], y[2 * j + 1]);
+        uint32_t lo, hi, sf;
+        bool four;
+        quant_block_tab<RULE, SR>(yp, ab, tc, s_tab, (k & 1) ? w1 : w0, lo, hi, sf, four);
+        const int64_t orow = c0 + CPL * lane + k;  // output row = source column
+        if (orow < p.cols) {
+          *reinterpret_cast<uint2*>(p.codes + orow * p.ld_codes + rb * 8) = make_uint2(lo, hi);
+          p.sf[sf_off(orow, rb, nbr, p.sf_layout)] = (uint8_t)sf;
+          if (p.choice) p.choice[orow * nbr + rb] = four ? 1 : 0;
+        }
+      }
+    }
+  }
+  if (failed && lane == 0) *p.tensor_scale = __int_as_float(0x7FC00000);  // NaN: the result is not valid
+  // let copies still in flight land before the CTA exits (bounded)
+  for (; consumed < issued; ++consumed) {
+    mbar_wait_for(bar0 + 8u * slot, ph, p.timeout_ns);
+    if (++slot == kColSlots) {
+      slot = 0;
+      ph ^= 1u;
     }
   }
 }
@@ -953,7 +1047,16 @@ static void launch_q(const QuantParams& p, int kind, int grid, cudaStream_t s, b
       launch_params(quant_rows_kernel<RULE, RHT, SR, kRowsPlain>, grid, 256, kRowSmemBytes, pdl, p, s);
       break;
     }
-    case 1: quant_cols_kernel<RULE, RHT, SR><<<grid, 256, 0, s>>>(p); break;
+    case 1: {
+      static bool attr = false;  // benign race: the attribute is idempotent
+      if (!attr) {
+        cudaFuncSetAttribute(quant_cols_kernel<RULE, RHT, SR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kColSmemBytes);
+        attr = true;
+      }
+      quant_cols_kernel<RULE, RHT, SR><<<grid, 256, kColSmemBytes, s>>>(p);
+      break;
+    }
     case 2: quant_2d_kernel<RULE, RHT, SR, false><<<grid, 256, 0, s>>>(p); break;
     default: quant_2d_kernel<RULE, RHT, SR, true><<<grid, 256, 0, s>>>(p); break;
   }
@@ -972,8 +1075,9 @@ static void launch_q_rule(const QuantParams& p, int kind, bool rht, bool sr, int
 
 int quant_grid(int64_t n_warp_tasks, int kind) {
   int64_t g = (n_warp_tasks + 7) / 8;
-  // the row kernel keeps three CTAs per SM resident (its shared-memory ring)
-  int64_t cap = (int64_t)sm_count() * (kind == 0 ? 3 : 8);
+  // the row and column kernels keep at most three CTAs per SM resident (their
+  // shared-memory rings)
+  int64_t cap = (int64_t)sm_count() * (kind <= 1 ? 3 : 8);
   if (g > cap) g = cap;
   return (int)(g < 1 ? 1 : g);
 }
