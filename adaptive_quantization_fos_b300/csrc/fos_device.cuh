@@ -445,14 +445,15 @@ __device__ __forceinline__ void sr_negn16(const uint32_t (&w)[16], float (&negn)
   for (int j = 0; j < 16; ++j) negn[j] = -(float)(w[j] >> 8);
 }
 
-// Stochastic-rounding codes of one candidate (negn from sr_negn16).
-__device__ __forceinline__ float cand_sr16(const float (&y)[16], float inv, const float (&negn)[16], uint32_t& lo,
+// Stochastic-rounding codes of one candidate (yp: the block's values as
+// packed pairs; negn from sr_negn16).
+__device__ __forceinline__ float cand_sr16(const uint64_t (&yp)[8], float inv, const float (&negn)[16], uint32_t& lo,
                                            uint32_t& hi) {
   F2 acc{0.0f, 0.0f};
   uint32_t b[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const F2 q = mul2(F2{y[2 * k], y[2 * k + 1]}, F2{inv, inv});
+    const F2 q = mul2(unpack_f2(yp[k]), F2{inv, inv});
     const F2 aq{fabsf(q.x), fabsf(q.y)};
     const F2 g = sr_mag2(aq, F2{negn[2 * k], negn[2 * k + 1]});
     // the grid value with q's sign converts exactly

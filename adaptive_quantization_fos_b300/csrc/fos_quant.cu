@@ -247,16 +247,8 @@ __device__ __forceinline__ void quant_block_tab(const uint64_t (&yp)[8], float a
                                                 uint32_t& hi, uint32_t& sf, bool& four) {
   const uint32_t pair = e4m3x2(__fmul_rn(ab, tc.k6), __fmul_rn(ab, tc.k4));
   const uint32_t sf6 = pair & 0xFFu, sf4 = pair >> 8;
-  float y[16], negn[16];
-  if (SR) {
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      F2 v = unpack_f2(yp[k]);
-      y[2 * k] = v.x;
-      y[2 * k + 1] = v.y;
-    }
-    sr_negn16(w, negn);
-  }
+  float negn[16];
+  if (SR) sr_negn16(w, negn);
   uint32_t lo6 = 0, hi6 = 0, lo4 = 0, hi4 = 0;
   float E6 = 0.0f, E4 = 0.0f;
 #pragma unroll
@@ -267,7 +259,7 @@ __device__ __forceinline__ void quant_block_tab(const uint64_t (&yp)[8], float a
     uint32_t l, h;
     float S;
     if (SR) {
-      S = cand_sr16(y, t.x, negn, l, h);
+      S = cand_sr16(yp, t.x, negn, l, h);
     } else {
       const uint64_t inv2 = pack_f2(t.x, t.x);
       uint64_t acc = 0ull;
@@ -865,7 +857,7 @@ __global__ void __launch_bounds__(256) quant_2d_kernel(QuantParams p) {
       uint32_t l, h;
       float S;
       if (SR) {
-        S = cand_sr16(y, tb.x, negn, l, h);
+        S = cand_sr16(yp, tb.x, negn, l, h);
       } else {
         const uint64_t inv2 = pack_f2(tb.x, tb.x);
         uint64_t acc = 0ull;
