@@ -281,16 +281,10 @@ __device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uin
   }
 }
 
-// Contiguous global -> shared copy on the async (bulk) path; completion is
-// counted in bytes on the mbarrier.  Addresses 16-byte aligned, size % 16 == 0.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
-
-// The same with an L2 eviction policy (from createpolicy) for the source lines.
+// Contiguous global -> shared copy on the async (bulk) path, with an L2
+// eviction policy (from createpolicy) for the source lines; the calling
+// thread arrives on the mbarrier and completion is counted there in bytes.
+// Addresses 16-byte aligned, size % 16 == 0.
 __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
                                               uint64_t policy) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
