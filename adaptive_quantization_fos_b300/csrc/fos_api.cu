@@ -184,7 +184,11 @@ fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
     if (fos::launch_quant_rows_fused(p, opt->scale_rule, rht, sr, tasks, stream) != cudaSuccess) return FOS_ERR_CUDA;
   } else {
     const int grid = fos::quant_grid(tasks, kind);
-    if (fos::launch_quant(p, opt->scale_rule, kind, rht, sr, grid, stream) != cudaSuccess) return FOS_ERR_CUDA;
+    // after this call's own amax launch, the quantize launch may overlap its
+    // tail; after the caller's work (a supplied amax), it may not: that work
+    // may still be writing x
+    if (fos::launch_quant(p, opt->scale_rule, kind, rht, sr, grid, stream, n_partials > 0) != cudaSuccess)
+      return FOS_ERR_CUDA;
   }
   if (opt->sf_layout == FOS_SF_SWIZZLED_128x4 && (R % 128 != 0 || nb % 4 != 0)) {
     if (fos::launch_sf_pad(sf, sf_bytes_of(R, nb, opt->sf_layout), R, nb, stream) != cudaSuccess)

@@ -68,8 +68,9 @@ int amax_grid(int64_t n_warp_tasks);
 int quant_grid(int64_t n_warp_tasks, int kind);
 cudaError_t launch_amax(const AmaxParams& p, bool hadamard, bool transpose, int grid, cudaStream_t s);
 // kind: 0 rows (1D), 1 cols (1D transposed), 2 2D, 3 2D transposed
-// pdl (row kernel only): the launch may overlap the stream's previous kernel,
-// which must be a row-kernel or amax launch whose outputs it waits for.
+// pdl: the launch may overlap the stream's previous kernel, which must be one
+// of this library's amax or row-quantize launches (the quantize kernel reads
+// x before waiting for it, and the partial maxima after).
 cudaError_t launch_quant(const QuantParams& p, int rule, int kind, bool rht, bool sr, int grid, cudaStream_t s,
                          bool pdl = false);
 // Rows (1D) quantized from partials of an earlier launch while 2 extra warps

@@ -146,6 +146,7 @@ __global__ void __launch_bounds__(256) amax_rows_kernel(AmaxParams p) {
 // RHT down columns: a lane owns 4 adjacent columns x 16 rows.
 __global__ void __launch_bounds__(256) amax_cols_kernel(AmaxParams p) {
   __shared__ float s_red[33];
+  pdl_launch_dependents();  // the quantize launch may start its own reads meanwhile
   const int lane = threadIdx.x & 31;
   const uint32_t rht_mask = rht_sign_mask(p.hk0, p.hk1);
   const int64_t ngroups = (p.cols + 127) >> 7;  // 128 columns per warp task
@@ -180,10 +181,10 @@ __global__ void __launch_bounds__(256) amax_cols_kernel(AmaxParams p) {
 __device__ __forceinline__ TensorConsts quant_prologue(const QuantParams& p, float* s_red) {
   float amax;
   if (p.n_partials == 0) {
-    amax = __ldg(p.amax_src);
+    amax = __ldcg(p.amax_src);
   } else {
     float m = 0.0f;
-    for (int i = threadIdx.x; i < p.n_partials; i += blockDim.x) m = fmaxf(m, __ldg(p.amax_src + i));
+    for (int i = threadIdx.x; i < p.n_partials; i += blockDim.x) m = fmaxf(m, __ldcg(p.amax_src + i));
     amax = block_max(m, s_red);
   }
   TensorConsts tc = tensor_consts(amax);
@@ -648,9 +649,7 @@ __global__ void __launch_bounds__(256, 2) quant_cols_kernel(QuantParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x < kColWarps * kColSlots) mbar_init(smem_addr(&s_bar[threadIdx.x]), 16);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  const TensorConsts tc = quant_prologue(p, s_red);
-  build_scale_table(tc.s_t, s_tab);
-  __syncthreads();
+  __syncthreads();  // the ring barriers are initialised before any copy
   const uint32_t rht_mask = RHT ? rht_sign_mask(p.hk0, p.hk1) : 0u;
   const int64_t nbr = p.rows >> 4;            // block-rows of the source = blocks per output row
   const int64_t ngr = (nbr + 3) >> 2;          // task rows (4 block-rows each)
@@ -682,6 +681,13 @@ __global__ void __launch_bounds__(256, 2) quant_cols_kernel(QuantParams p) {
   };
   int issued = 0, consumed = 0;
   for (int k = 0; k < kColSlots; ++k) issued += issue_next(k) ? 1 : 0;
+  // The input is read-only, so its first copies are in flight already; the
+  // partial maxima come from the amax launch before this one, which may still
+  // be running (programmatic dependent launch).  Everything after waits.
+  pdl_wait();
+  const TensorConsts tc = quant_prologue(p, s_red);
+  build_scale_table(tc.s_t, s_tab);
+  __syncthreads();
 
   int slot = 0;
   uint32_t ph = 0;
@@ -791,6 +797,7 @@ template <int RULE, bool RHT, bool SR, bool TRANS>
 __global__ void __launch_bounds__(256) quant_2d_kernel(QuantParams p) {
   __shared__ float s_red[33];
   __shared__ float2 s_tab[128];
+  pdl_wait();  // the partial maxima come from the amax launch before this one
   const TensorConsts tc = quant_prologue(p, s_red);
   build_scale_table(tc.s_t, s_tab);
   __syncthreads();
@@ -1046,11 +1053,11 @@ static void launch_q(const QuantParams& p, int kind, int grid, cudaStream_t s, b
                              kColSmemBytes);
         attr = true;
       }
-      quant_cols_kernel<RULE, RHT, SR><<<grid, 256, kColSmemBytes, s>>>(p);
+      launch_params(quant_cols_kernel<RULE, RHT, SR>, grid, 256, kColSmemBytes, pdl, p, s);
       break;
     }
-    case 2: quant_2d_kernel<RULE, RHT, SR, false><<<grid, 256, 0, s>>>(p); break;
-    default: quant_2d_kernel<RULE, RHT, SR, true><<<grid, 256, 0, s>>>(p); break;
+    case 2: launch_params(quant_2d_kernel<RULE, RHT, SR, false>, grid, 256, 0, pdl, p, s); break;
+    default: launch_params(quant_2d_kernel<RULE, RHT, SR, true>, grid, 256, 0, pdl, p, s); break;
   }
 }
 
