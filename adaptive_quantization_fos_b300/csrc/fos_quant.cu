@@ -4,9 +4,12 @@
 // arithmetic, not a contraction):
 //   amax_rows    max|y| of X (RHT along rows optional) -> one partial per CTA
 //   amax_cols    max|y| with the RHT running down columns (transposed input)
-//   quant_rows   1D blocks along rows: one lane owns 4 consecutive blocks
-//   quant_cols   1D blocks down columns (transposed output): one thread owns
-//                4 adjacent columns x 16 rows
+//   quant_rows   1D blocks along rows: a warp task is a 2048-value row
+//                segment from the warp's bulk-copy ring; lane l owns blocks
+//                l, l+32, l+64, l+96 (plain, one-launch and chained forms)
+//   quant_cols   1D blocks down columns (transposed output): a warp task is
+//                64 rows x 128 (RNE) or 64 (SR) columns from a bulk-copy
+//                ring; a lane owns 4 or 2 adjacent columns
 //   quant_2d     16x16 tiles: 16 lanes own the 16 source rows of a tile
 //   sf_pad_zero  zero the padding bytes of the swizzled scale layout
 //   dequant      x_hat = g * (sf * s_t)

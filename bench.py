@@ -59,14 +59,19 @@ def peaks() -> dict:
 
 
 def kernel_source_hash() -> str:
-    """Hash of the sources of the quantize kernel (to tell whether a recorded
-    DRAM-traffic figure still belongs to the current kernel)."""
+    """Hash of the code of the quantize kernels, comments and blank lines left
+    out (to tell whether a recorded DRAM-traffic figure still belongs to the
+    current kernels)."""
     import hashlib
+    import re
 
     h = hashlib.sha256()
     for f in ("fos_quant.cu", "fos_device.cuh"):
-        with open(os.path.join(ROOT, "adaptive_quantization_fos_b300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "adaptive_quantization_fos_b300", "csrc", f), encoding="utf-8") as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        code = [re.sub(r"//.*$", "", line).rstrip() for line in src.splitlines()]
+        h.update("\n".join(line for line in code if line).encode())
     return h.hexdigest()[:16]
 
 
