@@ -385,7 +385,8 @@ def e2e_host_buffers(torch, fos, mats_np, dev, steps) -> dict:
     codes, scales and tensor scale back to pinned host memory.  Three streams
     pipeline the matrices: matrix i+1's upload overlaps matrix i's
     quantization and matrix i-1's download (PCIe is full duplex)."""
-    order = sorted(mats_np, key=lambda k: mats_np[k].size)
+    # largest first: the last matrix, whose download ends the step, is then the smallest
+    order = sorted(mats_np, key=lambda k: -mats_np[k].size)
     host_in = {k: torch.from_numpy(mats_np[k].view(np.int16)).view(torch.bfloat16).pin_memory() for k in order}
     dev_in = {k: torch.empty(v.shape, dtype=torch.bfloat16, device=dev) for k, v in host_in.items()}
     qs = {k: fos.Quantizer(*v.shape, device=dev) for k, v in host_in.items()}
