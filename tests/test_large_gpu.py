@@ -1,0 +1,60 @@
+"""The row quantizer at a size where element indices pass 2^34, so the
+stochastic-rounding Philox counter (i / 4) needs its high word, and byte
+offsets pass 2^31: a 262208 x 65536 bf16 gradient (17.2 G values, 34 GB on the
+device), quantized with SR through the one-launch path (amax pass, grid
+barrier, quantize pass).  Rows on both sides of index 2^34 are compared with
+the oracle's quantization of the same rows at the same source indices.
+
+The matrix repeats one seeded 64-row block, so its amax is the block's; the
+stochastic-rounding words still differ everywhere (they depend on the index).
+"""
+import numpy as np
+import pytest
+
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+ROWS, COLS = 262208, 65536  # ROWS * COLS > 2^34
+BLOCK_ROWS = 64
+
+
+@pytest.fixture(scope="module")
+def fos():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    free, _ = torch.cuda.mem_get_info()
+    if free < 60 << 30:
+        pytest.skip("needs about 50 GB of free device memory")
+    import adaptive_quantization_fos_b300 as fos
+
+    return fos
+
+
+def test_sr_rows_beyond_2_pow_34(fos):
+    import torch
+
+    import oracle
+
+    base = workloads.gradients(BLOCK_ROWS, COLS, seed=7001)
+    dev_base = torch.from_numpy(base.view(np.int16)).view(torch.bfloat16).cuda()
+    x = dev_base.repeat(ROWS // BLOCK_ROWS + 1, 1)[:ROWS]
+    assert x.is_contiguous() and x.shape == (ROWS, COLS)
+    q = fos.quantize(x, rounding=fos.FOS_ROUND_STOCHASTIC, sr_seed=77, sf_layout=fos.FOS_SF_ROWMAJOR)
+    torch.cuda.synchronize()
+    amax = float(np.abs(workloads.bf16_to_f32(base)).max())
+    # the tensor amax is the block's (the matrix repeats it)
+    assert np.float32(q.tensor_scale.item()) == np.float32(oracle.quantize(base[:1], amax=amax).tensor_scale)
+    nb = COLS // 16
+    first_beyond = (1 << 34) // COLS  # the first row whose indices reach 2^34
+    for r in (0, 1, first_beyond - 1, first_beyond, ROWS - 1):
+        row = base[r % BLOCK_ROWS][None, :]
+        o = oracle.quantize(row, rounding=oracle.ROUND_SR, sr_seed=77, amax=amax, sf_layout=oracle.SF_ROWMAJOR,
+                            src_row0=r, src_cols=COLS)
+        got_codes = q.codes[r, : COLS // 2].cpu().numpy()
+        got_sf = q.sf[r * nb:(r + 1) * nb].cpu().numpy()
+        assert np.array_equal(got_codes, o.codes[0]), f"row {r}: codes differ"
+        assert np.array_equal(got_sf, o.sf[:nb]), f"row {r}: scales differ"
+    del x, q
+    torch.cuda.empty_cache()
