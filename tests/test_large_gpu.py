@@ -1,6 +1,6 @@
-"""The row quantizer at a size where element indices pass 2^34, so the
-stochastic-rounding Philox counter (i / 4) needs its high word, and byte
-offsets pass 2^31: a 262208 x 65536 bf16 gradient (17.2 G values, 34 GB on the
+"""Maximum sizes.  The row quantizer at a size where element indices pass
+2^34, so the stochastic-rounding Philox counter (i / 4) needs its high word,
+and byte offsets pass 2^31: a 262208 x 65536 bf16 gradient (17.2 G values, 34 GB on the
 device), quantized with SR through the one-launch path (amax pass, grid
 barrier, quantize pass).  Rows on both sides of index 2^34 are compared with
 the oracle's quantization of the same rows at the same source indices.
@@ -57,4 +57,34 @@ def test_sr_rows_beyond_2_pow_34(fos):
         assert np.array_equal(got_codes, o.codes[0]), f"row {r}: codes differ"
         assert np.array_equal(got_sf, o.sf[:nb]), f"row {r}: scales differ"
     del x, q
+    torch.cuda.empty_cache()
+
+
+def test_gemm_output_beyond_2_pow_31(fos):
+    """C = A W^T with 49152 x 49152 outputs (2.4 G elements, 4.8 GB of bf16,
+    offsets past 2^31), K = 256: sampled rows, the last tile row included,
+    within the GEMM bound of the oracle's FP64 product."""
+    import torch
+
+    import oracle
+    from fos_testutil import to_device_bf16
+
+    M = N = 49152
+    K = 256
+    xa = workloads.activations(M, K, seed=7101)
+    xw = workloads.student_t(N, K, seed=7102)
+    a = fos.quantize(to_device_bf16(xa))
+    w = fos.quantize(to_device_bf16(xw))
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fos.gemm(a, w, out=C, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, "a GEMM wait timed out"
+    rows = np.array([0, 1, 24575, M - 129, M - 2, M - 1])
+    ref, bnd = oracle.gemm_rows_matmul(oracle.dequantize(oracle.quantize(xa)), oracle.dequantize(oracle.quantize(xw)),
+                                       rows)
+    c = C[torch.from_numpy(rows).cuda()].float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(c).all()
+    assert np.all(np.abs(c - ref) <= 1e-3 * bnd + 2.0 ** -8 * np.abs(ref))
+    del C
     torch.cuda.empty_cache()
