@@ -534,10 +534,11 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       const int col0 = nb * BN + 128 * h;
       uint16_t* dst = args.c + (int64_t)row * args.ldc + col0;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int jh = 0; jh < 8; ++jh) {
+        const int j = jh >> 1;
         if (row < args.m) {
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
+          for (int g = 2 * (jh & 1); g < 2 * (jh & 1) + 2; ++g) {
             const int col = col0 + 32 * j + 8 * g;
             if (col < args.n) {
               uint4 o;
