@@ -103,6 +103,14 @@ def lib() -> ctypes.CDLL:
         L.orc_e4m3_rne_satfinite_n.argtypes = [vp, i64, vp]
         L.orc_sr_words_n.restype = None
         L.orc_sr_words_n.argtypes = [u64, vp, i64, vp]
+        L.orc_e8m0_decode.restype = ctypes.c_float
+        L.orc_e8m0_decode.argtypes = [ctypes.c_uint8]
+        L.orc_mx_exponent.restype = ctypes.c_int
+        L.orc_mx_exponent.argtypes = [ctypes.c_float, ctypes.c_int]
+        L.orc_quantize_mx.restype = ctypes.c_int
+        L.orc_quantize_mx.argtypes = [vp, i64, i64, i64, ctypes.c_int, vp, i64, vp, vp]
+        L.orc_dequantize_mx.restype = None
+        L.orc_dequantize_mx.argtypes = [vp, vp, i64, i64, i64, vp]
     return _lib
 
 
@@ -352,3 +360,54 @@ def linear_backward_rows(ops: list[QResult], dx_rows, dw_rows, matmul: bool = Fa
     dx = f(dequantize(ops[0]), dequantize(ops[1]), dx_rows)
     dw = f(dequantize(ops[2]), dequantize(ops[3]), dw_rows)
     return dx, dw
+
+
+# ----------------------------------------------------------------- MXFP4
+
+
+def e8m0_decode(b: int) -> float:
+    """R12: E8M0 byte -> 2^(b - 127) (0xFF: NaN)."""
+    return float(lib().orc_e8m0_decode(int(b)))
+
+
+def mx_exponent(a: float, m: int) -> int:
+    """R12: the candidate exponent, X6 = floor(log2 a) - 2 (m = 6, the MX
+    specification's shared exponent) or X6 + 1 (m = 4), clamped to [-127, 127]."""
+    return int(lib().orc_mx_exponent(float(a), int(m)))
+
+
+@dataclass
+class MXResult:
+    codes: np.ndarray   # uint8 [rows, cols/2]
+    scales: np.ndarray  # uint8 [rows, cols/32], E8M0
+    choice: np.ndarray  # uint8 [rows, cols/32], 1 = kept the 4-candidate
+    rows: int
+    cols: int
+
+
+def quantize_mx(x_bf16: np.ndarray, scale_rule: int = SCALE_4OVER6) -> MXResult:
+    """MXFP4 with the 4/6 choice (reading R12 of ``fos_oracle.c``): 32-value
+    blocks along the rows of a bf16 (uint16 bits) matrix, one E8M0 scale each,
+    no tensor scale.  The FP4 glossary page ("FP4 Nasıl Çalışır") defines the
+    format; the candidate rule is this build's reading."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    rows, cols = x.shape
+    assert cols % 32 == 0
+    codes = np.zeros((max(rows, 1), max(cols // 2, 1)), np.uint8)
+    scales = np.zeros((max(rows, 1), max(cols // 32, 1)), np.uint8)
+    choice = np.zeros_like(scales)
+    if rows and cols:
+        rc = lib().orc_quantize_mx(_p(x), rows, cols, cols, scale_rule, _p(codes), codes.shape[1], _p(scales),
+                                   _p(choice))
+        assert rc == 0
+    return MXResult(codes=codes[:rows, : cols // 2], scales=scales[:rows, : cols // 32],
+                    choice=choice[:rows, : cols // 32], rows=rows, cols=cols)
+
+
+def dequantize_mx(q: MXResult) -> np.ndarray:
+    """R12: x_hat = g * 2^X as float32 [rows, cols]."""
+    out = np.empty((q.rows, q.cols), np.float32)
+    codes = np.ascontiguousarray(q.codes)
+    scales = np.ascontiguousarray(q.scales)
+    lib().orc_dequantize_mx(_p(codes), _p(scales), q.rows, q.cols, codes.shape[1], _p(out))
+    return out

@@ -24,6 +24,8 @@
  *          1, 2, 3", SC'11: Philox4x32 with 10 rounds.
  *   [OCP]  OCP 8-bit floating point specification: E4M3 ("fn" variant, bias 7,
  *          no infinities, S.1111.111 is NaN, max 448).
+ *   [MX]   OCP Microscaling (MX) formats specification v1.0: the E8M0 scale
+ *          and the shared exponent floor(log2(amax)) - emax(element).
  *
  * Fixed readings (the pages leave these steps open):
  *   R1  tensor scale s_t = amax / (6*448) in FP32, amax over the (transformed)
@@ -48,6 +50,21 @@
  *       sumsq16 combined by a pairwise tree over the 16 source rows.
  *   R8  transposed input: the output describes X^T; blocks run along the
  *       rows of X; the RHT runs along the blocking dimension.
+ *   R12 MXFP4 ([FP4] "FP4 Nasıl Çalışır": 32 values under one 8-bit
+ *       power-of-two scale; [MX] E8M0: byte b = X + 127 means 2^X, 0xFF is
+ *       NaN; no tensor scale) with the 4/6 choice: the 6-candidate exponent is
+ *       [MX]'s own, X6 = floor(log2 amax) - 2 (E2M1's largest exponent is 2),
+ *       which maps the block maximum into [4, 8) and lets values above 6
+ *       saturate; the 4-candidate is X4 = X6 + 1, which maps the maximum
+ *       below 4 and saturates nothing (a candidate pair "maximum to 6" /
+ *       "maximum to 4" cannot be formed from powers of two otherwise: with X6
+ *       the smallest X whose 6 * 2^X covers amax, the 4-candidate's grid would
+ *       lie inside the 6-candidate's and could never win).  Both are clamped to
+ *       [-127, 127].  Each candidate's codes are the R4 roundings of
+ *       q = y * 2^-X; S_M is the sum of (q - g)^2 in the R2 order over each
+ *       16-value half, the halves then added; keep 4 iff 4 * S_4 < S_6 (the
+ *       4-candidate's error in the 6-candidate's units, exact), ties to 6.
+ *       An all-zero block gets byte 0 (2^-127) and zero codes.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -shared -fPIC.
  * FP32 arithmetic is IEEE binary32 round-to-nearest-even: every float
@@ -478,6 +495,87 @@ double orc_mae_nearest_grid(const float* x, int64_t n, int64_t block) {
     }
   }
   return err / (double)n;
+}
+
+/* ------------------------------------------------------------- MXFP4 */
+
+/* R12: E8M0 byte -> 2^(b - 127); 0xFF is NaN. */
+float orc_e8m0_decode(uint8_t b) {
+  if (b == 0xFF) return NAN;
+  return (float)ldexp(1.0, (int)b - 127);
+}
+
+/* R12: the candidate exponent for amax a > 0 (finite): X6 = floor(log2 a) - 2
+ * for M = 6, X4 = X6 + 1 for M = 4, clamped to [-127, 127]. */
+int orc_mx_exponent(float a, int M) {
+  int e2;
+  frexp((double)a, &e2); /* a = m * 2^e2 with m in [0.5, 1), so floor(log2 a) = e2 - 1 */
+  int X = (e2 - 1) - 2 + (M == 4 ? 1 : 0);
+  if (X < -127) X = -127;
+  if (X > 127) X = 127;
+  return X;
+}
+
+/* One candidate of a 32-value block: codes, and S (R2 order per 16-value
+ * half, then the halves added). */
+static float mx_candidate(const float y[32], int X, uint8_t codes[32]) {
+  const float inv = (float)ldexp(1.0, -X); /* exact: X in [-127, 127] */
+  float r[32];
+  for (int j = 0; j < 32; ++j) {
+    float q = y[j] * inv;
+    codes[j] = orc_e2m1_rne(q);
+    r[j] = q - orc_e2m1_decode(codes[j]);
+  }
+  return orc_sumsq16(r) + orc_sumsq16(r + 16);
+}
+
+/* R12: MXFP4 4/6 quantization of a bf16 matrix [rows, cols] (row stride ld
+ * elements, cols % 32 == 0) along its rows.  codes: rows x ld_codes bytes (two
+ * per byte, even element low); scales: rows x cols/32 E8M0 bytes; choice (may
+ * be NULL): rows x cols/32 bytes, 1 when the block kept the 4-candidate.
+ * scale_rule 0: 4/6, 1: 6 only, 2: 4 only. */
+int orc_quantize_mx(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int scale_rule, uint8_t* codes,
+                    int64_t ld_codes, uint8_t* scales, uint8_t* choice) {
+  if (cols % 32 != 0) return 1;
+  const int64_t nb = cols / 32;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t b = 0; b < nb; ++b) {
+      float y[32], a = 0.0f;
+      for (int j = 0; j < 32; ++j) {
+        y[j] = bf16_to_f32(x[r * ld + 32 * b + j]);
+        if (fabsf(y[j]) > a) a = fabsf(y[j]);
+      }
+      uint8_t c6[32], c4[32];
+      int X6, X4;
+      if (a == 0.0f) {
+        X6 = X4 = -127;
+      } else {
+        X6 = orc_mx_exponent(a, 6);
+        X4 = orc_mx_exponent(a, 4);
+      }
+      float S6 = mx_candidate(y, X6, c6);
+      float S4 = mx_candidate(y, X4, c4);
+      /* X4 is X6 + 1 (or equal at the clamp): bring S4 into the 6-candidate's units */
+      const float S4u = (X4 > X6) ? S4 * 4.0f : S4;
+      int four = (scale_rule == 2) || (scale_rule == 0 && S4u < S6);
+      const uint8_t* c = four ? c4 : c6;
+      for (int j = 0; j < 16; ++j) codes[r * ld_codes + 16 * b + j] = (uint8_t)(c[2 * j] | (c[2 * j + 1] << 4));
+      scales[r * nb + b] = (uint8_t)((four ? X4 : X6) + 127);
+      if (choice) choice[r * nb + b] = (uint8_t)four;
+    }
+  return 0;
+}
+
+/* R12: x_hat = g * 2^X, exact in FP32. */
+void orc_dequantize_mx(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t cols, int64_t ld_codes,
+                       float* out) {
+  const int64_t nb = cols / 32;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c) {
+      uint8_t byte = codes[r * ld_codes + c / 2];
+      uint8_t code = (c & 1) ? (byte >> 4) : (byte & 15);
+      out[r * cols + c] = orc_e2m1_decode(code) * orc_e8m0_decode(scales[r * nb + c / 32]);
+    }
 }
 
 /* ------------------------------------------- array helpers for the tests */

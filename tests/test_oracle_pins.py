@@ -458,3 +458,98 @@ def test_linear_backward_recipe_preserves_weight_gradient(orc):
     one_sided = orc.quantize(xb, transpose=True)  # X^T without the transform
     bad, _ = orc.gemm_rows(orc.dequantize(ops[2]), orc.dequantize(one_sided), np.arange(N))
     assert np.linalg.norm(bad - exact) / np.linalg.norm(exact) > 0.8
+
+
+# ------------------------------------------------------------ MXFP4 (R12)
+
+
+def test_e8m0_all_bytes(orc):
+    for b in range(255):
+        assert orc.e8m0_decode(b) == float(np.ldexp(np.float64(1.0), b - 127))
+    assert math.isnan(orc.e8m0_decode(255))
+
+
+def test_mx_exponent_against_brute_force(orc):
+    """X6 = floor(log2 a) - 2, found here by searching X over the integers for
+    the largest 2^(X+2) <= a in exact (Python float) arithmetic."""
+    rng = np.random.default_rng(41)
+    vals = list((rng.random(400) * 10.0 ** rng.uniform(-40, 38, 400)).astype(np.float32))
+    vals += [np.float32(v) for v in (1.0, 1.5, 2.0, 3.0, 4.0, 6.0, 6.5, 7.99, 8.0, 2.0 ** -126, 2.0 ** -140, 3e38)]
+    for a in vals:
+        a = float(a)
+        if a <= 0:
+            continue
+        X = -200
+        while 2.0 ** (X + 3) <= a:  # the largest X with 2^(X+2) <= a
+            X += 1
+        want6 = max(-127, min(127, X))
+        assert orc.mx_exponent(a, 6) == want6, a
+        assert orc.mx_exponent(a, 4) == max(-127, min(127, X + 1)), a
+
+
+def _mx_blocks_fp64(orc, x_bits):
+    """Per block: FP64 squared errors of both candidates, from the pinned
+    E2M1 rounding and the exponents, summed directly in the input's units."""
+    y = workloads.bf16_to_f32(x_bits).astype(np.float64).reshape(-1, 32)
+    out = []
+    for blk in y:
+        a = np.abs(blk).max()
+        if a == 0:
+            out.append((0.0, 0.0))
+            continue
+        errs = []
+        for m in (6, 4):
+            X = orc.mx_exponent(float(a), m)
+            q = (blk.astype(np.float32) * np.float32(2.0 ** -X)).astype(np.float32)
+            g = np.array([orc.e2m1_decode(c) for c in orc.e2m1_rne(q)], np.float64)
+            errs.append(float(((blk - g * 2.0 ** X) ** 2).sum()))
+        out.append(tuple(errs))
+    return out
+
+
+def test_mx_choice_against_fp64_brute_force(orc):
+    rng = np.random.default_rng(42)
+    x = workloads.bf16_bits(rng.standard_t(3, (16, 128)).astype(np.float32) * 10.0 ** rng.uniform(-3, 3, (16, 1)))
+    q = orc.quantize_mx(x)
+    errs = _mx_blocks_fp64(orc, x)
+    near = 0
+    for (e6, e4), c in zip(errs, q.choice.reshape(-1)):
+        if abs(e4 - e6) <= 1e-6 * max(e6, 1e-300):
+            near += 1
+            continue
+        assert c == (1 if e4 < e6 else 0)
+    assert near < len(errs) // 4
+    assert 0 < q.choice.sum() < q.choice.size  # both candidates occur
+
+
+def test_mx_grid_membership_and_no_worse_than_six(orc):
+    x = workloads.gradients(32, 256, seed=43)
+    q, q6 = orc.quantize_mx(x), orc.quantize_mx(x, scale_rule=1)
+    d = orc.dequantize_mx(q)
+    for r in range(q.rows):
+        for c in range(q.cols):
+            byte = q.codes[r, c // 2]
+            code = (byte >> 4) if c & 1 else (byte & 15)
+            X = int(q.scales[r, c // 32]) - 127
+            assert d[r, c] == np.float32(orc.e2m1_decode(code) * 2.0 ** X)
+    xf = workloads.bf16_to_f32(x).astype(np.float64)
+    e46 = ((orc.dequantize_mx(q) - xf) ** 2).reshape(-1, 32).sum(1)
+    e6 = ((orc.dequantize_mx(q6) - xf) ** 2).reshape(-1, 32).sum(1)
+    assert np.all(e46 <= e6 * (1 + 1e-6))
+    assert e46.sum() < e6.sum()
+
+
+def test_mx_hand_built_blocks(orc):
+    """A maximum of 7.5 saturates to 6 under the MX exponent (error 1.5) but
+    rounds to 8 = 2 * 4 under the coarser one (error 0.5): 4 must win.  A block
+    on the fine grid with maximum 6 is exact under the MX exponent: 6 wins and
+    the block comes back unchanged."""
+    a = np.zeros(32, np.float32)
+    a[0] = 7.5
+    b = np.array([6.0, 0.5, -1.5, 3.0] * 8, np.float32)
+    q = orc.quantize_mx(workloads.bf16_bits(np.stack([a, b])))
+    assert q.choice[0, 0] == 1 and q.scales[0, 0] == 127 + 1  # X4 = floor(log2 7.5) - 2 + 1 = 1
+    assert q.choice[1, 0] == 0 and q.scales[1, 0] == 127 + 0  # X6 = floor(log2 6) - 2 = 0
+    assert np.array_equal(orc.dequantize_mx(q)[1], b)
+    z = orc.quantize_mx(np.zeros((1, 32), np.uint16))
+    assert z.scales[0, 0] == 0 and not z.codes.any() and z.choice[0, 0] == 0
