@@ -115,6 +115,8 @@ def _load() -> ctypes.CDLL:
         "fos_quantize_batch": (i32, [ctypes.POINTER(fos_quant_job), i32, ctypes.POINTER(fos_quant_options), vp, sz,
                                      vp]),
         "fos_linear_backward_workspace_size": (i32, [i64, i64, i64, ctypes.POINTER(sz)]),
+        "fos_quantize_mxfp4": (i32, [vp, i64, i64, i64, i32, vp, i64, vp, vp, vp]),
+        "fos_dequantize_mxfp4": (i32, [vp, vp, i64, i64, i64, vp, i32, i64, vp]),
         "fos_linear_forward_workspace_size": (i32, [i64, i64, ctypes.POINTER(sz)]),
         "fos_linear_forward_operand": (i32, [i64, i64, vp, sz, ctypes.POINTER(fos_nvfp4_tensor)]),
         "fos_linear_forward": (i32, [vp, i64, i64, i64, ctypes.POINTER(fos_quant_options),
@@ -136,7 +138,7 @@ EXPORTED = ("fos_abi_version", "fos_status_string", "fos_sf_bytes", "fos_quantiz
             "fos_e4m3_encode", "fos_philox4x32_10", "fos_selftest_wait_limits", "fos_quantize_batch",
             "fos_quantize_batch_workspace_size", "fos_linear_backward", "fos_linear_backward_workspace_size",
             "fos_linear_backward_operands", "fos_linear_forward", "fos_linear_forward_workspace_size",
-            "fos_linear_forward_operand")
+            "fos_linear_forward_operand", "fos_quantize_mxfp4", "fos_dequantize_mxfp4")
 
 
 def _check(status: int, what: str) -> None:
@@ -527,3 +529,54 @@ class LinearForward:
         return NVFP4Tensor(codes=self.workspace[c0:c0 + d.rows * d.ld_codes].view(d.rows, d.ld_codes),
                            sf=self.workspace[s0:s0 + sfb], tensor_scale=self.workspace[t0:t0 + 4].view(torch.float32),
                            rows=d.rows, cols=d.cols, sf_layout=d.sf_layout)
+
+
+# ------------------------------------------------------------------ MXFP4
+
+
+def fos_quantize_mxfp4(x, rows, cols, ld_x, scale_rule, codes, ld_codes, scales, choice, stream) -> int:
+    return int(_lib.fos_quantize_mxfp4(x or None, rows, cols, ld_x, scale_rule, codes or None, ld_codes,
+                                       scales or None, choice or None, stream))
+
+
+def fos_dequantize_mxfp4(codes, scales, rows, cols, ld_codes, out, out_dtype, ld_out, stream) -> int:
+    return int(_lib.fos_dequantize_mxfp4(codes or None, scales or None, rows, cols, ld_codes, out or None,
+                                         out_dtype, ld_out, stream))
+
+
+@dataclass
+class MXFP4Tensor:
+    """Device buffers of one MXFP4 matrix (rows x cols values, 32-value blocks along cols)."""
+
+    codes: "object"   # uint8 [rows, ld_codes]
+    scales: "object"  # uint8 [rows, cols/32], E8M0
+    rows: int
+    cols: int
+    choice: "object" = None  # uint8 [rows, cols/32] or None
+
+
+def quantize_mxfp4(x, *, scale_rule=FOS_SCALE_4OVER6, with_choice=False, stream=None) -> MXFP4Tensor:
+    """MXFP4 with the 4/6 choice of a bf16 [rows, cols] CUDA tensor (contiguous rows)."""
+    torch = _torch()
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, cols = x.shape
+    ldc = max(16, ((cols // 2 + 15) // 16) * 16)
+    out = MXFP4Tensor(codes=torch.empty((rows, ldc), dtype=torch.uint8, device=x.device),
+                      scales=torch.empty((rows, cols // 32), dtype=torch.uint8, device=x.device), rows=rows,
+                      cols=cols,
+                      choice=torch.empty((rows, cols // 32), dtype=torch.uint8, device=x.device) if with_choice
+                      else None)
+    _check(fos_quantize_mxfp4(x.data_ptr(), rows, cols, x.stride(0), scale_rule, out.codes.data_ptr(), ldc,
+                              out.scales.data_ptr(), out.choice.data_ptr() if with_choice else 0,
+                              _stream_ptr(stream)), "fos_quantize_mxfp4")
+    return out
+
+
+def dequantize_mxfp4(q: MXFP4Tensor, dtype=None, stream=None):
+    torch = _torch()
+    dtype = torch.float32 if dtype is None else dtype
+    out = torch.empty((q.rows, q.cols), dtype=dtype, device=q.codes.device)
+    code = FOS_DTYPE_BF16 if dtype == torch.bfloat16 else FOS_DTYPE_F32
+    _check(fos_dequantize_mxfp4(q.codes.data_ptr(), q.scales.data_ptr(), q.rows, q.cols, q.codes.stride(0),
+                                out.data_ptr(), code, q.cols, _stream_ptr(stream)), "fos_dequantize_mxfp4")
+    return out

@@ -19,7 +19,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJDIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libfos.so")
-SOURCES = ["fos_api.cu", "fos_quant.cu", "fos_gemm.cu", "fos_noalloc.cu", "fos_linear.cu"]
+SOURCES = ["fos_api.cu", "fos_quant.cu", "fos_gemm.cu", "fos_noalloc.cu", "fos_linear.cu", "fos_mx.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--fmad=false", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-I" + os.path.join(ROOT, "include"), "-I" + CSRC]

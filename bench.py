@@ -475,7 +475,18 @@ def secondary(torch, fos, dev, pk) -> dict:
     measure("gradient_sr_1d", grad, rounding=fos.FOS_ROUND_STOCHASTIC, sr_seed=4002)
     measure("gradient_sr_2d", grad, rounding=fos.FOS_ROUND_STOCHASTIC, sr_seed=4002, block_2d=True)
     measure("gradient_rne_2d", grad, block_2d=True)
-    del grad
+    # MXFP4 with the 4/6 choice: no tensor scale, so one pass; 2 + 0.5 + 1/32
+    # algorithmic bytes per value
+    g = _to_dev(torch, grad, dev)
+    fos.quantize_mxfp4(g)
+    t_flush = _time_calls(torch, lambda: flush.fill_(1), 10)
+    t = _time_calls(torch, lambda: (flush.fill_(1), fos.quantize_mxfp4(g)), 10) - t_flush
+    gbs = g.numel() * (2 + 0.5 + 1 / 32) / (t * 1e-3) / 1e9
+    res["gradient_mxfp4"] = {"ms": round(t, 4), "gelem_s": round(g.numel() / (t * 1e-3) / 1e9, 2),
+                             "algorithmic_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4),
+                             "shape": list(g.shape), "options": "MXFP4, 4/6 choice between the MX exponent and one "
+                                                                "more, RNE, single pass"}
+    del g, grad
     res["linear_forward"] = linear_forward(torch, fos, dev, pk)
     res["linear_backward"] = linear_backward(torch, fos, dev, pk)
     return res

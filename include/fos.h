@@ -248,6 +248,42 @@ fos_status fos_dequantize(const fos_nvfp4_tensor* q, void* out, int32_t out_dtyp
 fos_status fos_gemm(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* C, int64_t ldc,
                     int32_t* dev_status, cudaStream_t stream);
 
+/* ---- MXFP4 with the 4/6 choice ---- */
+
+/*
+ * fos_quantize_mxfp4 -- MXFP4 ("FP4" glossary page: 32 values under one 8-bit
+ * power-of-two scale; E8M0 and the shared exponent as in the OCP
+ * Microscaling specification) with the Four Over Six choice between two
+ * power-of-two scales.  Per 32-value block along a row, with amax its largest
+ * magnitude:
+ *   X6 = floor(log2 amax) - 2 (the specification's exponent: maximum into
+ *        [4, 8), values above 6 saturate), X4 = X6 + 1 (maximum below 4),
+ *        both clamped to [-127, 127];
+ *   codes_M = E2M1_rne_satfinite(y * 2^-X_M) (sign kept);
+ *   S_M = sum (q - g)^2 over each 16-value half (even and odd FMA chains,
+ *        then one add), the two halves added;
+ *   keep 4 iff 4 * S_4 < S_6 (ties keep 6); scale byte = X + 127.
+ * An all-zero block gets byte 0 and zero codes.  No tensor scale, no amax
+ * pass: one launch.
+ *   x         device bf16 [rows][ld_x], 16-byte aligned, ld_x % 8 == 0,
+ *             cols % 32 == 0.
+ *   codes     device [rows][ld_codes] bytes, ld_codes >= cols/2, % 4 == 0,
+ *             4-byte aligned (16-byte aligned rows are stored 16 bytes at a time).
+ *   scales    device [rows][cols/32] E8M0 bytes; choice optional, same shape,
+ *             1 where the block kept the 4-candidate.
+ *   scale_rule FOS_SCALE_4OVER6, or FOS_SCALE_6 / FOS_SCALE_4 to force one.
+ */
+fos_status fos_quantize_mxfp4(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int32_t scale_rule,
+                              uint8_t* codes, int64_t ld_codes, uint8_t* scales, uint8_t* choice,
+                              cudaStream_t stream);
+
+/* fos_dequantize_mxfp4 -- x_hat = g * 2^(byte - 127), exact in FP32;
+ * FOS_DTYPE_BF16 output is that value rounded to nearest even.
+ * out: device [rows][ld_out] elements, ld_out >= cols. */
+fos_status fos_dequantize_mxfp4(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t cols,
+                                int64_t ld_codes, void* out, int32_t out_dtype, int64_t ld_out,
+                                cudaStream_t stream);
+
 /* ---- quantized linear backward ---- */
 
 /*

@@ -196,6 +196,25 @@ def test_linear_forward_validation(fos):
     assert (d.rows, d.cols, d.ld_codes) == (M, K, K // 2) and d.sf % 256 == 0 and d.tensor_scale % 256 == 0
 
 
+def test_mxfp4_validation(fos):
+    INVALID = fos.FOS_ERR_INVALID_ARG
+    fake = 1 << 20
+    q = fos.fos_quantize_mxfp4
+    assert q(fake, 4, 48, 48, 0, fake, 32, fake, 0, 0) == INVALID  # cols % 32
+    assert q(fake, 4, 64, 60, 0, fake, 32, fake, 0, 0) == INVALID  # ld_x < cols
+    assert q(fake, 4, 64, 68, 0, fake, 32, fake, 0, 0) == INVALID  # ld_x % 8
+    assert q(fake + 8, 4, 64, 64, 0, fake, 32, fake, 0, 0) == INVALID  # x 16-byte aligned
+    assert q(fake, 4, 64, 64, 3, fake, 32, fake, 0, 0) == INVALID  # scale rule
+    assert q(fake, 4, 64, 64, 0, fake, 30, fake, 0, 0) == INVALID  # ld_codes < cols / 2
+    assert q(fake, 4, 64, 64, 0, fake + 2, 32, fake, 0, 0) == INVALID  # codes 4-byte aligned
+    assert q(fake, 4, 64, 64, 0, fake, 32, 0, 0, 0) == INVALID  # scales
+    assert q(fake, 0, 64, 64, 0, 0, 32, 0, 0, 0) == fos.FOS_OK  # empty: nothing to launch
+    d = fos.fos_dequantize_mxfp4
+    assert d(fake, fake, 4, 48, 32, fake, 0, 48, 0) == INVALID
+    assert d(fake, fake, 4, 64, 32, fake, 7, 64, 0) == INVALID
+    assert d(fake, fake, 4, 64, 32, fake + 2, 0, 64, 0) == INVALID
+
+
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     import importlib.util
 

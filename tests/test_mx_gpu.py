@@ -1,0 +1,73 @@
+"""Parity of the MXFP4 4/6 quantizer (fos_quantize_mxfp4) with the oracle
+(reading R12): codes, E8M0 scale bytes and choices bit for bit, and the
+dequantized values exactly; ragged and edge-case inputs, all three scale
+rules, and the full-size gradient and weight shapes."""
+import numpy as np
+import pytest
+
+import workloads
+from fos_testutil import mixed_bits, to_device_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fos():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import adaptive_quantization_fos_b300 as fos
+
+    return fos
+
+
+def check(fos, bits, ld=None, scale_rule=0):
+    import torch
+
+    import oracle
+
+    x = to_device_bf16(bits, ld)
+    q = fos.quantize_mxfp4(x, scale_rule=scale_rule, with_choice=True)
+    d = fos.dequantize_mxfp4(q)
+    db = fos.dequantize_mxfp4(q, dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    o = oracle.quantize_mx(bits, scale_rule=scale_rule)
+    rows, cols = bits.shape
+    assert np.array_equal(q.codes[:, : cols // 2].cpu().numpy(), o.codes), "codes differ"
+    assert np.array_equal(q.scales.cpu().numpy(), o.scales), "scale bytes differ"
+    assert np.array_equal(q.choice.cpu().numpy(), o.choice), "choices differ"
+    want = oracle.dequantize_mx(o)
+    assert np.array_equal(d.cpu().numpy(), want), "dequantized values differ"
+    assert np.array_equal(db.float().cpu().numpy(), workloads.bf16_to_f32(workloads.bf16_bits(want)))
+    return o
+
+
+@pytest.mark.parametrize("shape", [(1, 32), (3, 96), (300, 1056), (129, 512), (64, 4096)])
+@pytest.mark.parametrize("rule", [0, 1, 2])
+def test_mx_matches_oracle(fos, shape, rule):
+    check(fos, mixed_bits(*shape, seed=shape[0] * 7 + shape[1]), scale_rule=rule)
+
+
+def test_mx_padded_rows_and_edges(fos):
+    check(fos, mixed_bits(40, 160, seed=3), ld=168)
+    zeros = np.zeros((2, 64), np.uint16)
+    zeros[1, 5] = 0x8000  # -0
+    o = check(fos, zeros)
+    assert not o.scales.any()
+    big = workloads.bf16_bits(np.full((2, 32), 3.0e38, np.float32))
+    tiny = workloads.bf16_bits(np.full((2, 32), 1.0e-38, np.float32) * np.arange(1, 33, dtype=np.float32))
+    sub = np.full((1, 32), 0x0003, np.uint16)  # bf16 subnormals
+    check(fos, np.concatenate([big, tiny]))
+    check(fos, sub)
+    seven = workloads.bf16_bits(np.array([[7.5] + [0.0] * 31, [6.0, 0.5, -1.5, 3.0] * 8], np.float32))
+    o = check(fos, seven)
+    assert o.choice[0, 0] == 1 and o.choice[1, 0] == 0
+
+
+@pytest.mark.parametrize("name,make", [
+    ("gradient 8192x12288", lambda: workloads.gradients(8192, 12288, seed=4001)),
+    ("gate_proj 12288x4096", lambda: workloads.student_t(12288, 4096, seed=2004)),
+])
+def test_mx_full_size(fos, name, make):
+    o = check(fos, make())
+    assert 0 < o.choice.mean() < 0.5, name
