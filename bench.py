@@ -644,6 +644,12 @@ def run_case(args) -> None:
                           transpose=True, hadamard=True, hadamard_seed=12)
         for _ in range(3):
             q(x)
+    elif args.case == "quant_mxfp4":
+        # 8192 x 12288 gradient (201 MB > L2), MXFP4 with the 4/6 choice: one
+        # single-pass kernel
+        x = _to_dev(torch, workloads.gradients(8192, 12288, seed=4001), dev)
+        for _ in range(3):
+            fos.quantize_mxfp4(x)
     elif args.case == "gemm":
         A = _to_dev(torch, workloads.activations(8192, 4096, seed=5001), dev)
         W = _to_dev(torch, workloads.student_t(12288, 4096, seed=5002), dev)
