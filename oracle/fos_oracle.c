@@ -29,8 +29,10 @@
  *
  * Fixed readings (the pages leave these steps open):
  *   R1  tensor scale s_t = amax / (6*448) in FP32, amax over the (transformed)
- *       tensor; the per-tensor reciprocal k_M = 1/(M*s_t) is taken once and the
- *       block scale candidate is E4M3_rne_satfinite(a_b * k_M).
+ *       tensor.  A block's candidate scale maps its maximum a_b to M (6 or 4):
+ *       t_M = M * s_t and sf_M = E4M3_rne_satfinite(a_b / t_M), the product
+ *       and the quotient each one FP32 rounding ([FOS] first section: the
+ *       block maximum is scaled to 4 or to 6); sf_M = 0 when t_M = 0.
  *   R2  a candidate's squared error is evaluated in the scaled domain:
  *       E_M = (sum_j (q_j - g_j)^2) * eff_M^2, q_j = y_j * (1/eff_M), with the
  *       sum in the fixed order of sumsq16() / the 2D tree; a candidate whose
@@ -295,10 +297,11 @@ typedef struct {
   float err;
 } cand_t;
 
-static cand_t eval_candidate(const float* y, const uint64_t* src, int nrows, float ab, float kM,
+static cand_t eval_candidate(const float* y, const uint64_t* src, int nrows, float ab, float tM,
                              float s_t, const orc_options* o, uint8_t* codes_out) {
   cand_t c;
-  float raw = ab * kM;
+  /* R1: the block maximum divided by M * s_t, one IEEE division */
+  float raw = (tM > 0.0f) ? ab / tM : 0.0f;
   c.sf = orc_e4m3_rne_satfinite(raw);
   float rowsum[16];
   if (c.sf == 0) {
@@ -371,8 +374,6 @@ int orc_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, cons
       if (fabsf(y[i]) > amax) amax = fabsf(y[i]);
   float s_t = amax / 2688.0f;
   float t6 = 6.0f * s_t, t4 = 4.0f * s_t;
-  float k6 = (t6 > 0.0f) ? 1.0f / t6 : 0.0f;
-  float k4 = (t4 > 0.0f) ? 1.0f / t4 : 0.0f;
   *tensor_scale = s_t;
 
   memset(sf, 0, (size_t)orc_sf_bytes(R, nb, o->sf_layout));
@@ -409,8 +410,8 @@ int orc_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, cons
       float ab = 0.0f;
       for (int i = 0; i < 16 * nrows; ++i)
         if (fabsf(ty[i]) > ab) ab = fabsf(ty[i]);
-      cand_t e6 = eval_candidate(ty, tsrc, nrows, ab, k6, s_t, o, c6);
-      cand_t e4 = eval_candidate(ty, tsrc, nrows, ab, k4, s_t, o, c4);
+      cand_t e6 = eval_candidate(ty, tsrc, nrows, ab, t6, s_t, o, c6);
+      cand_t e4 = eval_candidate(ty, tsrc, nrows, ab, t4, s_t, o, c4);
       int four;
       if (o->scale_rule == 1)
         four = 0;
