@@ -374,18 +374,53 @@ __device__ __forceinline__ void rht16(float (&v)[16], uint32_t mask) {
 }
 
 // ------------------------------------------------------------ per tensor
+// A block's candidate scale maps its maximum a_b to M = 6 or 4:
+// sf_M = E4M3(a_b / t_M) with t_M = M * s_t, the product and the quotient each
+// rounded once in FP32.  The quotient is formed without a division, by one
+// correction step after a reciprocal multiply (Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): with k = RN(1/t) and q = RN(a * k) within an ulp of a/t,
+// the residual r = a - q*t is exact in one FMA and RN(q + r*k) is RN(a/t),
+// provided nothing underflows.  To keep every quantity normal, a_b and t_M are
+// first scaled by P = 2^sigma with s_t * P in [1, 2) (sigma clamped to
+// [-126, 126]); the scaling is exact and leaves the quotient unchanged.  a_b * P
+// is clamped to 4096 * t_4 * P (a quotient of 1024 or more saturates to 448
+// either way), so a caller-supplied amax below a block's maximum cannot
+// overflow the steps.
 struct TensorConsts {
-  float s_t, k6, k4;
+  float s_t;
+  float p;          // 2^sigma
+  float nt6, nt4;   // -t_M * P
+  float k6, k4;     // RN(1 / (t_M * P)), 0 when t_M is 0
+  float clamp;      // 4096 * t_4 * P
 };
 
-// s_t = amax / 2688; k_M = 1 / (M * s_t) (0 when M * s_t is 0).
+// s_t = amax / 2688 and the constants of the candidate-scale quotients.
 __device__ __forceinline__ TensorConsts tensor_consts(float amax) {
   TensorConsts t;
   t.s_t = __fdiv_rn(amax, 2688.0f);
-  float t6 = __fmul_rn(6.0f, t.s_t), t4 = __fmul_rn(4.0f, t.s_t);
-  t.k6 = t6 > 0.0f ? __frcp_rn(t6) : 0.0f;
-  t.k4 = t4 > 0.0f ? __frcp_rn(t4) : 0.0f;
+  const int e = (int)((__float_as_uint(t.s_t) >> 23) & 0xFFu) - 127;  // exponent of a normal s_t
+  int sigma = t.s_t > 0.0f ? -e : 0;
+  sigma = sigma > 126 ? 126 : (sigma < -126 ? -126 : sigma);  // a subnormal s_t gives 126
+  t.p = __uint_as_float((uint32_t)(sigma + 127) << 23);
+  const float T6 = __fmul_rn(__fmul_rn(6.0f, t.s_t), t.p), T4 = __fmul_rn(__fmul_rn(4.0f, t.s_t), t.p);
+  t.nt6 = -T6;
+  t.nt4 = -T4;
+  t.k6 = T6 > 0.0f ? __frcp_rn(T6) : 0.0f;
+  t.k4 = T4 > 0.0f ? __frcp_rn(T4) : 0.0f;
+  t.clamp = __fmul_rn(4096.0f, T4);
   return t;
+}
+
+// The two candidate scale bytes of a block with maximum ab: low byte
+// E4M3(ab / t_6), high byte E4M3(ab / t_4), both quotients correctly rounded.
+__device__ __forceinline__ uint32_t candidate_scales(float ab, const TensorConsts& tc) {
+  const float a = fminf(__fmul_rn(ab, tc.p), tc.clamp);
+  const F2 aa{a, a}, k{tc.k6, tc.k4};
+  const F2 q = mul2(aa, k);
+  const F2 r = fma2(q, F2{tc.nt6, tc.nt4}, aa);  // a - q * t, exact
+  const F2 raw = fma2(r, k, q);
+  return e4m3x2(raw.x, raw.y);
 }
 
 // Fixed-order sum of 16 squares: FMA chains over even and odd positions, then one add.

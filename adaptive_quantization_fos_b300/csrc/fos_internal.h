@@ -12,10 +12,15 @@ namespace fos {
 // Upper bound on the number of CTAs of the amax pass (= partial maxima the
 // quantize kernels reduce in their prologue).
 constexpr int kMaxAmaxPartials = 2048;
-// Workspace: the partial maxima, then (at kBarrierOffset) the word of the
-// grid barrier of the one-launch row quantizer.
+// Workspace: the partial maxima, then (at kBarrierOffset) the words of the
+// one-launch row quantizer: the grid barrier's arrival counter, a flag that a
+// CTA which gave up on a wait raises, and the counter of CTAs that finished
+// (the last one writes the tensor scale, or NaN if the flag is up).  The host
+// clears the kBarrierWords words before each launch.
 constexpr size_t kBarrierOffset = kMaxAmaxPartials * sizeof(float);
+constexpr int kBarrierWords = 3;
 constexpr size_t kQuantWorkspaceBytes = kBarrierOffset + 256;
+static_assert(kBarrierOffset + kBarrierWords * sizeof(unsigned int) <= kQuantWorkspaceBytes, "workspace layout");
 
 struct AmaxParams {
   const uint16_t* x;

@@ -11,7 +11,7 @@
 //
 // Limits and behaviour a caller must know:
 //   - The array holds kNoAllocScratchFloats floats (8448 bytes: the partial
-//     maxima and the word of the one-launch quantizer's grid barrier).  Every
+//     maxima and the words of the one-launch quantizer's grid barrier).  Every
 //     GPU that loads the library holds it until the process exits.
 //   - The first call on each device looks up the array's device address (with
 //     that device current) and caches it.  Make that first call before any
@@ -21,8 +21,9 @@
 //     may produce wrong scales.
 //   - Nothing in the array needs clearing between calls: each call's amax pass
 //     writes every slot its quantize pass later reads, and each call clears
-//     the barrier word (a 4-byte cudaMemsetAsync on the caller's stream, which
-//     allocates nothing) before its launch.
+//     the one-launch quantizer's three barrier words (a 12-byte
+//     cudaMemsetAsync on the caller's stream, which allocates nothing) before
+//     its launch.
 //   - A call whose scratch need exceeds the array is rejected with
 //     FOS_ERR_INVALID_ARG.  The amax pass never runs more than
 //     kMaxAmaxPartials CTAs, so every call fos_quantize accepts fits.

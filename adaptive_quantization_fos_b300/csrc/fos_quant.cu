@@ -17,6 +17,7 @@
 // the amax pass needs no atomics, no memset and no extra finalize launch.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cfloat>
 #include <cstdint>
 
@@ -249,7 +250,7 @@ template <int RULE, bool SR>
 __device__ __forceinline__ void quant_block_tab(const uint64_t (&yp)[8], float ab, const TensorConsts& tc,
                                                 const float2* tab, const uint32_t (&w)[16], uint32_t& lo,
                                                 uint32_t& hi, uint32_t& sf, bool& four) {
-  const uint32_t pair = e4m3x2(__fmul_rn(ab, tc.k6), __fmul_rn(ab, tc.k4));
+  const uint32_t pair = candidate_scales(ab, tc);
   const uint32_t sf6 = pair & 0xFFu, sf4 = pair >> 8;
   float negn[16];
   if (SR) sr_negn16(w, negn);
@@ -415,6 +416,22 @@ __device__ __forceinline__ void next_job_amax(const QuantParams& p, uint8_t* rin
 // issue-bound quantization), leaving one partial per CTA for that job's launch.
 constexpr int kRowsPlain = 0, kRowsFused = 1, kRowsChained = 2;
 
+// End of a one-launch (kRowsFused) CTA, by one thread: a CTA that gave up on a
+// wait raises the flag word; the last CTA to finish writes the tensor scale,
+// or NaN when any CTA gave up.  Raising the flag comes before the finish count
+// (fenced), so the last CTA sees every flag however late a wait ran out.
+__device__ __forceinline__ void fused_finish(const QuantParams& p, bool ok, float s_t) {
+  unsigned int* const give_up = p.ws_barrier + 1;
+  unsigned int* const finished = p.ws_barrier + 2;
+  if (!ok) atomicOr(give_up, 1u);
+  __threadfence();
+  if (atomicAdd(finished, 1u) == gridDim.x - 1) {
+    __threadfence();
+    const bool any_gave_up = atomicOr(give_up, 0u) != 0u;
+    *p.tensor_scale = any_gave_up ? __int_as_float(0x7FC00000) : s_t;  // NaN: the result is not valid
+  }
+}
+
 template <int RULE, bool RHT, bool SR, int MODE>
 __global__ void __launch_bounds__(MODE == kRowsChained ? 320 : 256, MODE == kRowsChained ? 2 : (SR ? 2 : 3))
     quant_rows_kernel(QuantParams p) {
@@ -481,14 +498,15 @@ __global__ void __launch_bounds__(MODE == kRowsChained ? 320 : 256, MODE == kRow
     if (threadIdx.x == 0) {
       p.ws_partials[blockIdx.x] = m;
       s_ok = grid_barrier(p.ws_barrier, gridDim.x + p.barrier_extra, p.timeout_ns) ? 1 : 0;
-      if (!s_ok) *p.tensor_scale = __int_as_float(0x7FC00000);  // NaN: the result is not valid
     }
     __syncthreads();
-    if (!s_ok) return;
+    if (!s_ok) {
+      if (threadIdx.x == 0) fused_finish(p, false, 0.0f);
+      return;
+    }
     float mm = 0.0f;
     for (int i = threadIdx.x; i < (int)gridDim.x; i += blockDim.x) mm = fmaxf(mm, __ldcg(p.ws_partials + i));
-    tc = tensor_consts(block_max(mm, s_red));
-    if (blockIdx.x == 0 && threadIdx.x == 0) *p.tensor_scale = tc.s_t;
+    tc = tensor_consts(block_max(mm, s_red));  // the same in every CTA; the last to finish stores s_t
   }
   if (MODE == kRowsChained && warp >= kRowWarps) {
     // the next job's block maxima need nothing from earlier launches
@@ -607,7 +625,12 @@ __global__ void __launch_bounds__(MODE == kRowsChained ? 320 : 256, MODE == kRow
     }
   }
   if (lane == 0) {
-    if (failed) *p.tensor_scale = __int_as_float(0x7FC00000);  // NaN: the result is not valid
+    if (failed) {
+      if (FUSED)
+        s_ok = 0;  // reported by fused_finish below
+      else
+        *p.tensor_scale = __int_as_float(0x7FC00000);  // NaN: the result is not valid
+    }
     // let copies still in flight land before the CTA exits (bounded)
     for (; consumed < issued; ++consumed) {
       mbar_wait_for(bar0 + 8u * slot, ph, p.timeout_ns);
@@ -616,6 +639,10 @@ __global__ void __launch_bounds__(MODE == kRowsChained ? 320 : 256, MODE == kRow
         ph ^= 1u;
       }
     }
+  }
+  if constexpr (FUSED) {
+    __syncthreads();
+    if (threadIdx.x == 0) fused_finish(p, s_ok != 0, tc.s_t);
   }
 }
 
@@ -851,7 +878,7 @@ __global__ void __launch_bounds__(256) quant_2d_kernel(QuantParams p) {
     sr_words16<SR>((uint64_t)r * (uint64_t)p.cols + (uint64_t)c0, p, w);
     float negn[16];
     if (SR) sr_negn16(w, negn);
-    const uint32_t pair = e4m3x2(__fmul_rn(ab, tc.k6), __fmul_rn(ab, tc.k4));
+    const uint32_t pair = candidate_scales(ab, tc);
     const uint32_t sf6 = pair & 0xFFu, sf4 = pair >> 8;
     uint64_t yp[8];
 #pragma unroll
@@ -1036,43 +1063,50 @@ static cudaError_t launch_params(void (*fn)(QuantParams), int grid, int block, i
   return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
+// The dynamic shared-memory opt-in is a property of a kernel on one device:
+// it is set once per (kernel, device), and its error is returned.
+constexpr int kMaxDevices = 64;
+
+static int current_device() {
+  int d = -1;
+  return cudaGetDevice(&d) == cudaSuccess ? d : -1;
+}
+
+template <typename Fn>
+static cudaError_t smem_opt_in(Fn fn, int bytes, std::atomic<int>* done) {
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  if (dev < kMaxDevices && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev < kMaxDevices) done[dev].store(1, std::memory_order_release);
+  return e;
+}
+
 template <int RULE, bool RHT, bool SR>
-static void launch_q(const QuantParams& p, int kind, int grid, cudaStream_t s, bool pdl) {
+static cudaError_t launch_q(const QuantParams& p, int kind, int grid, cudaStream_t s, bool pdl) {
   switch (kind) {
     case 0: {
-      static bool attr = false;  // benign race: the attribute is idempotent
-      if (!attr) {
-        cudaFuncSetAttribute(quant_rows_kernel<RULE, RHT, SR, kRowsPlain>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kRowSmemBytes);
-        attr = true;
-      }
-      launch_params(quant_rows_kernel<RULE, RHT, SR, kRowsPlain>, grid, 256, kRowSmemBytes, pdl, p, s);
-      break;
+      auto fn = quant_rows_kernel<RULE, RHT, SR, kRowsPlain>;
+      static std::atomic<int> done[kMaxDevices];
+      const cudaError_t e = smem_opt_in(fn, kRowSmemBytes, done);
+      return e != cudaSuccess ? e : launch_params(fn, grid, 256, kRowSmemBytes, pdl, p, s);
     }
     case 1: {
-      static bool attr = false;  // benign race: the attribute is idempotent
-      if (!attr) {
-        cudaFuncSetAttribute(quant_cols_kernel<RULE, RHT, SR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kColSmemBytes);
-        attr = true;
-      }
-      launch_params(quant_cols_kernel<RULE, RHT, SR>, grid, 256, kColSmemBytes, pdl, p, s);
-      break;
+      auto fn = quant_cols_kernel<RULE, RHT, SR>;
+      static std::atomic<int> done[kMaxDevices];
+      const cudaError_t e = smem_opt_in(fn, kColSmemBytes, done);
+      return e != cudaSuccess ? e : launch_params(fn, grid, 256, kColSmemBytes, pdl, p, s);
     }
-    case 2: launch_params(quant_2d_kernel<RULE, RHT, SR, false>, grid, 256, 0, pdl, p, s); break;
-    default: launch_params(quant_2d_kernel<RULE, RHT, SR, true>, grid, 256, 0, pdl, p, s); break;
+    case 2: return launch_params(quant_2d_kernel<RULE, RHT, SR, false>, grid, 256, 0, pdl, p, s);
+    default: return launch_params(quant_2d_kernel<RULE, RHT, SR, true>, grid, 256, 0, pdl, p, s);
   }
 }
 
 template <int RULE>
-static void launch_q_rule(const QuantParams& p, int kind, bool rht, bool sr, int grid, cudaStream_t s, bool pdl) {
-  if (rht) {
-    if (sr) launch_q<RULE, true, true>(p, kind, grid, s, pdl);
-    else launch_q<RULE, true, false>(p, kind, grid, s, pdl);
-  } else {
-    if (sr) launch_q<RULE, false, true>(p, kind, grid, s, pdl);
-    else launch_q<RULE, false, false>(p, kind, grid, s, pdl);
-  }
+static cudaError_t launch_q_rule(const QuantParams& p, int kind, bool rht, bool sr, int grid, cudaStream_t s,
+                                 bool pdl) {
+  if (rht) return sr ? launch_q<RULE, true, true>(p, kind, grid, s, pdl) : launch_q<RULE, true, false>(p, kind, grid, s, pdl);
+  return sr ? launch_q<RULE, false, true>(p, kind, grid, s, pdl) : launch_q<RULE, false, false>(p, kind, grid, s, pdl);
 }
 
 int quant_grid(int64_t n_warp_tasks, int kind) {
@@ -1087,15 +1121,19 @@ int quant_grid(int64_t n_warp_tasks, int kind) {
 template <int RULE, bool RHT, bool SR>
 static cudaError_t launch_rows_fused(const QuantParams& p, int64_t n_tasks, cudaStream_t s) {
   auto fn = quant_rows_kernel<RULE, RHT, SR, kRowsFused>;
-  static int per_sm = 0;  // benign race: every thread computes the same value
+  // resident CTAs per SM, found once per device (the grid barrier needs all
+  // CTAs resident at once)
+  static std::atomic<int> per_sm_of[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  int per_sm = dev < kMaxDevices ? per_sm_of[dev].load(std::memory_order_acquire) : 0;
   if (per_sm == 0) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowSmemBytes);
     if (e != cudaSuccess) return e;
-    int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, 256, kRowSmemBytes);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, 256, kRowSmemBytes);
     if (e != cudaSuccess) return e;
-    if (n < 1) return cudaErrorInvalidConfiguration;
-    per_sm = n;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    if (dev < kMaxDevices) per_sm_of[dev].store(per_sm, std::memory_order_release);
   }
   int64_t grid = (int64_t)per_sm * sm_count();
   const int64_t want = (n_tasks + kRowWarps - 1) / kRowWarps;
@@ -1104,7 +1142,8 @@ static cudaError_t launch_rows_fused(const QuantParams& p, int64_t n_tasks, cuda
   if (grid < 1) grid = 1;
   QuantParams q = p;
   void* args[] = {&q};
-  cudaError_t e = cudaMemsetAsync(p.ws_barrier, 0, sizeof(unsigned int), s);
+  // the barrier's arrival counter, the give-up flag and the exit counter
+  cudaError_t e = cudaMemsetAsync(p.ws_barrier, 0, kBarrierWords * sizeof(unsigned int), s);
   if (e != cudaSuccess) return e;
   return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fn), dim3((unsigned)grid), dim3(256), args,
                                      kRowSmemBytes, s);
@@ -1120,12 +1159,9 @@ static cudaError_t launch_rows_fused_rule(const QuantParams& p, bool rht, bool s
 template <int RULE, bool RHT, bool SR>
 static cudaError_t launch_rows_chained(const QuantParams& p, int grid, cudaStream_t s) {
   auto fn = quant_rows_kernel<RULE, RHT, SR, kRowsChained>;
-  static bool attr = false;  // benign race: the attribute is idempotent
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kChainSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<int> done[kMaxDevices];
+  const cudaError_t e = smem_opt_in(fn, kChainSmemBytes, done);
+  if (e != cudaSuccess) return e;
   // always the successor of a launch of the same batch: overlap its tail
   return launch_params(fn, grid, 32 * (kRowWarps + kAmaxWarps), kChainSmemBytes, true, p, s);
 }
@@ -1159,11 +1195,10 @@ cudaError_t launch_quant_rows_fused(const QuantParams& p, int rule, bool rht, bo
 cudaError_t launch_quant(const QuantParams& p, int rule, int kind, bool rht, bool sr, int grid, cudaStream_t s,
                          bool pdl) {
   switch (rule) {
-    case FOS_SCALE_6: launch_q_rule<FOS_SCALE_6>(p, kind, rht, sr, grid, s, pdl); break;
-    case FOS_SCALE_4: launch_q_rule<FOS_SCALE_4>(p, kind, rht, sr, grid, s, pdl); break;
-    default: launch_q_rule<FOS_SCALE_4OVER6>(p, kind, rht, sr, grid, s, pdl); break;
+    case FOS_SCALE_6: return launch_q_rule<FOS_SCALE_6>(p, kind, rht, sr, grid, s, pdl);
+    case FOS_SCALE_4: return launch_q_rule<FOS_SCALE_4>(p, kind, rht, sr, grid, s, pdl);
+    default: return launch_q_rule<FOS_SCALE_4OVER6>(p, kind, rht, sr, grid, s, pdl);
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_sf_pad(uint8_t* sf, int64_t bytes, int64_t R, int64_t nb, cudaStream_t s) {

@@ -69,10 +69,14 @@ OPTS = [dict(), dict(hadamard=True, hadamard_seed=21), dict(rounding=1, sr_seed=
 def test_forward_matches_oracle(fos, M, N, K, opts):
     import oracle
 
-    if opts.get("block_2d") and M % 16:
-        pytest.skip("2D tiles need whole 16-row groups")
     x = mixed_bits(M, K, seed=M + K)
     w = workloads.student_t(N, K, seed=N + 3)
+    if opts.get("block_2d") and M % 16:
+        # 16 x 16 tiles need whole 16-row groups: the call is refused, nothing runs
+        with pytest.raises(fos.FosError) as e:
+            run(fos, x, w, **opts)
+        assert e.value.status == fos.FOS_ERR_INVALID_ARG
+        return
     layer, y, qw = run(fos, x, w, **opts)
     qx = oracle.quantize(x, **opts)
     want = QOut(codes=np.ascontiguousarray(qx.codes[:, : K // 2]), sf=qx.sf, s_t=np.float32(qx.tensor_scale),
