@@ -111,6 +111,7 @@ def _load() -> ctypes.CDLL:
         "fos_e4m3_encode": (i32, [vp, i64, vp, vp]),
         "fos_philox4x32_10": (i32, [vp, i64, u64, vp, vp]),
         "fos_selftest_wait_limits": (i32, [vp, sz, u64, vp, vp]),
+        "fos_selftest_mma_rate": (i32, [i32, i64, i32, vp, vp]),
         "fos_quantize_batch_workspace_size": (i32, [i32, ctypes.POINTER(sz)]),
         "fos_quantize_batch": (i32, [ctypes.POINTER(fos_quant_job), i32, ctypes.POINTER(fos_quant_options), vp, sz,
                                      vp]),
@@ -138,7 +139,7 @@ EXPORTED = ("fos_abi_version", "fos_status_string", "fos_sf_bytes", "fos_quantiz
             "fos_e4m3_encode", "fos_philox4x32_10", "fos_selftest_wait_limits", "fos_quantize_batch",
             "fos_quantize_batch_workspace_size", "fos_linear_backward", "fos_linear_backward_workspace_size",
             "fos_linear_backward_operands", "fos_linear_forward", "fos_linear_forward_workspace_size",
-            "fos_linear_forward_operand", "fos_quantize_mxfp4", "fos_dequantize_mxfp4")
+            "fos_linear_forward_operand", "fos_quantize_mxfp4", "fos_dequantize_mxfp4", "fos_selftest_mma_rate")
 
 
 def _check(status: int, what: str) -> None:
@@ -196,6 +197,10 @@ def fos_gemm(A: fos_nvfp4_tensor, B: fos_nvfp4_tensor, C, ldc, dev_status, strea
 
 def fos_selftest_wait_limits(scratch, scratch_bytes, timeout_ns, result, stream) -> int:
     return int(_lib.fos_selftest_wait_limits(scratch, scratch_bytes, timeout_ns, result, stream))
+
+
+def fos_selftest_mma_rate(n_cols, iters, grid, dev_status, stream) -> int:
+    return int(_lib.fos_selftest_mma_rate(n_cols, iters, grid, dev_status or None, stream))
 
 
 def fos_e2m1_encode(x, n, codes, stream) -> int:

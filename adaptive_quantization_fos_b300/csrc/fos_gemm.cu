@@ -570,6 +570,76 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   }
 }
 
+// ------------------------------------------------- tensor-pipe rate probe
+// The MMA instruction of the GEMM (kind::mxf4nvf4, E4M3 scales per 16 values,
+// M = 128, N = BN, K = 64) issued `iters` x 4 times back to back by one
+// thread per CTA on operands that stay in shared memory (zeros) with scale
+// columns of E4M3 1.0: no loads, no scale staging, no stores.  It measures
+// the instruction's throughput on this part, the ceiling the GEMM's operand
+// pipeline is compared with.  Nothing asynchronous but the MMAs is ever in
+// flight; their completion is awaited (bounded) before the tensor memory is
+// freed.  The dynamic shared memory (over half an SM's) keeps one CTA per SM.
+constexpr int kRateSmemBytes = 120 * 1024;
+
+template <int BN>
+__global__ void __launch_bounds__(128, 1) mma_rate_kernel(int64_t iters, uint64_t timeout_ns, int32_t* status) {
+  constexpr int kA = kBM * kBKBytes, kB = BN * kBKBytes;
+  constexpr uint32_t kCols = BN == 256 ? 512 : 256;  // accumulator + 48 scale columns, a power of 2
+  static_assert(BN + 48 <= (int)kCols, "tensor memory budget");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_slot;
+  const int warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < (kA + kB) / 16; i += blockDim.x) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                 "r"(kCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // the operands were written through the generic proxy; the MMA reads them through the async proxy
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  // scale columns [BN, BN + 48) of this warp's lane quadrant: E4M3 1.0 in every byte
+  {
+    const uint4 one = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
+    const uint32_t col = tmem + ((uint32_t)(32 * warp) << 16) + BN;
+    tc_st16(col, one, one, one, one);
+    tc_st16(col + 16, one, one, one, one);
+    tc_st16(col + 32, one, one, one, one);
+    tc_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 32) {
+    constexpr uint32_t idesc = mma_idesc(kBM, BN);
+    const uint64_t adesc = smem_desc(smem_u32(smem), 16, 1024, 2);
+    const uint64_t bdesc = smem_desc(smem_u32(smem + kA), 16, 1024, 2);
+    const uint32_t sfa = tmem + BN, sfb = sfa + 16;
+    for (int64_t it = 0; it < iters; ++it)
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        tc_mma(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, sfa + 4 * kk, sfb + (BN / 32) * kk, (it | kk) != 0);
+    tc_commit(smem_u32(&bar));
+    if (!mbar_wait(smem_u32(&bar), 0, timeout_ns, nullptr) && status) atomicExch(status, (int)FOS_ERR_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");
+  }
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- host side
@@ -705,6 +775,22 @@ fos_status gemm_after_producer_of_a(const fos_nvfp4_tensor* A, const fos_nvfp4_t
   return gemm_checked(A, B, C, ldc, dev_status, kDefaultTimeoutNs, 0, true, stream);
 }
 }  // namespace fos
+
+extern "C" fos_status fos_selftest_mma_rate(int32_t n_cols, int64_t iters, int32_t grid, int32_t* dev_status,
+                                            cudaStream_t stream) {
+  if ((n_cols != 128 && n_cols != 256) || iters < 1 || iters > (1ll << 24) || grid < 1) return FOS_ERR_INVALID_ARG;
+  if (dev_status && !aligned(dev_status, 4)) return FOS_ERR_INVALID_ARG;
+  const int g = grid < sm_count() ? grid : sm_count();
+  const void* fn = n_cols == 256 ? reinterpret_cast<const void*>(mma_rate_kernel<256>)
+                                 : reinterpret_cast<const void*>(mma_rate_kernel<128>);
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kRateSmemBytes) != cudaSuccess)
+    return FOS_ERR_CUDA;
+  if (n_cols == 256)
+    mma_rate_kernel<256><<<g, 128, kRateSmemBytes, stream>>>(iters, kDefaultTimeoutNs, dev_status);
+  else
+    mma_rate_kernel<128><<<g, 128, kRateSmemBytes, stream>>>(iters, kDefaultTimeoutNs, dev_status);
+  return cudaGetLastError() == cudaSuccess ? FOS_OK : FOS_ERR_CUDA;
+}
 
 extern "C" fos_status fos_gemm(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* C, int64_t ldc,
                                int32_t* dev_status, cudaStream_t stream) {

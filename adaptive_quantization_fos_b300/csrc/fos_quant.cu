@@ -522,14 +522,18 @@ __global__ void __launch_bounds__(MODE == kRowsChained ? 320 : 256, MODE == kRow
   uint8_t* slots = q_smem + warp * (kRowSlots * kRowSlotBytes);
   const uint32_t bar0 = smem_addr(&s_bar[warp * kRowSlots]);
 
-  // producer cursor (lane 0): the next task to fetch
+  // producer cursor (lane 0): the next task to fetch.  The quantize pass runs
+  // the rows from last to first: an amax pass over the same matrix (the one
+  // of this launch, or the previous launch's amax warps) read them first to
+  // last, so the rows it read last -- the ones most likely still in L2 --
+  // are quantized first.
   int64_t pr = gw / wpr, pch = gw - pr * wpr;
   auto issue_next = [&](int slot) -> bool {
     if (pr >= p.R) return false;
     const int64_t c0 = pch * 128;
     const int64_t nblk = nb - c0 < 128 ? nb - c0 : 128;
-    bulk_g2s_hint(smem_addr(slots + slot * kRowSlotBytes), p.x + pr * p.ld + c0 * 16, (uint32_t)(nblk * 32),
-                  bar0 + 8u * slot, stream_once);
+    bulk_g2s_hint(smem_addr(slots + slot * kRowSlotBytes), p.x + (p.R - 1 - pr) * p.ld + c0 * 16,
+                  (uint32_t)(nblk * 32), bar0 + 8u * slot, stream_once);
     pr += dr;
     pch += dch;
     if (pch >= wpr) {
@@ -557,12 +561,13 @@ __global__ void __launch_bounds__(MODE == kRowsChained ? 320 : 256, MODE == kRow
   int slot = 0;
   uint32_t ph = 0;
   bool failed = false;
-  int64_t r = gw / wpr, ch = gw - r * wpr;
-  for (; r < p.R; r += dr, ch += dch) {
+  int64_t ri = gw / wpr, ch = gw - ri * wpr;
+  for (; ri < p.R; ri += dr, ch += dch) {
     if (ch >= wpr) {
       ch -= wpr;
-      if (++r >= p.R) break;
+      if (++ri >= p.R) break;
     }
+    const int64_t r = p.R - 1 - ri;  // rows run last to first (see the note at the ring)
     const int64_t c0 = ch * 128;
     const int nblk = nb - c0 < 128 ? (int)(nb - c0) : 128;
     // every lane observes the copy's completion itself; the verdict is made

@@ -106,11 +106,13 @@ class ClockSampler:
                0x100: "display_clock_setting"}
     NVML_CLOCK_SM = 1
 
-    def __init__(self, device_index: int, period_s: float = 0.005):
+    def __init__(self, device_index: int, period_s: float = 0.001):
         import ctypes
 
         self.period = period_s
         self.samples: list[tuple[int, int]] = []
+        self.times: list[float] = []
+        self.window: tuple[float, float] | None = None
         self.max_mhz = None
         self._stop = threading.Event()
         self._ok = False
@@ -162,7 +164,13 @@ class ClockSampler:
             if self.nv.nvmlDeviceGetClockInfo(self.h, self.NVML_CLOCK_SM, ctypes.byref(clk)) == 0 and \
                     self._reasons_fn(self.h, ctypes.byref(rs)) == 0:
                 self.samples.append((clk.value, rs.value))
+                self.times.append(time.perf_counter())
             time.sleep(self.period)
+
+    def mark(self, t0: float, t1: float) -> None:
+        """Host-time bounds of the timed region (the rest of the sampled
+        window runs the same work untimed, so short regions get samples)."""
+        self.window = (t0, t1)
 
     def __enter__(self):
         if self._ok:
@@ -182,9 +190,17 @@ class ClockSampler:
         bits = 0
         for _, r in self.samples:
             bits |= r
-        return {"sm_mhz": statistics.median(s for s, _ in self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": [n for b, n in self.REASONS.items() if bits & b and n != "gpu_idle"],
-                "samples": len(self.samples)}
+        out = {"sm_mhz": statistics.median(s for s, _ in self.samples), "sm_max_mhz": self.max_mhz,
+               "reasons": [n for b, n in self.REASONS.items() if bits & b and n != "gpu_idle"],
+               "samples": len(self.samples), "period_ms": self.period * 1e3}
+        if self.window:
+            inside = [s for (s, _), t in zip(self.samples, self.times) if self.window[0] <= t <= self.window[1]]
+            out["samples_timed_region"] = len(inside)
+            if inside:
+                out["sm_mhz_timed_region"] = statistics.median(inside)
+            out["note"] = ("sampled over the timed region and an untimed continuation of the same steps "
+                           "(at least 0.3 s of load in all)")
+        return out
 
 
 # ------------------------------------------------------------ distributed
@@ -230,19 +246,55 @@ class Dist:
 # ------------------------------------------------------------ CPU oracle
 
 
-def cpu_oracle_rate(mats: dict, rows_per_matrix: int) -> tuple[float, str, float]:
-    """Time the oracle on the first `rows_per_matrix` rows of each matrix."""
+def host_cpu() -> dict:
+    """The host's logical core count and CPU model (from /proc/cpuinfo)."""
+    model = "unknown"
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    try:
+        n = len(os.sched_getaffinity(0))
+    except AttributeError:
+        n = os.cpu_count() or 1
+    return {"nproc": n, "model": model}
+
+
+def oracle_quantize_threads(orc, bits: np.ndarray, threads: int, pool) -> None:
+    """The oracle's quantization of one matrix on `threads` host threads: the
+    tensor amax first (one pass), then row ranges in parallel, each with that
+    amax supplied, so every range gets the whole matrix's tensor scale.  The
+    oracle's C code releases the interpreter lock while it runs."""
+    if threads <= 1:
+        orc.quantize(bits)
+        return
+    amax = float(np.abs(workloads.bf16_to_f32(bits)).max())
+    bounds = np.linspace(0, bits.shape[0], threads + 1).astype(int)
+    parts = [bits[a:b] for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+    list(pool.map(lambda part: orc.quantize(part, amax=amax), parts))
+
+
+def cpu_oracle_rate(mats: dict, rows_per_matrix: int, threads: int = 1) -> tuple[float, str, float]:
+    """Time the oracle on the first `rows_per_matrix` rows of each matrix, on
+    `threads` host threads (row ranges)."""
+    from concurrent.futures import ThreadPoolExecutor
+
     import oracle
 
     oracle.build()
-    n = 0
-    t0 = time.perf_counter()
-    for bits in mats.values():
-        sub = np.ascontiguousarray(bits[:rows_per_matrix])
-        oracle.quantize(sub)
-        n += sub.size
-    dt = time.perf_counter() - t0
-    sample = f"first {rows_per_matrix} rows of each of the 7 matrices ({n / 1e6:.1f}M values), 1 thread"
+    subs = [np.ascontiguousarray(bits[:rows_per_matrix]) for bits in mats.values()]
+    n = sum(s.size for s in subs)
+    with ThreadPoolExecutor(max_workers=max(1, threads)) as pool:
+        t0 = time.perf_counter()
+        for sub in subs:
+            oracle_quantize_threads(oracle, sub, threads, pool)
+        dt = time.perf_counter() - t0
+    sample = (f"first {rows_per_matrix} rows of each of the 7 matrices ({n / 1e6:.1f}M values), "
+              f"{threads} thread{'s' if threads > 1 else ''}")
     return n / dt / 1e9, sample, dt
 
 
@@ -294,11 +346,20 @@ def run_fos(args, dist: Dist) -> None:
     dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
+        h0 = time.perf_counter()
         e0.record(stream)
         for _ in range(args.steps):
             step()
         e1.record(stream)
         torch.cuda.synchronize()
+        h1 = time.perf_counter()
+        clk.mark(h0, h1)
+        # the same steps, untimed, so that the clock record covers at least
+        # 0.3 s of this load even when the timed region is a few ms
+        while time.perf_counter() - h0 < 0.3:
+            for _ in range(20):
+                step()
+            torch.cuda.synchronize()
     dist.barrier()
     t_ms = dist.max(e0.elapsed_time(e1), dev)
     ms_per_step = t_ms / args.steps
@@ -366,9 +427,15 @@ def run_fos(args, dist: Dist) -> None:
         out["e2e"] = e2e_host_buffers(torch, fos, mats_np, dev, max(2, min(args.steps, 5)))
         out["secondary"] = secondary(torch, fos, dev, pk)
     if dist.rank == 0 and dist.world == 1 and not args.no_extras:
-        rate, sample, secs = cpu_oracle_rate(mats_np, CPU_SAMPLE_ROWS)
-        out["cpu_baseline"] = {"value": round(rate, 6), "unit": "Gelem/s", "cores": 1, "kind": "oracle",
-                               "sample": sample, "seconds": round(secs, 2)}
+        cpu = host_cpu()
+        rate1, sample1, secs1 = cpu_oracle_rate(mats_np, CPU_SAMPLE_ROWS, 1)
+        rows_all = min(4096, CPU_SAMPLE_ROWS * max(1, cpu["nproc"] // 4))
+        rate_n, sample_n, secs_n = cpu_oracle_rate(mats_np, rows_all, cpu["nproc"])
+        out["cpu_baseline"] = {"value": round(rate_n, 6), "unit": "Gelem/s", "cores": cpu["nproc"], "kind": "oracle",
+                               "sample": sample_n, "seconds": round(secs_n, 2), "cpu_model": cpu["model"],
+                               "nproc": cpu["nproc"],
+                               "single_thread": {"value": round(rate1, 6), "cores": 1, "sample": sample1,
+                                                 "seconds": round(secs1, 2)}}
     if dist.rank == 0:
         print(json.dumps(out), flush=True)
     dist.close()
@@ -527,6 +594,34 @@ def linear_backward(torch, fos, dev, pk) -> dict:
             "options": "SR on dY (both copies), RHT along M on dY^T and X^T, W^T 1D"}
 
 
+def mma_rate(torch, fos, dev) -> dict:
+    """The tensor-pipe throughput of the GEMM's own MMA instruction
+    (kind::mxf4nvf4, E4M3 scales per 16 values, M = 128, K = 64, N = 128 or
+    256) on this GPU: fos_selftest_mma_rate, one CTA per SM issuing MMAs back
+    to back on operands resident in shared memory, timed with CUDA events."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    s = torch.cuda.current_stream(dev)
+    out = {"sms": sms}
+    iters = 1 << 15
+    with ClockSampler(dev.index) as clk:
+        for n in (256, 128):
+            for it in (64, iters):  # a short warm-up launch, then the timed one
+                e0, e1 = _events(torch, 2)
+                e0.record(s)
+                st = fos.fos_selftest_mma_rate(n, it, sms, status.data_ptr(), s.cuda_stream)
+                e1.record(s)
+                if st != fos.FOS_OK:
+                    return {"status": f"probe unavailable (status {st})"}
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            out[f"n{n}"] = {"ms": round(ms, 3), "tflops": round(2.0 * 128 * n * 64 * 4 * iters * sms / (ms * 1e-3) / 1e12, 1)}
+    out["timeout"] = int(status.item()) != 0
+    out["clocks"] = clk.summary()
+    out["instruction"] = "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X, M=128, K=64"
+    return out
+
+
 def linear_forward(torch, fos, dev, pk) -> dict:
     """Quantize A (8192 x 4096 activations) and W (12288 x 4096 weights) with
     4/6 1D RNE, then C = A W^T in NVFP4 on the tensor cores.  Also the whole
@@ -551,7 +646,10 @@ def linear_forward(torch, fos, dev, pk) -> dict:
         t_two = _time_calls(torch, lambda: (qa(A), fos.gemm(a, w, out=C)), 50)
     tf = flops / (t * 1e-3) / 1e12
     fp4_peak = pk["bf16_tflops"] * 6.0  # measured bf16 burst x nominal dense fp4/bf16 ratio (13.5 / 2.25)
+    rate = mma_rate(torch, fos, dev)
     return {"gemm_ms": round(t, 4), "tflops": round(tf, 1), "clocks": clk.summary(),
+            "mma_rate_probe": rate,
+            "frac_of_mma_rate": round(tf / rate["n256"]["tflops"], 4) if rate.get("n256") else None,
             "layer_forward_ms": round(t_layer, 4), "layer_forward_tflops": round(flops / (t_layer * 1e-3) / 1e12, 1),
             "quantize_then_gemm_ms": round(t_two, 4),
             "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
@@ -568,13 +666,19 @@ def run_reference(args, dist: Dist) -> None:
     import oracle
 
     oracle.build()
+    from concurrent.futures import ThreadPoolExecutor
+
     mats_np = workloads.qwen3_8b_weights()
-    subs = {k: np.ascontiguousarray(v[:REF_SAMPLE_ROWS]) for k, v in mats_np.items()}
+    cpu = host_cpu()
+    threads = cpu["nproc"]
+    rows = REF_SAMPLE_ROWS * max(1, min(threads, 64) // 4)
+    subs = {k: np.ascontiguousarray(v[:rows]) for k, v in mats_np.items()}
     n = sum(v.size for v in subs.values())
+    pool = ThreadPoolExecutor(max_workers=threads)
 
     def step():
         for v in subs.values():
-            oracle.quantize(v)
+            oracle_quantize_threads(oracle, v, threads, pool)
 
     for _ in range(args.warmup):
         step()
@@ -582,14 +686,16 @@ def run_reference(args, dist: Dist) -> None:
     for _ in range(args.steps):
         step()
     dt = time.perf_counter() - t0
+    pool.shutdown()
     value = n * args.steps / dt / 1e9
-    sample = f"first {REF_SAMPLE_ROWS} rows of each of the 7 matrices per step ({n / 1e6:.2f}M values), 1 thread"
+    sample = (f"first {rows} rows of each of the 7 matrices per step ({n / 1e6:.2f}M values), {threads} threads "
+              f"over row ranges ({cpu['model']})")
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "Gelem/s", "n_gpus": dist.world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
            "config": {"workload": WORKLOAD, "elements_per_step": n, "l2": "host run (no GPU)"},
-           "cpu_baseline": {"value": round(value, 6), "unit": "Gelem/s", "cores": 1, "kind": "oracle",
-                            "sample": sample},
+           "cpu_baseline": {"value": round(value, 6), "unit": "Gelem/s", "cores": threads, "kind": "oracle",
+                            "sample": sample, "cpu_model": cpu["model"], "nproc": cpu["nproc"]},
            "e2e": {"value": round(value, 6), "unit": "Gelem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 

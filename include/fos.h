@@ -397,6 +397,24 @@ fos_status fos_linear_forward(const void* x, int64_t ld_x, int64_t M, int64_t K,
 fos_status fos_selftest_wait_limits(void* scratch, size_t scratch_bytes, uint64_t timeout_ns, int32_t* result,
                                     cudaStream_t stream);
 
+/*
+ * fos_selftest_mma_rate -- a measurement, not a product path: the tensor-pipe
+ * throughput of the GEMM's own MMA instruction on this GPU, the ceiling that
+ * fos_gemm's achieved rate is compared with.  The pages have no counterpart.
+ * min(grid, SM count) CTAs (one per SM) each issue iters x 4 MMAs of
+ * kind::mxf4nvf4 with E4M3 scales per 16 values, M = 128, N = n_cols, K = 64,
+ * back to back on zero operands held in shared memory (scales 1.0): no loads,
+ * no stores.  Work done: 2 * 128 * n_cols * 64 * 4 * iters flops per CTA;
+ * the caller times the launch on `stream` (CUDA events).
+ *   n_cols      128 or 256.
+ *   iters       1 .. 2^24.
+ *   dev_status  optional device int32: FOS_ERR_TIMEOUT if the completion wait
+ *               outlasted its limit (2 s); left untouched otherwise.
+ * Returns FOS_ERR_INVALID_ARG on other arguments, FOS_ERR_CUDA if the launch fails.
+ */
+fos_status fos_selftest_mma_rate(int32_t n_cols, int64_t iters, int32_t grid, int32_t* dev_status,
+                                 cudaStream_t stream);
+
 /* ---- element codecs (the conversions the quantizer uses), for testing ---- */
 
 /* codes[i] = E2M1 code (RNE, saturating, sign kept) of x[i]; one code per byte. */

@@ -225,3 +225,10 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
                                            f'LIB_PATH = {str(tmp_path / "missing.so")!r}')
     with pytest.raises(ImportError):
         exec(compile(src, spec.origin, "exec"), mod.__dict__)
+
+
+def test_mma_rate_rejects_bad_arguments(fos):
+    assert fos.fos_selftest_mma_rate(64, 10, 1, 0, None) == fos.FOS_ERR_INVALID_ARG
+    assert fos.fos_selftest_mma_rate(256, 0, 1, 0, None) == fos.FOS_ERR_INVALID_ARG
+    assert fos.fos_selftest_mma_rate(256, 1 << 25, 1, 0, None) == fos.FOS_ERR_INVALID_ARG
+    assert fos.fos_selftest_mma_rate(128, 10, 0, 0, None) == fos.FOS_ERR_INVALID_ARG
