@@ -342,12 +342,9 @@ __device__ __forceinline__ bool grid_barrier(unsigned int* word, unsigned int n,
 }
 
 // ------------------------------------------------------------------- RHT
-// In place on 16 values: sign flips (bit j of mask), butterflies of stride
-// 1, 2, 4, 8 -- (a, b) -> (a + b, a - b) -- then an exact scaling by 1/4.
-__device__ __forceinline__ void rht16(float (&v)[16], uint32_t mask) {
-#pragma unroll
-  for (int j = 0; j < 16; ++j)
-    if ((mask >> j) & 1u) v[j] = -v[j];
+// In place on 16 values: the butterflies of stride 1, 2, 4, 8 --
+// (a, b) -> (a + b, a - b) -- without the final scaling by 1/4.
+__device__ __forceinline__ void butterflies16(float (&v)[16]) {
 #pragma unroll
   for (int j = 0; j < 16; j += 2) {
     float a = v[j], b = v[j + 1];
@@ -365,6 +362,15 @@ __device__ __forceinline__ void rht16(float (&v)[16], uint32_t mask) {
       v[j + h] = d.x; v[j + h + 1] = d.y;
     }
   }
+}
+
+// In place on 16 values: sign flips (bit j of mask), the butterflies, then an
+// exact scaling by 1/4.
+__device__ __forceinline__ void rht16(float (&v)[16], uint32_t mask) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if ((mask >> j) & 1u) v[j] = -v[j];
+  butterflies16(v);
 #pragma unroll
   for (int j = 0; j < 16; j += 2) {
     F2 s = mul2(F2{v[j], v[j + 1]}, F2{0.25f, 0.25f});

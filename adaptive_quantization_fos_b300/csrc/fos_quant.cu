@@ -125,6 +125,11 @@ __device__ __forceinline__ void unpack16(const uint32_t (&w)[8], uint32_t mask, 
 // RHT butterflies (stride 1, 2, 4, 8) and the 1/4 scaling; signs already applied.
 __device__ __forceinline__ void hadamard16(float (&v)[16]) { rht16(v, 0u); }
 
+// The amax passes take the block maxima of the transform without its 1/4:
+// rounding is monotone, so max_j |fl(w_j / 4)| = fl(max_j |w_j| / 4), and the
+// scaling is applied once to a thread's running maximum (unscaled_to_amax).
+__device__ __forceinline__ float unscaled_to_amax(float m) { return __fmul_rn(m, 0.25f); }
+
 // max |y_j| of 16 floats with the three-input maximum of magnitudes
 // (sm_100+): 7 instructions instead of 15.  Inputs are finite.
 __device__ __forceinline__ float max3abs(float a, float b, float c) {
@@ -160,10 +165,11 @@ __global__ void __launch_bounds__(256) amax_rows_kernel(AmaxParams p) {
     } else {
       float y[16];
       unpack16(w, rht_mask, y);
-      hadamard16(y);
+      butterflies16(y);  // 1/4 applied to the maximum below
       m = fmaxf(m, absmax16(y));
     }
   }
+  if (RHT) m = unscaled_to_amax(m);
   m = block_max(m, s_red);
   if (threadIdx.x == 0) p.partials[blockIdx.x] = m;
 }
@@ -193,10 +199,11 @@ __global__ void __launch_bounds__(256) amax_cols_kernel(AmaxParams p) {
         uint32_t s = ((rht_mask >> i) & 1u) << 31;
         y[i] = __uint_as_float(((k & 1) ? (wv & 0xFFFF0000u) : (wv << 16)) ^ s);
       }
-      hadamard16(y);
+      butterflies16(y);  // 1/4 applied to the maximum below
       m = fmaxf(m, absmax16(y));
     }
   }
+  m = unscaled_to_amax(m);
   m = block_max(m, s_red);
   if (threadIdx.x == 0) p.partials[blockIdx.x] = m;
 }
@@ -399,13 +406,14 @@ __device__ __forceinline__ void next_job_amax(const QuantParams& p, uint8_t* rin
         if (RHT) {
           float y[16];
           unpack16(wv[j], rht_mask, y);
-          hadamard16(y);
+          butterflies16(y);  // 1/4 applied to the maximum below
           m = fmaxf(m, absmax16(y));
         } else {
           m = fmaxf(m, absmax16_bf16(wv[j]));
         }
       }
     }
+    if (RHT) m = unscaled_to_amax(m);
     if (failed) m = __int_as_float(0x7FC00000);
     if (lane == 0) {
       for (; consumed < issued; ++consumed) {
@@ -508,13 +516,14 @@ __global__ void __launch_bounds__(MODE == kRowsChained ? 320 : 256, MODE == kRow
         if (RHT) {
           float y[16];
           unpack16(wv[j], rht_mask, y);
-          hadamard16(y);
+          butterflies16(y);  // 1/4 applied to the maximum below
           m = fmaxf(m, absmax16(y));
         } else {
           m = fmaxf(m, absmax16_bf16(wv[j]));
         }
       }
     }
+    if (RHT) m = unscaled_to_amax(m);
     m = block_max(m, s_red);
     if (threadIdx.x == 0) {
       p.ws_partials[blockIdx.x] = m;

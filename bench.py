@@ -530,10 +530,27 @@ def secondary(torch, fos, dev, pk) -> dict:
         t_flush = _time_calls(torch, lambda: flush.fill_(1), reps)
         t = _time_calls(torch, call, reps) - t_flush
         n = x.numel()
+        gbs = n * BYTES_PER_ELEM_QUANT / (t * 1e-3) / 1e9
         res[name] = {"ms": round(t, 4), "gelem_s": round(n / (t * 1e-3) / 1e9, 2),
-                     "algorithmic_gbs": round(n * BYTES_PER_ELEM_QUANT / (t * 1e-3) / 1e9, 1),
+                     "algorithmic_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4),
                      "shape": list(x.shape), "options": {k: v for k, v in opts.items() if k != "tensor_amax"}}
+        if delayed:
+            # the same call with the tensor amax supplied (delayed scaling, a
+            # previous step's amax): the quantize pass alone
+            amax = fos.tensor_amax(x, hadamard=opts.get("hadamard", False), transpose=opts.get("transpose", False),
+                                   hadamard_seed=opts.get("hadamard_seed", 0))
+            qd = fos.Quantizer(*x.shape, device=dev, tensor_amax=amax, **opts)
 
+            def call_d():
+                flush.fill_(1)
+                qd(x)
+
+            td = _time_calls(torch, call_d, reps) - t_flush
+            gd = n * BYTES_PER_ELEM_QUANT / (td * 1e-3) / 1e9
+            res[name]["amax_supplied"] = {"ms": round(td, 4), "gelem_s": round(n / (td * 1e-3) / 1e9, 2),
+                                          "algorithmic_gbs": round(gd, 1), "frac_of_hbm": round(gd / pk["hbm_gbs"], 4)}
+
+    delayed = True
     act = workloads.activations(16384, 4096, seed=3001)
     measure("activation_rht_rowmajor", act, hadamard=True, hadamard_seed=3002)
     measure("activation_rht_transposed", act, hadamard=True, hadamard_seed=3002, transpose=True)
@@ -750,12 +767,36 @@ def run_case(args) -> None:
                           transpose=True, hadamard=True, hadamard_seed=12)
         for _ in range(3):
             q(x)
+    elif args.case == "quant_rows_rht":
+        # 16384 x 4096 activations with the RHT, amax supplied: only the row
+        # quantize kernel runs
+        x = _to_dev(torch, workloads.activations(16384, 4096, seed=3001), dev)
+        amax = fos.tensor_amax(x, hadamard=True, hadamard_seed=3002)
+        q = fos.Quantizer(*x.shape, device=dev, tensor_amax=amax, hadamard=True, hadamard_seed=3002)
+        for _ in range(3):
+            q(x)
+    elif args.case == "quant_2d":
+        # the 8192 x 12288 gradient in 16 x 16 tiles, RNE, amax supplied: only
+        # the 2D quantize kernel runs
+        x = _to_dev(torch, workloads.gradients(8192, 12288, seed=4001), dev)
+        amax = fos.tensor_amax(x)
+        q = fos.Quantizer(*x.shape, device=dev, tensor_amax=amax, block_2d=True)
+        for _ in range(3):
+            q(x)
     elif args.case == "quant_mxfp4":
         # 8192 x 12288 gradient (201 MB > L2), MXFP4 with the 4/6 choice: one
         # single-pass kernel
         x = _to_dev(torch, workloads.gradients(8192, 12288, seed=4001), dev)
         for _ in range(3):
             fos.quantize_mxfp4(x)
+    elif args.case == "mma_rate":
+        # the tensor-pipe rate probe: one CTA per SM issuing the GEMM's MMA
+        # instruction back to back (N = 256), three launches
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        for _ in range(3):
+            st = fos.fos_selftest_mma_rate(256, 4096, sms, 0, torch.cuda.current_stream().cuda_stream)
+            if st != fos.FOS_OK:
+                raise SystemExit(f"probe status {st}")
     elif args.case == "gemm":
         A = _to_dev(torch, workloads.activations(8192, 4096, seed=5001), dev)
         W = _to_dev(torch, workloads.student_t(12288, 4096, seed=5002), dev)
