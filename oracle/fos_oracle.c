@@ -66,7 +66,10 @@
  *       q = y * 2^-X; S_M is the sum of (q - g)^2 in the R2 order over each
  *       16-value half, the halves then added; keep 4 iff 4 * S_4 < S_6 (the
  *       4-candidate's error in the 6-candidate's units, exact), ties to 6.
- *       An all-zero block gets byte 0 (2^-127) and zero codes.
+ *       An all-zero block gets byte 0 (2^-127) and zero codes.  A block that
+ *       holds a NaN or an infinity gets the E8M0 NaN byte 0xFF ([MX]: a NaN
+ *       scale makes every value of its block NaN; E2M1 itself has neither),
+ *       zero codes and choice 0.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -shared -fPIC.
  * FP32 arithmetic is IEEE binary32 round-to-nearest-even: every float
@@ -542,9 +545,17 @@ int orc_quantize_mx(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, i
   for (int64_t r = 0; r < rows; ++r)
     for (int64_t b = 0; b < nb; ++b) {
       float y[32], a = 0.0f;
+      int finite = 1;
       for (int j = 0; j < 32; ++j) {
         y[j] = bf16_to_f32(x[r * ld + 32 * b + j]);
+        if (!isfinite(y[j])) finite = 0;
         if (fabsf(y[j]) > a) a = fabsf(y[j]);
+      }
+      if (!finite) { /* R12: the NaN scale, zero codes */
+        for (int j = 0; j < 16; ++j) codes[r * ld_codes + 16 * b + j] = 0;
+        scales[r * nb + b] = 0xFF;
+        if (choice) choice[r * nb + b] = 0;
+        continue;
       }
       uint8_t c6[32], c4[32];
       int X6, X4;

@@ -606,3 +606,38 @@ def test_mx_hand_built_blocks(orc):
     assert np.array_equal(orc.dequantize_mx(q)[1], b)
     z = orc.quantize_mx(np.zeros((1, 32), np.uint16))
     assert z.scales[0, 0] == 0 and not z.codes.any() and z.choice[0, 0] == 0
+
+
+def test_mx_non_finite_blocks_get_the_nan_scale(orc):
+    """R12: a block holding a NaN or an infinity gets the E8M0 NaN byte 0xFF
+    (the OCP MX specification: a NaN scale makes its whole block NaN), zero
+    codes and choice 0, and dequantizes to NaN; the other blocks of the row are
+    quantized as if it were not there."""
+    rng = np.random.default_rng(44)
+    x = rng.standard_normal((3, 128)).astype(np.float32)
+    x[0, 5] = np.inf
+    x[1, 40] = -np.inf
+    x[2, 70] = np.nan
+    bits = workloads.bf16_bits(np.nan_to_num(x, nan=0.0, posinf=0.0, neginf=0.0))
+    bits[0, 5], bits[1, 40], bits[2, 70] = 0x7F80, 0xFF80, 0x7FC0  # +inf, -inf, NaN
+    q = orc.quantize_mx(bits)
+    bad = {(0, 0), (1, 1), (2, 2)}
+    for r in range(3):
+        for b in range(4):
+            if (r, b) in bad:
+                assert q.scales[r, b] == 0xFF and q.choice[r, b] == 0
+                assert not q.codes[r, 16 * b: 16 * b + 16].any()
+            else:
+                assert q.scales[r, b] != 0xFF
+    clean = bits.copy()
+    clean[0, 5] = clean[1, 40] = clean[2, 70] = 0
+    qc = orc.quantize_mx(clean)
+    for r in range(3):
+        for b in range(4):
+            if (r, b) not in bad:
+                assert q.scales[r, b] == qc.scales[r, b]
+                assert np.array_equal(q.codes[r, 16 * b: 16 * b + 16], qc.codes[r, 16 * b: 16 * b + 16])
+    d = orc.dequantize_mx(q)
+    for r, b in bad:
+        assert np.isnan(d[r, 32 * b: 32 * b + 32]).all()
+    assert np.isfinite(d[0, 32:]).all()
