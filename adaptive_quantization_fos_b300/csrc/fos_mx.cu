@@ -16,6 +16,7 @@
 // thread owns one 32-value block (64 contiguous bytes; a warp reads 2 KB).
 #include <cuda_runtime.h>
 
+#include <cfloat>
 #include <cstdint>
 
 #include "fos.h"
@@ -24,6 +25,12 @@
 
 namespace fos {
 namespace {
+
+__device__ __forceinline__ float max_nan_f32(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
 
 struct MxParams {
   const uint16_t* x;
@@ -34,6 +41,20 @@ struct MxParams {
   uint8_t* choice;  // optional, same shape
   int codes16;      // codes 16-byte aligned with ld_codes % 16 == 0
 };
+
+// max |x| of 16 bf16 values held as 8 words, NaN-propagating: a NaN input
+// gives NaN, an infinity gives infinity (the sign bit of the bf16 maxima is
+// junk from xorsign and is dropped).
+__device__ __forceinline__ float absmax16_bf16_nan(const uint32_t (&w)[8]) {
+  uint32_t m[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m[k]) : "r"(w[2 * k]), "r"(w[2 * k + 1]));
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m[0]) : "r"(m[0]), "r"(m[1]));
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m[2]) : "r"(m[2]), "r"(m[3]));
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m[0]) : "r"(m[0]), "r"(m[2]));
+  return max_nan_f32(fabsf(__uint_as_float(m[0] << 16)), fabsf(__uint_as_float(m[0] & 0xFFFF0000u)));
+}
 
 // floor(log2 a) for a finite float a > 0, from its bits (exact).
 __device__ __forceinline__ int floor_log2(float a) {
@@ -82,7 +103,10 @@ __global__ void __launch_bounds__(256) quant_mx_kernel(MxParams p) {
     }
     const uint32_t lo8[8] = {wv[0], wv[1], wv[2], wv[3], wv[4], wv[5], wv[6], wv[7]};
     const uint32_t hi8[8] = {wv[8], wv[9], wv[10], wv[11], wv[12], wv[13], wv[14], wv[15]};
-    const float a = fmaxf(absmax16_bf16(lo8), absmax16_bf16(hi8));
+    const float a = max_nan_f32(absmax16_bf16_nan(lo8), absmax16_bf16_nan(hi8));
+    // a block holding a NaN or an infinity gets the E8M0 NaN scale 0xFF (its
+    // every value decodes to NaN) with zero codes
+    const bool finite = a <= FLT_MAX;
     int X6 = -127, X4 = -127;
     if (a > 0.0f) {
       const int e = floor_log2(a);
@@ -97,8 +121,10 @@ __global__ void __launch_bounds__(256) quant_mx_kernel(MxParams p) {
     if (RULE != FOS_SCALE_4) S6 = mx_candidate(yp, exp2_neg(X6), c6);
     if (RULE != FOS_SCALE_6) S4 = mx_candidate(yp, exp2_neg(X4), c4);
     const float S4u = X4 > X6 ? __fmul_rn(S4, 4.0f) : S4;
-    const bool four = (RULE == FOS_SCALE_4) || (RULE == FOS_SCALE_4OVER6 && S4u < S6);
-    const uint32_t* c = four ? c4 : c6;
+    const bool four = finite && ((RULE == FOS_SCALE_4) || (RULE == FOS_SCALE_4OVER6 && S4u < S6));
+    uint32_t c[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) c[k] = finite ? (four ? c4[k] : c6[k]) : 0u;
     uint8_t* dst = p.codes + r * p.ld_codes + b * 16;
     if (p.codes16) {
       *reinterpret_cast<uint4*>(dst) = make_uint4(c[0], c[1], c[2], c[3]);
@@ -106,7 +132,7 @@ __global__ void __launch_bounds__(256) quant_mx_kernel(MxParams p) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) reinterpret_cast<uint32_t*>(dst)[k] = c[k];
     }
-    p.scales[t] = (uint8_t)((four ? X4 : X6) + 127);
+    p.scales[t] = finite ? (uint8_t)((four ? X4 : X6) + 127) : (uint8_t)0xFF;
     if (p.choice) p.choice[t] = four ? 1 : 0;
   }
 }
@@ -127,8 +153,10 @@ __global__ void __launch_bounds__(256) dequant_mx_kernel(MxDequantParams p) {
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = t / nb, b = t - r * nb;
     const int X = (int)p.scales[t] - 127;
-    // 2^X: normal for X >= -126; 2^-127 is the subnormal 0x00400000
-    const float s = X >= -126 ? __uint_as_float((uint32_t)(X + 127) << 23) : __uint_as_float(0x00400000u);
+    // 2^X: normal for X >= -126; 2^-127 is the subnormal 0x00400000; byte
+    // 0xFF is the NaN scale (every value of the block NaN)
+    const float s = X == 128 ? __uint_as_float(0x7FC00000u)
+                  : X >= -126 ? __uint_as_float((uint32_t)(X + 127) << 23) : __uint_as_float(0x00400000u);
     const uint8_t* cw = p.codes + r * p.ld_codes + b * 16;
 #pragma unroll
     for (int k = 0; k < 16; ++k) {

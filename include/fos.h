@@ -263,7 +263,9 @@ fos_status fos_gemm(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* 
  *   S_M = sum (q - g)^2 over each 16-value half (even and odd FMA chains,
  *        then one add), the two halves added;
  *   keep 4 iff 4 * S_4 < S_6 (ties keep 6); scale byte = X + 127.
- * An all-zero block gets byte 0 and zero codes.  No tensor scale, no amax
+ * An all-zero block gets byte 0 and zero codes.  A block that holds a NaN or
+ * an infinity gets the E8M0 NaN byte 0xFF, zero codes and choice 0: it
+ * dequantizes to NaN (MXFP4 has no other way to carry it).  No tensor scale, no amax
  * pass: one launch.
  *   x         device bf16 [rows][ld_x], 16-byte aligned, ld_x % 8 == 0,
  *             cols % 32 == 0.

@@ -71,3 +71,36 @@ def test_mx_padded_rows_and_edges(fos):
 def test_mx_full_size(fos, name, make):
     o = check(fos, make())
     assert 0 < o.choice.mean() < 0.5, name
+
+
+@pytest.mark.parametrize("scale_rule", [0, 1, 2])
+def test_mx_non_finite_blocks(fos, scale_rule):
+    """Blocks holding +inf, -inf or NaN get the E8M0 NaN byte 0xFF with zero
+    codes and choice 0 (reading R12) and dequantize to NaN, bit for bit with
+    the oracle; the other blocks are unaffected."""
+    import torch
+
+    import oracle
+
+    bits = mixed_bits(5, 256, seed=77)
+    bits[0, 3] = 0x7F80   # +inf
+    bits[1, 100] = 0xFF80  # -inf
+    bits[2, 255] = 0x7FC0  # NaN
+    bits[3, 32:64] = 0x7F81  # a block of signalling-pattern NaNs
+    x = to_device_bf16(bits)
+    q = fos.quantize_mxfp4(x, scale_rule=scale_rule, with_choice=True)
+    d = fos.dequantize_mxfp4(q)
+    db = fos.dequantize_mxfp4(q, dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    o = oracle.quantize_mx(bits, scale_rule=scale_rule)
+    assert np.array_equal(q.codes[:, :128].cpu().numpy(), o.codes), "codes differ"
+    assert np.array_equal(q.scales.cpu().numpy(), o.scales), "scale bytes differ"
+    assert np.array_equal(q.choice.cpu().numpy(), o.choice), "choices differ"
+    assert (o.scales == 0xFF).sum() == 4
+    want = oracle.dequantize_mx(o)
+    assert np.array_equal(d.cpu().numpy(), want, equal_nan=True), "dequantized values differ"
+    got_b = db.view(torch.int16).cpu().numpy().view(np.uint16)
+    nan_b = (got_b & 0x7F80) == 0x7F80
+    assert np.array_equal(nan_b & ((got_b & 0x7F) != 0), np.isnan(want)), "bf16 NaN positions differ"
+    fin = ~np.isnan(want)
+    assert np.array_equal(got_b[fin], workloads.bf16_bits(want)[fin])
