@@ -91,3 +91,37 @@ def mixed_bits(rows: int, cols: int, seed: int) -> np.ndarray:
     flat[rng.integers(0, n, max(n // 200, 1))] = -0.0
     flat[rng.integers(0, n, max(n // 300, 1))] *= 1e-30  # tiny magnitudes
     return workloads.bf16_bits(x)
+
+
+def e4m3_tie_blocks():
+    """bf16 rows whose tensor amax is 1.1484375 (s_t = 7/16384 exactly) and
+    whose block maxima a_b make a_b / (M s_t) land exactly on the midpoint of
+    two neighbouring E4M3 values, for M = 4 and M = 6: the cases where a
+    quotient must round to the even neighbour."""
+    from fractions import Fraction
+
+    import oracle
+    import workloads
+
+    finite = [Fraction(float(v)) for v in oracle.e4m3_decode(np.arange(0x7F))]
+    s_t = Fraction(7, 16384)
+    amax = Fraction(1.1484375)
+    ties = []  # (a_b, M, the even neighbour's byte)
+    for M in (4, 6):
+        for k in range(1, len(finite) - 1):
+            mid = (finite[k] + finite[k + 1]) / 2
+            a = mid * M * s_t
+            if a > amax or a <= 0:
+                continue
+            f = np.float32(float(a))
+            if Fraction(float(f)) != a or (f.view(np.uint32) & 0xFFFF):
+                continue  # not a bf16 value
+            ties.append((a, M, k if k % 2 == 0 else k + 1))
+    rows = []
+    for a, _, _ in ties:
+        row = np.zeros(64, np.float32)
+        row[0] = 1.1484375  # the tensor amax (its own block)
+        row[16] = float(a)  # a block whose maximum is the tie
+        row[17:32] = float(a) * np.linspace(-0.9, 0.9, 15)
+        rows.append(row)
+    return workloads.bf16_bits(np.stack(rows)), ties

@@ -641,3 +641,21 @@ def test_mx_non_finite_blocks_get_the_nan_scale(orc):
     for r, b in bad:
         assert np.isnan(d[r, 32 * b: 32 * b + 32]).all()
     assert np.isfinite(d[0, 32:]).all()
+
+
+def test_candidate_scales_round_exact_ties_to_even(orc):
+    """Blocks whose maximum makes a_b / (M s_t) land exactly on the midpoint of
+    two E4M3 values (s_t = 7/16384; found with exact rational arithmetic):
+    the candidate's scale byte must be the even neighbour (round to nearest
+    even, on the exact quotient)."""
+    from fos_testutil import e4m3_tie_blocks
+
+    bits, ties = e4m3_tie_blocks()
+    assert sum(1 for t in ties if t[1] == 4) > 100 and sum(1 for t in ties if t[1] == 6) >= 4
+    for rule, M in ((orc.SCALE_4, 4), (orc.SCALE_6, 6)):
+        q = orc.quantize(bits, scale_rule=rule, sf_layout=orc.SF_ROWMAJOR)
+        assert q.tensor_scale == 7 / 16384
+        sf = q.sf.reshape(bits.shape[0], 4)
+        for r, (_, m, even) in enumerate(ties):
+            if m == M:
+                assert sf[r, 1] == even, (r, hex(sf[r, 1]), hex(even))

@@ -146,3 +146,22 @@ def test_outlier_matrix_matches_and_beats_six_only():
     g46 = check(x)
     check(x, scale_rule=1)
     assert 0 < g46.choice.mean() < 1
+
+
+def test_candidate_scales_at_exact_e4m3_ties():
+    import oracle
+
+    from fos_testutil import e4m3_tie_blocks
+
+    bits, ties = e4m3_tie_blocks()
+    assert len(ties) >= 20
+    # the oracle takes the even neighbour on every tie (RNE of the quotient)
+    for rule, M in ((2, 4), (1, 6)):
+        o = oracle.quantize(bits, scale_rule=rule, sf_layout=1)
+        sf = o.sf.reshape(bits.shape[0], 4)
+        for r, (_, m, even) in enumerate(ties):
+            if m == M:
+                assert sf[r, 1] == even, (r, hex(sf[r, 1]), hex(even))
+    for rule in (0, 1, 2):
+        check(bits, scale_rule=rule)
+        check(bits, scale_rule=rule, sf_layout=1)
