@@ -603,8 +603,10 @@ def linear_backward(torch, fos, dev, pk) -> dict:
     with ClockSampler(dev.index) as clk:
         t = _time_calls(torch, lambda: bw(dy, x, w, dx=dx, dw=dw), 20)
         tq = _time_calls(torch, lambda: [q(s) for q, s in zip(qs, srcs)], 20)
+        names = ["dY_rows_sr", "Wt_cols", "dYt_cols_sr_rht", "Xt_cols_rht"]
+        each = {n: round(_time_calls(torch, lambda q=q, s=s: q(s), 20), 4) for n, q, s in zip(names, qs, srcs)}
     flops = 2 * 2.0 * M * N * K
-    return {"ms": round(t, 4), "quantize_ms": round(tq, 4), "gemm_ms": round(t - tq, 4),
+    return {"ms": round(t, 4), "quantize_ms": round(tq, 4), "quantize_ms_each": each, "gemm_ms": round(t - tq, 4),
             "tflops_effective": round(flops / (t * 1e-3) / 1e12, 1),
             "gemm_tflops": round(flops / ((t - tq) * 1e-3) / 1e12, 1), "clocks": clk.summary(),
             "shape": {"M": M, "N": N, "K": K},
