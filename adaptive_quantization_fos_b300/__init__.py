@@ -75,6 +75,18 @@ class fos_nvfp4_tensor(ctypes.Structure):
     ]
 
 
+class fos_mxfp4_tensor(ctypes.Structure):
+    _fields_ = [
+        ("codes", ctypes.c_void_p),
+        ("sf", ctypes.c_void_p),
+        ("rows", ctypes.c_int64),
+        ("cols", ctypes.c_int64),
+        ("ld_codes", ctypes.c_int64),
+        ("sf_layout", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+
 class fos_backward_options(ctypes.Structure):
     _fields_ = [
         ("struct_size", ctypes.c_uint32),
@@ -116,8 +128,11 @@ def _load() -> ctypes.CDLL:
         "fos_quantize_batch": (i32, [ctypes.POINTER(fos_quant_job), i32, ctypes.POINTER(fos_quant_options), vp, sz,
                                      vp]),
         "fos_linear_backward_workspace_size": (i32, [i64, i64, i64, ctypes.POINTER(sz)]),
-        "fos_quantize_mxfp4": (i32, [vp, i64, i64, i64, i32, vp, i64, vp, vp, vp]),
-        "fos_dequantize_mxfp4": (i32, [vp, vp, i64, i64, i64, vp, i32, i64, vp]),
+        "fos_mxfp4_sf_bytes": (i32, [i64, i64, i32, ctypes.POINTER(sz)]),
+        "fos_quantize_mxfp4": (i32, [vp, i64, i64, i64, i32, i32, vp, i64, vp, vp, vp]),
+        "fos_dequantize_mxfp4": (i32, [ctypes.POINTER(fos_mxfp4_tensor), vp, i32, i64, vp]),
+        "fos_gemm_mxfp4": (i32, [ctypes.POINTER(fos_mxfp4_tensor), ctypes.POINTER(fos_mxfp4_tensor), vp, i64, vp,
+                                 vp]),
         "fos_linear_forward_workspace_size": (i32, [i64, i64, ctypes.POINTER(sz)]),
         "fos_linear_forward_operand": (i32, [i64, i64, vp, sz, ctypes.POINTER(fos_nvfp4_tensor)]),
         "fos_linear_forward": (i32, [vp, i64, i64, i64, ctypes.POINTER(fos_quant_options),
@@ -139,7 +154,8 @@ EXPORTED = ("fos_abi_version", "fos_status_string", "fos_sf_bytes", "fos_quantiz
             "fos_e4m3_encode", "fos_philox4x32_10", "fos_selftest_wait_limits", "fos_quantize_batch",
             "fos_quantize_batch_workspace_size", "fos_linear_backward", "fos_linear_backward_workspace_size",
             "fos_linear_backward_operands", "fos_linear_forward", "fos_linear_forward_workspace_size",
-            "fos_linear_forward_operand", "fos_quantize_mxfp4", "fos_dequantize_mxfp4", "fos_selftest_mma_rate")
+            "fos_linear_forward_operand", "fos_mxfp4_sf_bytes", "fos_quantize_mxfp4", "fos_dequantize_mxfp4",
+            "fos_gemm_mxfp4", "fos_selftest_mma_rate")
 
 
 def _check(status: int, what: str) -> None:
@@ -539,14 +555,23 @@ class LinearForward:
 # ------------------------------------------------------------------ MXFP4
 
 
-def fos_quantize_mxfp4(x, rows, cols, ld_x, scale_rule, codes, ld_codes, scales, choice, stream) -> int:
-    return int(_lib.fos_quantize_mxfp4(x or None, rows, cols, ld_x, scale_rule, codes or None, ld_codes,
+def fos_mxfp4_sf_bytes(rows: int, cols: int, sf_layout: int = FOS_SF_SWIZZLED_128x4) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.fos_mxfp4_sf_bytes(rows, cols, sf_layout, ctypes.byref(n)), "fos_mxfp4_sf_bytes")
+    return n.value
+
+
+def fos_quantize_mxfp4(x, rows, cols, ld_x, scale_rule, sf_layout, codes, ld_codes, scales, choice, stream) -> int:
+    return int(_lib.fos_quantize_mxfp4(x or None, rows, cols, ld_x, scale_rule, sf_layout, codes or None, ld_codes,
                                        scales or None, choice or None, stream))
 
 
-def fos_dequantize_mxfp4(codes, scales, rows, cols, ld_codes, out, out_dtype, ld_out, stream) -> int:
-    return int(_lib.fos_dequantize_mxfp4(codes or None, scales or None, rows, cols, ld_codes, out or None,
-                                         out_dtype, ld_out, stream))
+def fos_dequantize_mxfp4(q: fos_mxfp4_tensor, out, out_dtype, ld_out, stream) -> int:
+    return int(_lib.fos_dequantize_mxfp4(ctypes.byref(q), out or None, out_dtype, ld_out, stream))
+
+
+def fos_gemm_mxfp4(A: fos_mxfp4_tensor, B: fos_mxfp4_tensor, C, ldc, dev_status, stream) -> int:
+    return int(_lib.fos_gemm_mxfp4(ctypes.byref(A), ctypes.byref(B), C, ldc, dev_status or None, stream))
 
 
 @dataclass
@@ -554,25 +579,40 @@ class MXFP4Tensor:
     """Device buffers of one MXFP4 matrix (rows x cols values, 32-value blocks along cols)."""
 
     codes: "object"   # uint8 [rows, ld_codes]
-    scales: "object"  # uint8 [rows, cols/32], E8M0
+    scales: "object"  # uint8 E8M0: [rows, cols/32] (row-major) or flat fos_mxfp4_sf_bytes (swizzled)
     rows: int
     cols: int
+    sf_layout: int = FOS_SF_SWIZZLED_128x4
     choice: "object" = None  # uint8 [rows, cols/32] or None
 
+    def as_c(self) -> fos_mxfp4_tensor:
+        t = fos_mxfp4_tensor()
+        t.codes = self.codes.data_ptr()
+        t.sf = self.scales.data_ptr()
+        t.rows = self.rows
+        t.cols = self.cols
+        t.ld_codes = self.codes.stride(0) if self.codes.dim() == 2 else self.cols // 2
+        t.sf_layout = self.sf_layout
+        return t
 
-def quantize_mxfp4(x, *, scale_rule=FOS_SCALE_4OVER6, with_choice=False, stream=None) -> MXFP4Tensor:
+
+def quantize_mxfp4(x, *, scale_rule=FOS_SCALE_4OVER6, sf_layout=FOS_SF_SWIZZLED_128x4, with_choice=False,
+                   stream=None) -> MXFP4Tensor:
     """MXFP4 with the 4/6 choice of a bf16 [rows, cols] CUDA tensor (contiguous rows)."""
     torch = _torch()
     assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
     rows, cols = x.shape
     ldc = max(16, ((cols // 2 + 15) // 16) * 16)
-    out = MXFP4Tensor(codes=torch.empty((rows, ldc), dtype=torch.uint8, device=x.device),
-                      scales=torch.empty((rows, cols // 32), dtype=torch.uint8, device=x.device), rows=rows,
-                      cols=cols,
+    if sf_layout == FOS_SF_ROWMAJOR:
+        scales = torch.empty((rows, cols // 32), dtype=torch.uint8, device=x.device)
+    else:
+        scales = torch.empty(max(1, fos_mxfp4_sf_bytes(rows, cols, sf_layout)), dtype=torch.uint8, device=x.device)
+    out = MXFP4Tensor(codes=torch.empty((rows, ldc), dtype=torch.uint8, device=x.device), scales=scales, rows=rows,
+                      cols=cols, sf_layout=sf_layout,
                       choice=torch.empty((rows, cols // 32), dtype=torch.uint8, device=x.device) if with_choice
                       else None)
-    _check(fos_quantize_mxfp4(x.data_ptr(), rows, cols, x.stride(0), scale_rule, out.codes.data_ptr(), ldc,
-                              out.scales.data_ptr(), out.choice.data_ptr() if with_choice else 0,
+    _check(fos_quantize_mxfp4(x.data_ptr(), rows, cols, x.stride(0), scale_rule, sf_layout, out.codes.data_ptr(),
+                              ldc, out.scales.data_ptr(), out.choice.data_ptr() if with_choice else 0,
                               _stream_ptr(stream)), "fos_quantize_mxfp4")
     return out
 
@@ -582,6 +622,16 @@ def dequantize_mxfp4(q: MXFP4Tensor, dtype=None, stream=None):
     dtype = torch.float32 if dtype is None else dtype
     out = torch.empty((q.rows, q.cols), dtype=dtype, device=q.codes.device)
     code = FOS_DTYPE_BF16 if dtype == torch.bfloat16 else FOS_DTYPE_F32
-    _check(fos_dequantize_mxfp4(q.codes.data_ptr(), q.scales.data_ptr(), q.rows, q.cols, q.codes.stride(0),
-                                out.data_ptr(), code, q.cols, _stream_ptr(stream)), "fos_dequantize_mxfp4")
+    _check(fos_dequantize_mxfp4(q.as_c(), out.data_ptr(), code, q.cols, _stream_ptr(stream)),
+           "fos_dequantize_mxfp4")
+    return out
+
+
+def gemm_mxfp4(A: MXFP4Tensor, B: MXFP4Tensor, out=None, status=None, stream=None):
+    """C = A . B^T (bf16) from two MXFP4 operands quantized along K (swizzled scales)."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty((A.rows, B.rows), dtype=torch.bfloat16, device=A.codes.device)
+    _check(fos_gemm_mxfp4(A.as_c(), B.as_c(), out.data_ptr(), out.stride(0),
+                          status.data_ptr() if status is not None else 0, _stream_ptr(stream)), "fos_gemm_mxfp4")
     return out

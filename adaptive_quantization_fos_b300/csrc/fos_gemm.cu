@@ -21,6 +21,10 @@
 //               reads 32 accumulator lanes x 128 columns into registers, hands
 //               the accumulator back at once (so the next tile's MMAs start
 //               while it stores), scales, rounds to bf16 and stores.
+// The MXFP4 form (gemm_mxfp4_kernel) is the same kernel with E8M0 scales, one
+// per 32 values: its 512-byte scale chunks each span 128 values of K (two MMA
+// steps), and the staging warps give each 32-value scale to both 16-value
+// halves it covers, so the MMA reads the same tensor-memory scale image.
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel records
 // FOS_ERR_TIMEOUT, all roles stop, in-flight copies and MMAs are drained
 // (again bounded) and the tensor memory is freed before the CTA exits.
@@ -30,6 +34,7 @@
 
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "fos.h"
 
@@ -39,7 +44,7 @@ namespace {
 constexpr int kBM = 128;              // rows of A per tile (= tensor-memory lanes)
 constexpr int kBKBytes = 128;         // codes bytes per row per stage (256 values)
 constexpr int kKPerMma = 64;          // values of K per MMA
-constexpr int kSfChunk = 512;         // scale bytes of 128 rows x 64 values
+constexpr int kSfChunk = 512;         // scale bytes of 128 rows x 4 scales (64 NVFP4 / 128 MXFP4 values)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
 
@@ -73,7 +78,7 @@ struct GemmArgs {
   int64_t ldc;
   int32_t m, n, k;       // k in values
   int32_t tiles_m, tiles_n, num_kb;
-  int64_t sf_ktiles;     // 512-byte scale chunks per 128-row tile (= K / 64)
+  int64_t sf_ktiles;     // 512-byte scale chunks per 128-row tile (K / 64 NVFP4, ceil(K / 128) MXFP4)
   int32_t* status;
   uint64_t timeout_ns;
   int32_t stall_test;    // 1: the producer never fills a stage (bounded-wait self test)
@@ -161,9 +166,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 }
 
 // Instruction descriptor of kind::mxf4nvf4: E2M1 A and B (format 1), both
-// K-major, E4M3 scales (scale format 0), N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t mma_idesc(int m, int n) {
-  return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+// K-major, N >> 3 at bit 17, the scale format at bit 23 (0: E4M3, 1: E8M0),
+// M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t mma_idesc(int m, int n, bool e8m0 = false) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((e8m0 ? 1u : 0u) << 23) |
+         ((uint32_t)(m >> 4) << 24);
 }
 
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -212,6 +219,15 @@ __device__ __forceinline__ void tc_st16(uint32_t taddr, const uint4& a, const ui
 
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// E8M0 scale words of one MXFP4 chunk row (4 scales of 32 values) for the
+// MMA step `step` (0 or 1) of the two it spans: each 32-value scale serves
+// both 16-value quarters of the step it covers, [s0 s0 s1 s1] or [s2 s2 s3 s3].
+__device__ __forceinline__ uint4 mx_step_words(const uint4& w, int step) {
+  const uint32_t sel = step ? 0x3322u : 0x1100u;
+  return make_uint4(__byte_perm(w.x, 0u, sel), __byte_perm(w.y, 0u, sel), __byte_perm(w.z, 0u, sel),
+                    __byte_perm(w.w, 0u, sel));
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -235,11 +251,13 @@ __device__ __forceinline__ void raise_timeout(const GemmArgs& a, volatile int* a
 }
 
 // ------------------------------------------------------------------ kernel
-template <int BN>
-__global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
-    gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                      const GemmArgs args) {
+// MX: E8M0 scales per 32 values (MXFP4) instead of E4M3 per 16 (NVFP4).
+template <int BN, bool MX>
+__device__ __forceinline__ void gemm_body(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const GemmArgs& args) {
   using C = Cfg<BN>;
+  // 512-byte scale chunks per 128 rows per stage, and those a stage of kkc MMA steps uses
+  constexpr int kChunksPerStage = MX ? 2 : 4;
+  auto n_chunks = [](int kkc) { return MX ? (kkc + 1) >> 1 : kkc; };
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
@@ -306,23 +324,24 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         for (int h = 0; h < BN / 128; ++h)
           if ((nb * (BN / 128) + h) * 128 < args.n) ++halves;
         for (int kb = 0; kb < pre; ++kb) {
-          const int kkc = min(4, kmma_total - 4 * kb);
+          const int nch = n_chunks(min(4, kmma_total - 4 * kb));
           const uint32_t st = smem_u32(smem + kb * C::kStageBytes);
           const uint32_t sfa_dst = st + C::kABytes + C::kBBytes;
-          mbar_expect_tx(sf_full(kb), (1 + halves) * kkc * kSfChunk);
+          mbar_expect_tx(sf_full(kb), (1 + halves) * nch * kSfChunk);
           for (int h = 0; h < halves; ++h)
             bulk_load(sfa_dst + C::kSfaBytes + h * 4 * kSfChunk,
-                      args.sfb + ((int64_t)(nb * (BN / 128) + h) * args.sf_ktiles + 4 * kb) * kSfChunk,
-                      kkc * kSfChunk, sf_full(kb));
+                      args.sfb + ((int64_t)(nb * (BN / 128) + h) * args.sf_ktiles + kChunksPerStage * kb) * kSfChunk,
+                      nch * kSfChunk, sf_full(kb));
           mbar_expect_tx(full_bar(kb), C::kABytes + C::kBBytes);
           tma_load_2d(st + C::kABytes, &tm_b, kb * kBKBytes, nb * BN, full_bar(kb));
         }
         pdl_wait();
         for (int kb = 0; kb < pre; ++kb) {
-          const int kkc = min(4, kmma_total - 4 * kb);
+          const int nch = n_chunks(min(4, kmma_total - 4 * kb));
           const uint32_t st = smem_u32(smem + kb * C::kStageBytes);
-          bulk_load(st + C::kABytes + C::kBBytes, args.sfa + ((int64_t)mb * args.sf_ktiles + 4 * kb) * kSfChunk,
-                    kkc * kSfChunk, sf_full(kb));
+          bulk_load(st + C::kABytes + C::kBBytes,
+                    args.sfa + ((int64_t)mb * args.sf_ktiles + kChunksPerStage * kb) * kSfChunk, nch * kSfChunk,
+                    sf_full(kb));
           tma_load_2d(st, &tm_a, kb * kBKBytes, mb * kBM, full_bar(kb));
           ++issued;
         }
@@ -338,7 +357,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
             break;
           }
           if (!args.stall_test) {
-            const int kkc = min(4, kmma_total - 4 * kb);
+            const int nch = n_chunks(min(4, kmma_total - 4 * kb));
             int halves = 0;
             for (int h = 0; h < BN / 128; ++h)
               if ((nb * (BN / 128) + h) * 128 < args.n) ++halves;
@@ -346,13 +365,14 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
             // the small scale copies first, on their own barrier, so the
             // scales reach tensor memory while the code tiles are in flight
             const uint32_t sfa_dst = st + C::kABytes + C::kBBytes;
-            mbar_expect_tx(sf_full(s), (1 + halves) * kkc * kSfChunk);
-            bulk_load(sfa_dst, args.sfa + ((int64_t)mb * args.sf_ktiles + 4 * kb) * kSfChunk, kkc * kSfChunk,
-                      sf_full(s));
+            mbar_expect_tx(sf_full(s), (1 + halves) * nch * kSfChunk);
+            bulk_load(sfa_dst, args.sfa + ((int64_t)mb * args.sf_ktiles + kChunksPerStage * kb) * kSfChunk,
+                      nch * kSfChunk, sf_full(s));
             for (int h = 0; h < halves; ++h)
               bulk_load(sfa_dst + C::kSfaBytes + h * 4 * kSfChunk,
-                        args.sfb + ((int64_t)(nb * (BN / 128) + h) * args.sf_ktiles + 4 * kb) * kSfChunk,
-                        kkc * kSfChunk, sf_full(s));
+                        args.sfb + ((int64_t)(nb * (BN / 128) + h) * args.sf_ktiles + kChunksPerStage * kb) *
+                                       kSfChunk,
+                        nch * kSfChunk, sf_full(s));
             mbar_expect_tx(full_bar(s), C::kABytes + C::kBBytes);
             tma_load_2d(st, &tm_a, kb * kBKBytes, mb * kBM, full_bar(s));
             tma_load_2d(st + C::kABytes, &tm_b, kb * kBKBytes, nb * BN, full_bar(s));
@@ -380,7 +400,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = mma_idesc(kBM, BN);
+      constexpr uint32_t idesc = mma_idesc(kBM, BN, MX);
       const uint32_t acc = tmem;
       int s = 0;
       uint32_t ph = 0, acc_ph = 0;
@@ -440,7 +460,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16) + 128 * h;
     const uint32_t quad = (uint32_t)(32 * q) << 16;
     pdl_wait();  // A's tensor scale comes from the previous kernel under programmatic launch
-    const float alpha = __fmul_rn(__ldcg(args.sta), __ldcg(args.stb));
+    const float alpha = MX ? 1.0f : __fmul_rn(__ldcg(args.sta), __ldcg(args.stb));
     uint32_t acc_ph = 0;
     // scale-staging cursor: the next stage (tile, k block) in this CTA's sequence
     int sf_s = 0, sf_t = blockIdx.x, sf_kb = 0;
@@ -463,7 +483,23 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       const uint32_t st = smem_u32(smem + sf_s * C::kStageBytes);
       const uint32_t sfa_s = st + C::kABytes + C::kBBytes + 16u * lane, sfb_s = sfa_s + C::kSfaBytes;
       const uint32_t sf_col = tmem + quad + BN + sf_s * C::kSfStageCols;
-      if (BN == 256) {
+      if (MX) {
+        // one chunk spans two K steps: this warp (256-column tiles) stages
+        // steps 2h, 2h+1 from chunk h, a 128-column tile all four from chunks 0, 1
+        if (BN == 256) {
+          const uint4 a = lds128(sfa_s + h * kSfChunk), b0 = lds128(sfb_s + h * kSfChunk),
+                      b1 = lds128(sfb_s + 4 * kSfChunk + h * kSfChunk);
+          tc_st8(sf_col + 8 * h, mx_step_words(a, 0), mx_step_words(a, 1));
+          tc_st16(sf_col + 16 + 16 * h, mx_step_words(b0, 0), mx_step_words(b1, 0), mx_step_words(b0, 1),
+                  mx_step_words(b1, 1));
+        } else {
+          const uint4 a0 = lds128(sfa_s), a1 = lds128(sfa_s + kSfChunk), b0 = lds128(sfb_s),
+                      b1 = lds128(sfb_s + kSfChunk);
+          tc_st16(sf_col, mx_step_words(a0, 0), mx_step_words(a0, 1), mx_step_words(a1, 0), mx_step_words(a1, 1));
+          tc_st16(sf_col + 16, mx_step_words(b0, 0), mx_step_words(b0, 1), mx_step_words(b1, 0),
+                  mx_step_words(b1, 1));
+        }
+      } else if (BN == 256) {
         // this warp: K steps 2h, 2h+1 of A (columns 8h..8h+7) and of both B halves
         // (columns 16+16h .. 16+16h+15: [B0 k][B1 k][B0 k+1][B1 k+1])
         const uint32_t k0 = 2u * h;
@@ -570,6 +606,20 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   }
 }
 
+template <int BN>
+__global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
+    gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                      const __grid_constant__ GemmArgs args) {
+  gemm_body<BN, false>(tm_a, tm_b, args);
+}
+
+template <int BN>
+__global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
+    gemm_mxfp4_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                      const __grid_constant__ GemmArgs args) {
+  gemm_body<BN, true>(tm_a, tm_b, args);
+}
+
 // ------------------------------------------------- tensor-pipe rate probe
 // The MMA instruction of the GEMM (kind::mxf4nvf4, E4M3 scales per 16 values,
 // M = 128, N = BN, K = 64) issued `iters` x 4 times back to back by one
@@ -647,14 +697,32 @@ namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-bool valid_operand(const fos_nvfp4_tensor* t) {
-  if (!t || !t->codes || !t->sf || !t->tensor_scale) return false;
-  if (t->rows < 0 || t->rows > INT32_MAX || t->cols <= 0 || t->cols % kKPerMma != 0 || t->cols > INT32_MAX)
-    return false;
-  if (t->ld_codes < t->cols / 2 || t->ld_codes % 16 != 0 || !aligned(t->codes, 16) || !aligned(t->sf, 16))
-    return false;
-  return t->sf_layout == FOS_SF_SWIZZLED_128x4;
+// One FP4 operand of either format (tensor_scale null for MXFP4).
+struct Operand {
+  const uint8_t* codes;
+  const uint8_t* sf;
+  const float* tensor_scale;
+  int64_t rows, cols, ld_codes;
+};
+
+bool valid_codes_and_scales(const uint8_t* codes, const uint8_t* sf, int64_t rows, int64_t cols, int64_t ld_codes,
+                            int32_t sf_layout) {
+  if (!codes || !sf) return false;
+  if (rows < 0 || rows > INT32_MAX || cols <= 0 || cols % kKPerMma != 0 || cols > INT32_MAX) return false;
+  if (ld_codes < cols / 2 || ld_codes % 16 != 0 || !aligned(codes, 16) || !aligned(sf, 16)) return false;
+  return sf_layout == FOS_SF_SWIZZLED_128x4;
 }
+
+bool valid_operand(const fos_nvfp4_tensor* t) {
+  return t && t->tensor_scale && valid_codes_and_scales(t->codes, t->sf, t->rows, t->cols, t->ld_codes, t->sf_layout);
+}
+
+bool valid_operand(const fos_mxfp4_tensor* t) {
+  return t && valid_codes_and_scales(t->codes, t->sf, t->rows, t->cols, t->ld_codes, t->sf_layout);
+}
+
+Operand operand(const fos_nvfp4_tensor* t) { return {t->codes, t->sf, t->tensor_scale, t->rows, t->cols, t->ld_codes}; }
+Operand operand(const fos_mxfp4_tensor* t) { return {t->codes, t->sf, nullptr, t->rows, t->cols, t->ld_codes}; }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -693,30 +761,30 @@ int sm_count() {
   return n > 0 ? n : 148;
 }
 
-template <int BN>
-fos_status launch_gemm(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* Cout, int64_t ldc,
-                       int32_t* dev_status, uint64_t timeout_ns, int stall_test, int grid_cap, bool pdl,
-                       cudaStream_t stream) {
+template <int BN, bool MX>
+fos_status launch_gemm(const Operand& A, const Operand& B, void* Cout, int64_t ldc, int32_t* dev_status,
+                       uint64_t timeout_ns, int stall_test, int grid_cap, bool pdl, cudaStream_t stream) {
   using C = Cfg<BN>;
   CUtensorMap ta, tb;
-  const int64_t kbytes = A->cols / 2;
-  if (!make_codes_map(&ta, A->codes, A->rows, kbytes, A->ld_codes, kBM) ||
-      !make_codes_map(&tb, B->codes, B->rows, kbytes, B->ld_codes, BN))
+  const int64_t kbytes = A.cols / 2;
+  if (!make_codes_map(&ta, A.codes, A.rows, kbytes, A.ld_codes, kBM) ||
+      !make_codes_map(&tb, B.codes, B.rows, kbytes, B.ld_codes, BN))
     return FOS_ERR_CUDA;
   GemmArgs a{};
-  a.sfa = A->sf;
-  a.sfb = B->sf;
-  a.sta = A->tensor_scale;
-  a.stb = B->tensor_scale;
+  a.sfa = A.sf;
+  a.sfb = B.sf;
+  a.sta = A.tensor_scale;
+  a.stb = B.tensor_scale;
   a.c = static_cast<uint16_t*>(Cout);
   a.ldc = ldc;
-  a.m = (int32_t)A->rows;
-  a.n = (int32_t)B->rows;
-  a.k = (int32_t)A->cols;
-  a.tiles_m = (int32_t)((A->rows + kBM - 1) / kBM);
-  a.tiles_n = (int32_t)((B->rows + BN - 1) / BN);
-  a.num_kb = (int32_t)((A->cols + 255) / 256);
-  a.sf_ktiles = A->cols / kKPerMma;
+  a.m = (int32_t)A.rows;
+  a.n = (int32_t)B.rows;
+  a.k = (int32_t)A.cols;
+  a.tiles_m = (int32_t)((A.rows + kBM - 1) / kBM);
+  a.tiles_n = (int32_t)((B.rows + BN - 1) / BN);
+  a.num_kb = (int32_t)((A.cols + 255) / 256);
+  // scale chunks of 4 scales per 128-row tile: 64 values each (NVFP4) or 128 (MXFP4, the last one padded)
+  a.sf_ktiles = MX ? (A.cols + 127) / 128 : A.cols / kKPerMma;
   a.status = dev_status;
   a.timeout_ns = timeout_ns;
   a.stall_test = stall_test;
@@ -725,8 +793,8 @@ fos_status launch_gemm(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, voi
   int grid = sm_count();
   if (grid_cap > 0 && grid > grid_cap) grid = grid_cap;
   if (grid > tiles) grid = (int)tiles;
-  if (cudaFuncSetAttribute(gemm_nvfp4_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
-      cudaSuccess)
+  const auto kernel = MX ? gemm_mxfp4_kernel<BN> : gemm_nvfp4_kernel<BN>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
     return FOS_ERR_CUDA;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)grid);
@@ -738,20 +806,23 @@ fos_status launch_gemm(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, voi
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gemm_nvfp4_kernel<BN>, ta, tb, a) == cudaSuccess ? FOS_OK : FOS_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, kernel, ta, tb, a) == cudaSuccess ? FOS_OK : FOS_ERR_CUDA;
 }
 
-fos_status gemm_checked(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* C, int64_t ldc,
-                        int32_t* dev_status, uint64_t timeout_ns, int stall_test, bool pdl, cudaStream_t stream) {
+template <typename T>
+fos_status gemm_checked(const T* A, const T* B, void* C, int64_t ldc, int32_t* dev_status, uint64_t timeout_ns,
+                        int stall_test, bool pdl, cudaStream_t stream) {
+  constexpr bool MX = std::is_same<T, fos_mxfp4_tensor>::value;
   if (!valid_operand(A) || !valid_operand(B) || !C) return FOS_ERR_INVALID_ARG;
   if (A->cols != B->cols || B->rows % 8 != 0) return FOS_ERR_INVALID_ARG;
   if (ldc < B->rows || ldc % 8 != 0 || !aligned(C, 16)) return FOS_ERR_INVALID_ARG;
   if (dev_status && !aligned(dev_status, 4)) return FOS_ERR_INVALID_ARG;
   if (A->rows == 0 || B->rows == 0) return FOS_OK;
+  const Operand a = operand(A), b = operand(B);
   // 256-column tiles unless the last one would be half empty
   if (B->rows % 256 == 0 || B->rows % 256 > 128)
-    return launch_gemm<256>(A, B, C, ldc, dev_status, timeout_ns, stall_test, 0, pdl, stream);
-  return launch_gemm<128>(A, B, C, ldc, dev_status, timeout_ns, stall_test, 0, pdl, stream);
+    return launch_gemm<256, MX>(a, b, C, ldc, dev_status, timeout_ns, stall_test, 0, pdl, stream);
+  return launch_gemm<128, MX>(a, b, C, ldc, dev_status, timeout_ns, stall_test, 0, pdl, stream);
 }
 
 }  // namespace
@@ -767,7 +838,7 @@ fos_status gemm_stall_selftest(void* scratch, size_t scratch_bytes, uint64_t tim
   fos_nvfp4_tensor B{b + 16384, b + 34816, reinterpret_cast<float*>(b + 36864), 128, 256, 128,
                      FOS_SF_SWIZZLED_128x4, 0};
   if (cudaMemsetAsync(b, 0, 40960, s) != cudaSuccess) return FOS_ERR_CUDA;
-  return launch_gemm<128>(&A, &B, b + 40960, 128, status, timeout_ns, 1, 1, false, s);
+  return launch_gemm<128, false>(operand(&A), operand(&B), b + 40960, 128, status, timeout_ns, 1, 1, false, s);
 }
 
 fos_status gemm_after_producer_of_a(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* C, int64_t ldc,
@@ -794,5 +865,10 @@ extern "C" fos_status fos_selftest_mma_rate(int32_t n_cols, int64_t iters, int32
 
 extern "C" fos_status fos_gemm(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* C, int64_t ldc,
                                int32_t* dev_status, cudaStream_t stream) {
+  return gemm_checked(A, B, C, ldc, dev_status, kDefaultTimeoutNs, 0, false, stream);
+}
+
+extern "C" fos_status fos_gemm_mxfp4(const fos_mxfp4_tensor* A, const fos_mxfp4_tensor* B, void* C, int64_t ldc,
+                                     int32_t* dev_status, cudaStream_t stream) {
   return gemm_checked(A, B, C, ldc, dev_status, kDefaultTimeoutNs, 0, false, stream);
 }

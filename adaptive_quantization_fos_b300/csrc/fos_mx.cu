@@ -14,6 +14,9 @@
 //
 // No tensor scale means no amax pass: one launch reads each value once.  One
 // thread owns one 32-value block (64 contiguous bytes; a warp reads 2 KB).
+// Scales go row-major or into the 128x4 tiles the block-scaled MMA reads
+// (one tile: 128 rows x 4 scales = 128 values of K); the same launch zeroes
+// the tiles' pad bytes.
 #include <cuda_runtime.h>
 
 #include <cfloat>
@@ -37,10 +40,32 @@ struct MxParams {
   int64_t rows, cols, ld;  // cols % 32 == 0
   uint8_t* codes;
   int64_t ld_codes;
-  uint8_t* scales;  // [rows][cols / 32]
-  uint8_t* choice;  // optional, same shape
+  uint8_t* scales;  // [rows][cols / 32] or 128x4 tiles over cols / 32 scale columns
+  uint8_t* choice;  // optional, [rows][cols / 32]
   int codes16;      // codes 16-byte aligned with ld_codes % 16 == 0
+  int layout;       // fos_sf_layout
 };
+
+// Zero the pad bytes of a 128x4-tiled scale buffer of R rows and nb scale
+// columns: rows R .. pad128(R)-1 of every padded column, then columns
+// nb .. pad4(nb)-1 of the real rows.  Grid-stride over the pad bytes only.
+__device__ __forceinline__ void zero_sf_pads(uint8_t* sf, int64_t R, int64_t nb) {
+  const int64_t nbp = (nb + 3) & ~int64_t(3), Rp = (R + 127) & ~int64_t(127);
+  const int64_t n_rows_pad = (Rp - R) * nbp, n_cols_pad = R * (nbp - nb);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_rows_pad + n_cols_pad; i += stride) {
+    int64_t r, c;
+    if (i < n_rows_pad) {
+      r = R + i / nbp;
+      c = i - (r - R) * nbp;
+    } else {
+      const int64_t j = i - n_rows_pad, w = nbp - nb;
+      r = j / w;
+      c = nb + (j - r * w);
+    }
+    sf[sf_off(r, c, nb, 0)] = 0;
+  }
+}
 
 // max |x| of 16 bf16 values held as 8 words, NaN-propagating: a NaN input
 // gives NaN, an infinity gives infinity (the sign bit of the bf16 maxima is
@@ -89,6 +114,7 @@ template <int RULE>
 __global__ void __launch_bounds__(256) quant_mx_kernel(MxParams p) {
   const int64_t nb = p.cols >> 5;
   const int64_t n = p.rows * nb;
+  if (p.layout == FOS_SF_SWIZZLED_128x4) zero_sf_pads(p.scales, p.rows, nb);
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = t / nb, b = t - r * nb;
     const uint4* src = reinterpret_cast<const uint4*>(p.x + r * p.ld + b * 32);
@@ -132,7 +158,7 @@ __global__ void __launch_bounds__(256) quant_mx_kernel(MxParams p) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) reinterpret_cast<uint32_t*>(dst)[k] = c[k];
     }
-    p.scales[t] = finite ? (uint8_t)((four ? X4 : X6) + 127) : (uint8_t)0xFF;
+    p.scales[sf_off(r, b, nb, p.layout)] = finite ? (uint8_t)((four ? X4 : X6) + 127) : (uint8_t)0xFF;
     if (p.choice) p.choice[t] = four ? 1 : 0;
   }
 }
@@ -142,6 +168,7 @@ struct MxDequantParams {
   const uint8_t* scales;
   int64_t rows, cols, ld_codes, ld_out;
   void* out;
+  int layout;
 };
 
 // x_hat = g * 2^X (exact in FP32; bf16 output is that value rounded to
@@ -152,7 +179,7 @@ __global__ void __launch_bounds__(256) dequant_mx_kernel(MxDequantParams p) {
   const int64_t n = p.rows * nb;
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = t / nb, b = t - r * nb;
-    const int X = (int)p.scales[t] - 127;
+    const int X = (int)p.scales[sf_off(r, b, nb, p.layout)] - 127;
     // 2^X: normal for X >= -126; 2^-127 is the subnormal 0x00400000; byte
     // 0xFF is the NaN scale (every value of the block NaN)
     const float s = X == 128 ? __uint_as_float(0x7FC00000u)
@@ -190,12 +217,22 @@ bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>
 
 extern "C" {
 
+fos_status fos_mxfp4_sf_bytes(int64_t rows, int64_t cols, int32_t sf_layout, size_t* bytes) {
+  if (!bytes || rows < 0 || cols < 0 || cols % 32 != 0) return FOS_ERR_INVALID_ARG;
+  if (sf_layout != FOS_SF_SWIZZLED_128x4 && sf_layout != FOS_SF_ROWMAJOR) return FOS_ERR_INVALID_ARG;
+  const int64_t nb = cols / 32;
+  *bytes = sf_layout == FOS_SF_ROWMAJOR ? (size_t)(rows * nb)
+                                        : (size_t)(((rows + 127) / 128) * 128 * ((nb + 3) / 4) * 4);
+  return FOS_OK;
+}
+
 fos_status fos_quantize_mxfp4(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int32_t scale_rule,
-                              uint8_t* codes, int64_t ld_codes, uint8_t* scales, uint8_t* choice,
-                              cudaStream_t stream) {
+                              int32_t sf_layout, uint8_t* codes, int64_t ld_codes, uint8_t* scales,
+                              uint8_t* choice, cudaStream_t stream) {
   using fos::aligned;
   if (rows < 0 || cols < 0 || cols % 32 != 0 || ld_x < cols || ld_x % 8 != 0) return FOS_ERR_INVALID_ARG;
   if (scale_rule < FOS_SCALE_4OVER6 || scale_rule > FOS_SCALE_4) return FOS_ERR_INVALID_ARG;
+  if (sf_layout != FOS_SF_SWIZZLED_128x4 && sf_layout != FOS_SF_ROWMAJOR) return FOS_ERR_INVALID_ARG;
   if (rows == 0 || cols == 0) return FOS_OK;
   if (!x || !aligned(x, 16) || !codes || !scales) return FOS_ERR_INVALID_ARG;
   if (ld_codes < cols / 2 || ld_codes % 4 != 0 || !aligned(codes, 4)) return FOS_ERR_INVALID_ARG;
@@ -209,6 +246,7 @@ fos_status fos_quantize_mxfp4(const void* x, int64_t rows, int64_t cols, int64_t
   p.scales = scales;
   p.choice = choice;
   p.codes16 = aligned(codes, 16) && ld_codes % 16 == 0;
+  p.layout = sf_layout;
   const int g = fos::mx_grid(rows * (cols / 32));
   switch (scale_rule) {
     case FOS_SCALE_6: fos::quant_mx_kernel<FOS_SCALE_6><<<g, 256, 0, stream>>>(p); break;
@@ -218,16 +256,17 @@ fos_status fos_quantize_mxfp4(const void* x, int64_t rows, int64_t cols, int64_t
   return cudaGetLastError() == cudaSuccess ? FOS_OK : FOS_ERR_CUDA;
 }
 
-fos_status fos_dequantize_mxfp4(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t cols,
-                                int64_t ld_codes, void* out, int32_t out_dtype, int64_t ld_out,
+fos_status fos_dequantize_mxfp4(const fos_mxfp4_tensor* q, void* out, int32_t out_dtype, int64_t ld_out,
                                 cudaStream_t stream) {
-  if (rows < 0 || cols < 0 || cols % 32 != 0 || ld_codes < cols / 2 || ld_out < cols) return FOS_ERR_INVALID_ARG;
+  if (!q || q->rows < 0 || q->cols < 0 || q->cols % 32 != 0 || q->ld_codes < q->cols / 2 || ld_out < q->cols)
+    return FOS_ERR_INVALID_ARG;
+  if (q->sf_layout != FOS_SF_SWIZZLED_128x4 && q->sf_layout != FOS_SF_ROWMAJOR) return FOS_ERR_INVALID_ARG;
   if (out_dtype != FOS_DTYPE_F32 && out_dtype != FOS_DTYPE_BF16) return FOS_ERR_INVALID_ARG;
-  if (rows == 0 || cols == 0) return FOS_OK;
-  if (!codes || !scales || !out) return FOS_ERR_INVALID_ARG;
+  if (q->rows == 0 || q->cols == 0) return FOS_OK;
+  if (!q->codes || !q->sf || !out) return FOS_ERR_INVALID_ARG;
   if (!fos::aligned(out, out_dtype == FOS_DTYPE_F32 ? 4 : 2)) return FOS_ERR_INVALID_ARG;
-  fos::MxDequantParams p{codes, scales, rows, cols, ld_codes, ld_out, out};
-  const int g = fos::mx_grid(rows * (cols / 32));
+  fos::MxDequantParams p{q->codes, q->sf, q->rows, q->cols, q->ld_codes, ld_out, out, q->sf_layout};
+  const int g = fos::mx_grid(q->rows * (q->cols / 32));
   if (out_dtype == FOS_DTYPE_BF16)
     fos::dequant_mx_kernel<true><<<g, 256, 0, stream>>>(p);
   else

@@ -666,9 +666,21 @@ def linear_forward(torch, fos, dev, pk) -> dict:
     tf = flops / (t * 1e-3) / 1e12
     fp4_peak = pk["bf16_tflops"] * 6.0  # measured bf16 burst x nominal dense fp4/bf16 ratio (13.5 / 2.25)
     rate = mma_rate(torch, fos, dev)
+    # the same contraction from MXFP4 operands (E8M0 scales per 32 values)
+    am, wm = fos.quantize_mxfp4(A), fos.quantize_mxfp4(W)
+    try:
+        fos.gemm_mxfp4(am, wm, out=C)
+        with ClockSampler(dev.index) as clk_mx:
+            t_mx = _time_calls(torch, lambda: fos.gemm_mxfp4(am, wm, out=C), 50)
+        tf_mx = flops / (t_mx * 1e-3) / 1e12
+        mx = {"gemm_ms": round(t_mx, 4), "tflops": round(tf_mx, 1), "clocks": clk_mx.summary(),
+              "frac_of_mma_rate": round(tf_mx / rate["n256"]["tflops"], 4) if rate.get("n256") else None}
+    except fos.FosError as e:
+        mx = {"status": f"gemm_mxfp4 unavailable: {e}"}
     return {"gemm_ms": round(t, 4), "tflops": round(tf, 1), "clocks": clk.summary(),
             "mma_rate_probe": rate,
             "frac_of_mma_rate": round(tf / rate["n256"]["tflops"], 4) if rate.get("n256") else None,
+            "gemm_mxfp4": mx,
             "layer_forward_ms": round(t_layer, 4), "layer_forward_tflops": round(flops / (t_layer * 1e-3) / 1e12, 1),
             "quantize_then_gemm_ms": round(t_two, 4),
             "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
@@ -807,6 +819,15 @@ def run_case(args) -> None:
         C = torch.empty((8192, 12288), dtype=torch.bfloat16, device=dev)
         for _ in range(3):
             fos.gemm(a, w, out=C)
+    elif args.case == "gemm_mx":
+        # the same contraction from MXFP4 operands
+        A = _to_dev(torch, workloads.activations(8192, 4096, seed=5001), dev)
+        W = _to_dev(torch, workloads.student_t(12288, 4096, seed=5002), dev)
+        a = fos.quantize_mxfp4(A)
+        w = fos.quantize_mxfp4(W)
+        C = torch.empty((8192, 12288), dtype=torch.bfloat16, device=dev)
+        for _ in range(3):
+            fos.gemm_mxfp4(a, w, out=C)
     else:
         raise SystemExit(f"unknown case {args.case}")
     torch.cuda.synchronize()

@@ -21,9 +21,10 @@
  *            of stride 1,2,4,8; s_j = 1-2*bit_j of word 0 of
  *            Philox4x32-10(counter (0,0,0,1), key = hadamard_seed)).
  *   s_t    = amax / 2688 (= 6*448), amax = max|y| over the tensor.
- *   k_M    = 1 / (M*s_t) for M in {6, 4}, once per tensor.
+ *   t_M    = M*s_t rounded to FP32, for M in {6, 4}, once per tensor.
  *   per block (16 values, or a 16x16 tile): a = max|y|;
- *   sf_M   = E4M3_rne_satfinite(a * k_M);  eff_M = float(sf_M) * s_t;
+ *   sf_M   = E4M3_rne_satfinite(a / t_M), the quotient correctly rounded to
+ *            FP32 (the block maximum mapped to M);  eff_M = float(sf_M) * s_t;
  *   q      = y * min(1/eff_M, FLT_MAX);  code = E2M1(q) (RNE, or stochastic:
  *            round up iff ((w >> 8) * 2^-24) < p, w = word (i mod 4) of
  *            Philox4x32-10(counter (lo32(i/4), hi32(i/4), 0, 0), key = sr_seed),
@@ -54,7 +55,7 @@
 extern "C" {
 #endif
 
-#define FOS_ABI_VERSION 1
+#define FOS_ABI_VERSION 2
 
 typedef enum fos_status {
   FOS_OK = 0,
@@ -250,6 +251,23 @@ fos_status fos_gemm(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* 
 
 /* ---- MXFP4 with the 4/6 choice ---- */
 
+/* An MXFP4 matrix: rows x cols values, 32-value blocks along cols, one E8M0
+ * scale byte per block and no tensor scale. */
+typedef struct fos_mxfp4_tensor {
+  const uint8_t* codes; /* device: rows x ld_codes bytes, 2 codes per byte, even column in the low nibble */
+  const uint8_t* sf;    /* device: E8M0 block scales in sf_layout, cols/32 scale columns */
+  int64_t rows;
+  int64_t cols;         /* multiple of 32 */
+  int64_t ld_codes;     /* bytes between rows, >= cols/2 */
+  int32_t sf_layout;    /* fos_sf_layout over the cols/32 scale columns */
+  int32_t reserved;
+} fos_mxfp4_tensor;
+
+/* Bytes of an MXFP4 scale buffer for rows x cols values (cols % 32 == 0):
+ * rows * cols/32 row-major, or the 128x4 tiles of FOS_SF_SWIZZLED_128x4 over
+ * cols/32 scale columns (one tile spans 128 rows x 128 values). */
+fos_status fos_mxfp4_sf_bytes(int64_t rows, int64_t cols, int32_t sf_layout, size_t* bytes);
+
 /*
  * fos_quantize_mxfp4 -- MXFP4 ("FP4" glossary page: 32 values under one 8-bit
  * power-of-two scale; E8M0 and the shared exponent as in the OCP
@@ -269,22 +287,41 @@ fos_status fos_gemm(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* 
  * pass: one launch.
  *   x         device bf16 [rows][ld_x], 16-byte aligned, ld_x % 8 == 0,
  *             cols % 32 == 0.
+ *   sf_layout FOS_SF_ROWMAJOR ([rows][cols/32]) or FOS_SF_SWIZZLED_128x4
+ *             (the layout fos_gemm_mxfp4 reads; pad bytes are written 0).
  *   codes     device [rows][ld_codes] bytes, ld_codes >= cols/2, % 4 == 0,
  *             4-byte aligned (16-byte aligned rows are stored 16 bytes at a time).
- *   scales    device [rows][cols/32] E8M0 bytes; choice optional, same shape,
- *             1 where the block kept the 4-candidate.
+ *   scales    device, fos_mxfp4_sf_bytes(rows, cols, sf_layout) bytes;
+ *             choice optional, [rows][cols/32], 1 where the block kept the
+ *             4-candidate.
  *   scale_rule FOS_SCALE_4OVER6, or FOS_SCALE_6 / FOS_SCALE_4 to force one.
  */
 fos_status fos_quantize_mxfp4(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int32_t scale_rule,
-                              uint8_t* codes, int64_t ld_codes, uint8_t* scales, uint8_t* choice,
-                              cudaStream_t stream);
+                              int32_t sf_layout, uint8_t* codes, int64_t ld_codes, uint8_t* scales,
+                              uint8_t* choice, cudaStream_t stream);
 
 /* fos_dequantize_mxfp4 -- x_hat = g * 2^(byte - 127), exact in FP32;
  * FOS_DTYPE_BF16 output is that value rounded to nearest even.
- * out: device [rows][ld_out] elements, ld_out >= cols. */
-fos_status fos_dequantize_mxfp4(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t cols,
-                                int64_t ld_codes, void* out, int32_t out_dtype, int64_t ld_out,
+ * out: device [q->rows][ld_out] elements, ld_out >= q->cols. */
+fos_status fos_dequantize_mxfp4(const fos_mxfp4_tensor* q, void* out, int32_t out_dtype, int64_t ld_out,
                                 cudaStream_t stream);
+
+/*
+ * fos_gemm_mxfp4 -- C = sum_k (gA * 2^XA)(gB * 2^XB): the contraction of two
+ * MXFP4 operands A [M,K] and B [N,K], both quantized along K, with FP32
+ * accumulation on the tensor cores ("FP4", "FP4 ile Çıkarım ve Eğitim":
+ * FP4 products accumulate at higher precision) and bf16 output.  The same
+ * block-scaled MMA as fos_gemm with E8M0 scales; each 32-value scale serves
+ * both 16-value halves of its block, so the product is exactly that of the
+ * dequantized operands up to the FP32 accumulation.
+ *   A, B      the same K, K % 64 == 0; FOS_SF_SWIZZLED_128x4 scales
+ *             (fos_quantize_mxfp4), 16-byte aligned; codes 16-byte aligned
+ *             with ld_codes % 16 == 0.  M any size >= 0; N % 8 == 0.
+ *   C         device bf16 [M][ldc], ldc >= N, ldc % 8 == 0, 16-byte aligned.
+ *   dev_status optional device int32, as for fos_gemm.
+ */
+fos_status fos_gemm_mxfp4(const fos_mxfp4_tensor* A, const fos_mxfp4_tensor* B, void* C, int64_t ldc,
+                          int32_t* dev_status, cudaStream_t stream);
 
 /* ---- quantized linear backward ---- */
 

@@ -38,21 +38,22 @@ def test_struct_layout_matches_header(fos, tmp_path):
     src = tmp_path / "layout.c"
     src.write_text(
         '#include <stdio.h>\n#include <stddef.h>\n#include "fos.h"\n'
-        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu\\n\", sizeof(fos_quant_options),"
+        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu %zu %zu %zu\\n\", sizeof(fos_quant_options),"
         " offsetof(fos_quant_options, sr_seed), offsetof(fos_quant_options, tensor_amax),"
-        " sizeof(fos_nvfp4_tensor), offsetof(fos_nvfp4_tensor, rows), offsetof(fos_nvfp4_tensor, sf_layout));"
+        " sizeof(fos_nvfp4_tensor), offsetof(fos_nvfp4_tensor, rows), offsetof(fos_nvfp4_tensor, sf_layout),"
+        " sizeof(fos_mxfp4_tensor), offsetof(fos_mxfp4_tensor, rows), offsetof(fos_mxfp4_tensor, sf_layout));"
         "return 0;}\n")
     exe = tmp_path / "layout"
     subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), "-I", "/usr/local/cuda/include", str(src),
                            "-o", str(exe)])
     got = [int(v) for v in subprocess.check_output([str(exe)]).split()]
-    O, T = fos.fos_quant_options, fos.fos_nvfp4_tensor
+    O, T, X = fos.fos_quant_options, fos.fos_nvfp4_tensor, fos.fos_mxfp4_tensor
     assert got == [ctypes.sizeof(O), O.sr_seed.offset, O.tensor_amax.offset, ctypes.sizeof(T), T.rows.offset,
-                   T.sf_layout.offset]
+                   T.sf_layout.offset, ctypes.sizeof(X), X.rows.offset, X.sf_layout.offset]
 
 
 def test_version_and_sizes(fos):
-    assert fos.fos_abi_version() == 1
+    assert fos.fos_abi_version() == 2
     assert fos.fos_sf_bytes(300, 1040) == 384 * 68
     assert fos.fos_sf_bytes(300, 1040, fos.FOS_SF_ROWMAJOR) == 300 * 65
     assert fos.fos_sf_bytes(0, 0) == 0
@@ -200,19 +201,56 @@ def test_mxfp4_validation(fos):
     INVALID = fos.FOS_ERR_INVALID_ARG
     fake = 1 << 20
     q = fos.fos_quantize_mxfp4
-    assert q(fake, 4, 48, 48, 0, fake, 32, fake, 0, 0) == INVALID  # cols % 32
-    assert q(fake, 4, 64, 60, 0, fake, 32, fake, 0, 0) == INVALID  # ld_x < cols
-    assert q(fake, 4, 64, 68, 0, fake, 32, fake, 0, 0) == INVALID  # ld_x % 8
-    assert q(fake + 8, 4, 64, 64, 0, fake, 32, fake, 0, 0) == INVALID  # x 16-byte aligned
-    assert q(fake, 4, 64, 64, 3, fake, 32, fake, 0, 0) == INVALID  # scale rule
-    assert q(fake, 4, 64, 64, 0, fake, 30, fake, 0, 0) == INVALID  # ld_codes < cols / 2
-    assert q(fake, 4, 64, 64, 0, fake + 2, 32, fake, 0, 0) == INVALID  # codes 4-byte aligned
-    assert q(fake, 4, 64, 64, 0, fake, 32, 0, 0, 0) == INVALID  # scales
-    assert q(fake, 0, 64, 64, 0, 0, 32, 0, 0, 0) == fos.FOS_OK  # empty: nothing to launch
+    assert q(fake, 4, 48, 48, 0, 0, fake, 32, fake, 0, 0) == INVALID  # cols % 32
+    assert q(fake, 4, 64, 60, 0, 0, fake, 32, fake, 0, 0) == INVALID  # ld_x < cols
+    assert q(fake, 4, 64, 68, 0, 0, fake, 32, fake, 0, 0) == INVALID  # ld_x % 8
+    assert q(fake + 8, 4, 64, 64, 0, 0, fake, 32, fake, 0, 0) == INVALID  # x 16-byte aligned
+    assert q(fake, 4, 64, 64, 3, 0, fake, 32, fake, 0, 0) == INVALID  # scale rule
+    assert q(fake, 4, 64, 64, 0, 2, fake, 32, fake, 0, 0) == INVALID  # scale layout
+    assert q(fake, 4, 64, 64, 0, 0, fake, 30, fake, 0, 0) == INVALID  # ld_codes < cols / 2
+    assert q(fake, 4, 64, 64, 0, 0, fake + 2, 32, fake, 0, 0) == INVALID  # codes 4-byte aligned
+    assert q(fake, 4, 64, 64, 0, 0, fake, 32, 0, 0, 0) == INVALID  # scales
+    assert q(fake, 0, 64, 64, 0, 0, 0, 32, 0, 0, 0) == fos.FOS_OK  # empty: nothing to launch
     d = fos.fos_dequantize_mxfp4
-    assert d(fake, fake, 4, 48, 32, fake, 0, 48, 0) == INVALID
-    assert d(fake, fake, 4, 64, 32, fake, 7, 64, 0) == INVALID
-    assert d(fake, fake, 4, 64, 32, fake + 2, 0, 64, 0) == INVALID
+    t = fos.fos_mxfp4_tensor(codes=fake, sf=fake, rows=4, cols=48, ld_codes=32)
+    assert d(t, fake, 0, 48, 0) == INVALID  # cols % 32
+    t.cols = 64
+    assert d(t, fake, 7, 64, 0) == INVALID  # dtype
+    assert d(t, fake + 2, 0, 64, 0) == INVALID  # f32 output 4-byte aligned
+    assert d(t, fake, 0, 48, 0) == INVALID  # ld_out < cols
+    t.sf_layout = 5
+    assert d(t, fake, 0, 64, 0) == INVALID  # scale layout
+    assert fos.fos_mxfp4_sf_bytes(300, 1056) == 384 * 36
+    assert fos.fos_mxfp4_sf_bytes(300, 1056, fos.FOS_SF_ROWMAJOR) == 300 * 33
+    assert fos.fos_mxfp4_sf_bytes(0, 0) == 0
+    with pytest.raises(fos.FosError):
+        fos.fos_mxfp4_sf_bytes(10, 48)
+
+
+def test_gemm_mxfp4_validation(fos):
+    INVALID = fos.FOS_ERR_INVALID_ARG
+    fake = 1 << 20
+    g = fos.fos_gemm_mxfp4
+    A = fos.fos_mxfp4_tensor(codes=fake, sf=fake, rows=128, cols=256, ld_codes=128)
+    B = fos.fos_mxfp4_tensor(codes=fake, sf=fake, rows=256, cols=512, ld_codes=256)
+    assert g(A, B, fake, 256, 0, 0) == INVALID  # K differs
+    B.cols, B.ld_codes = 256, 128
+    assert g(A, B, fake, 100, 0, 0) == INVALID  # ldc < N
+    assert g(A, B, fake + 8, 256, 0, 0) == INVALID  # C not 16-byte aligned
+    B.rows = 250
+    assert g(A, B, fake, 256, 0, 0) == INVALID  # N % 8
+    B.rows = 256
+    A.cols = B.cols = 96
+    assert g(A, B, fake, 256, 0, 0) == INVALID  # K % 64
+    A.cols = B.cols = 256
+    A.sf = fake + 4
+    assert g(A, B, fake, 256, 0, 0) == INVALID  # scales 16-byte aligned
+    A.sf = fake
+    A.sf_layout = fos.FOS_SF_ROWMAJOR
+    assert g(A, B, fake, 256, 0, 0) == INVALID  # the MMA reads the 128x4 layout only
+    A.sf_layout = fos.FOS_SF_SWIZZLED_128x4
+    A.rows = 0
+    assert g(A, B, fake, 256, 0, 0) == fos.FOS_OK  # empty: nothing to launch
 
 
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):

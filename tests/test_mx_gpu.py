@@ -1,7 +1,8 @@
 """Parity of the MXFP4 4/6 quantizer (fos_quantize_mxfp4) with the oracle
 (reading R12): codes, E8M0 scale bytes and choices bit for bit, and the
-dequantized values exactly; ragged and edge-case inputs, all three scale
-rules, and the full-size gradient and weight shapes."""
+dequantized values exactly, with the scales row-major and in the 128x4 tiles
+the block-scaled MMA reads (pad bytes zero); ragged and edge-case inputs, all
+three scale rules, and the full-size gradient and weight shapes."""
 import numpy as np
 import pytest
 
@@ -21,24 +22,48 @@ def fos():
     return fos
 
 
-def check(fos, bits, ld=None, scale_rule=0):
+def scales_rowmajor(fos, q):
+    """The GPU's scale bytes as [rows, cols/32]; for the 128x4 tiles, also
+    check that every pad byte is zero."""
+    import oracle
+
+    sf = q.scales.cpu().numpy().reshape(-1)
+    nb = q.cols // 32
+    if q.sf_layout == fos.FOS_SF_ROWMAJOR:
+        return sf.reshape(q.rows, nb)
+    assert sf.size == oracle.sf_bytes(q.rows, nb)
+    real = np.zeros(sf.size, bool)
+    r, c = np.meshgrid(np.arange(q.rows), np.arange(nb), indexing="ij")
+    real[((r // 128) * ((nb + 3) // 4) + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + c % 4] = True
+    assert not sf[~real].any(), "pad bytes of the 128x4 tiles are not zero"
+    return oracle.sf_to_rowmajor(sf, q.rows, nb)
+
+
+def check(fos, bits, ld=None, scale_rule=0, layouts=None):
     import torch
 
     import oracle
 
     x = to_device_bf16(bits, ld)
-    q = fos.quantize_mxfp4(x, scale_rule=scale_rule, with_choice=True)
-    d = fos.dequantize_mxfp4(q)
-    db = fos.dequantize_mxfp4(q, dtype=torch.bfloat16)
-    torch.cuda.synchronize()
     o = oracle.quantize_mx(bits, scale_rule=scale_rule)
-    rows, cols = bits.shape
-    assert np.array_equal(q.codes[:, : cols // 2].cpu().numpy(), o.codes), "codes differ"
-    assert np.array_equal(q.scales.cpu().numpy(), o.scales), "scale bytes differ"
-    assert np.array_equal(q.choice.cpu().numpy(), o.choice), "choices differ"
     want = oracle.dequantize_mx(o)
-    assert np.array_equal(d.cpu().numpy(), want), "dequantized values differ"
-    assert np.array_equal(db.float().cpu().numpy(), workloads.bf16_to_f32(workloads.bf16_bits(want)))
+    rows, cols = bits.shape
+    for layout in layouts or (fos.FOS_SF_ROWMAJOR, fos.FOS_SF_SWIZZLED_128x4):
+        q = fos.quantize_mxfp4(x, scale_rule=scale_rule, sf_layout=layout, with_choice=True)
+        if layout == fos.FOS_SF_SWIZZLED_128x4:
+            # again into a buffer of junk: the launch itself writes every byte, pads included
+            q.scales.fill_(0xA5)
+            assert fos.fos_quantize_mxfp4(x.data_ptr(), rows, cols, x.stride(0), scale_rule, layout,
+                                          q.codes.data_ptr(), q.codes.stride(0), q.scales.data_ptr(),
+                                          q.choice.data_ptr(), None) == fos.FOS_OK
+        d = fos.dequantize_mxfp4(q)
+        db = fos.dequantize_mxfp4(q, dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        assert np.array_equal(q.codes[:, : cols // 2].cpu().numpy(), o.codes), "codes differ"
+        assert np.array_equal(scales_rowmajor(fos, q), o.scales), "scale bytes differ"
+        assert np.array_equal(q.choice.cpu().numpy(), o.choice), "choices differ"
+        assert np.array_equal(d.cpu().numpy(), want), "dequantized values differ"
+        assert np.array_equal(db.float().cpu().numpy(), workloads.bf16_to_f32(workloads.bf16_bits(want)))
     return o
 
 
@@ -88,13 +113,13 @@ def test_mx_non_finite_blocks(fos, scale_rule):
     bits[2, 255] = 0x7FC0  # NaN
     bits[3, 32:64] = 0x7F81  # a block of signalling-pattern NaNs
     x = to_device_bf16(bits)
-    q = fos.quantize_mxfp4(x, scale_rule=scale_rule, with_choice=True)
+    q = fos.quantize_mxfp4(x, scale_rule=scale_rule, sf_layout=fos.FOS_SF_SWIZZLED_128x4, with_choice=True)
     d = fos.dequantize_mxfp4(q)
     db = fos.dequantize_mxfp4(q, dtype=torch.bfloat16)
     torch.cuda.synchronize()
     o = oracle.quantize_mx(bits, scale_rule=scale_rule)
     assert np.array_equal(q.codes[:, :128].cpu().numpy(), o.codes), "codes differ"
-    assert np.array_equal(q.scales.cpu().numpy(), o.scales), "scale bytes differ"
+    assert np.array_equal(scales_rowmajor(fos, q), o.scales), "scale bytes differ"
     assert np.array_equal(q.choice.cpu().numpy(), o.choice), "choices differ"
     assert (o.scales == 0xFF).sum() == 4
     want = oracle.dequantize_mx(o)
