@@ -48,6 +48,32 @@ def test_batch_matches_oracle(fos, opts):
         assert_same(got[i], oracle_quantize(b, **oopts), f"job {i} {b.shape} {opts}")
 
 
+def test_batch_quantizer_reused_on_new_inputs(fos):
+    """One BatchQuantizer called on the same inputs twice, then on other
+    tensors of the same shapes (other addresses, one of them inside wider
+    rows), then on the first ones again: every call must quantize the tensors
+    it is given."""
+    import torch
+
+    shapes = [(64, 256), (300, 1040)]
+    first = [mixed_bits(r, c, seed=51 + i) for i, (r, c) in enumerate(shapes)]
+    second = [mixed_bits(r, c, seed=61 + i) for i, (r, c) in enumerate(shapes)]
+    xa = [to_device_bf16(b) for b in first]
+    xb = [to_device_bf16(second[0]), to_device_bf16(second[1], 1048)]
+    bq = fos.BatchQuantizer(shapes, with_choice=True)
+
+    def got():
+        torch.cuda.synchronize()
+        return [QOut(codes=o.codes[:, : o.cols // 2].cpu().numpy(),
+                     sf=o.sf.cpu().numpy()[: fos.fos_sf_bytes(o.rows, o.cols, o.sf_layout)],
+                     s_t=np.float32(o.tensor_scale.item()), choice=o.choice.cpu().numpy()) for o in bq.outs]
+
+    for xs, bits in ((xa, first), (xa, first), (xb, second), (xa, first)):
+        bq(xs)
+        for i, (g, b) in enumerate(zip(got(), bits)):
+            assert_same(g, oracle_quantize(b), f"job {i}")
+
+
 def test_batch_padded_rows_and_weight_like_jobs(fos):
     bits = [workloads.student_t(512, 4096, seed=81), mixed_bits(256, 1024, seed=82),
             workloads.student_t(1024, 1536, seed=83)]
