@@ -15,8 +15,10 @@
 // No tensor scale means no amax pass: one launch reads each value once.  One
 // thread owns one 32-value block (64 contiguous bytes; a warp reads 2 KB).
 // Scales go row-major or into the 128x4 tiles the block-scaled MMA reads
-// (one tile: 128 rows x 4 scales = 128 values of K); the same launch zeroes
-// the tiles' pad bytes.
+// (one tile: 128 rows x 4 scales = 128 values of K).  For the tiles, thread t
+// takes the block whose scale byte is byte t of the buffer, so a warp stores
+// 32 contiguous scale bytes (and reads 8 rows x 4 neighbouring blocks, 256
+// contiguous bytes a row); a thread whose byte is padding writes a zero.
 #include <cuda_runtime.h>
 
 #include <cfloat>
@@ -45,27 +47,6 @@ struct MxParams {
   int codes16;      // codes 16-byte aligned with ld_codes % 16 == 0
   int layout;       // fos_sf_layout
 };
-
-// Zero the pad bytes of a 128x4-tiled scale buffer of R rows and nb scale
-// columns: rows R .. pad128(R)-1 of every padded column, then columns
-// nb .. pad4(nb)-1 of the real rows.  Grid-stride over the pad bytes only.
-__device__ __forceinline__ void zero_sf_pads(uint8_t* sf, int64_t R, int64_t nb) {
-  const int64_t nbp = (nb + 3) & ~int64_t(3), Rp = (R + 127) & ~int64_t(127);
-  const int64_t n_rows_pad = (Rp - R) * nbp, n_cols_pad = R * (nbp - nb);
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_rows_pad + n_cols_pad; i += stride) {
-    int64_t r, c;
-    if (i < n_rows_pad) {
-      r = R + i / nbp;
-      c = i - (r - R) * nbp;
-    } else {
-      const int64_t j = i - n_rows_pad, w = nbp - nb;
-      r = j / w;
-      c = nb + (j - r * w);
-    }
-    sf[sf_off(r, c, nb, 0)] = 0;
-  }
-}
 
 // max |x| of 16 bf16 values held as 8 words, NaN-propagating: a NaN input
 // gives NaN, an infinity gives infinity (the sign bit of the bf16 maxima is
@@ -113,10 +94,24 @@ __device__ __forceinline__ float mx_candidate(const uint64_t (&yp)[16], float in
 template <int RULE>
 __global__ void __launch_bounds__(256) quant_mx_kernel(MxParams p) {
   const int64_t nb = p.cols >> 5;
-  const int64_t n = p.rows * nb;
-  if (p.layout == FOS_SF_SWIZZLED_128x4) zero_sf_pads(p.scales, p.rows, nb);
+  const bool tiled = p.layout == FOS_SF_SWIZZLED_128x4;
+  const int64_t n_ct = (nb + 3) >> 2;  // 4-scale column tiles
+  const int64_t n = tiled ? (((p.rows + 127) >> 7) * n_ct) << 9 : p.rows * nb;
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = t / nb, b = t - r * nb;
+    int64_t r, b;
+    if (tiled) {
+      // byte t of the tiles: tile t/512, and inside it (r%32)*16 + ((r%128)/32)*4 + b%4
+      const int64_t tile = t >> 9, w = t & 511, rt = tile / n_ct;
+      r = (rt << 7) + (((w >> 2) & 3) << 5) + (w >> 4);
+      b = ((tile - rt * n_ct) << 2) + (w & 3);
+      if (r >= p.rows || b >= nb) {
+        p.scales[t] = 0;
+        continue;
+      }
+    } else {
+      r = t / nb;
+      b = t - r * nb;
+    }
     const uint4* src = reinterpret_cast<const uint4*>(p.x + r * p.ld + b * 32);
     uint32_t wv[16];
 #pragma unroll
@@ -158,8 +153,8 @@ __global__ void __launch_bounds__(256) quant_mx_kernel(MxParams p) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) reinterpret_cast<uint32_t*>(dst)[k] = c[k];
     }
-    p.scales[sf_off(r, b, nb, p.layout)] = finite ? (uint8_t)((four ? X4 : X6) + 127) : (uint8_t)0xFF;
-    if (p.choice) p.choice[t] = four ? 1 : 0;
+    p.scales[t] = finite ? (uint8_t)((four ? X4 : X6) + 127) : (uint8_t)0xFF;
+    if (p.choice) p.choice[r * nb + b] = four ? 1 : 0;
   }
 }
 
