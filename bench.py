@@ -338,14 +338,15 @@ def run_fos(args, dist: Dist) -> None:
     def step():
         bq(xs)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-
     e0, e1 = _events(torch, 2)
-    dist.barrier()
-    torch.cuda.synchronize()
+    # the clock sampler starts before the warm-up: its thread's start-up then
+    # does not compete with the timed region's first launches
     with ClockSampler(dev.index) as clk:
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        dist.barrier()
+        torch.cuda.synchronize()
         h0 = time.perf_counter()
         e0.record(stream)
         for _ in range(args.steps):
