@@ -444,45 +444,51 @@ __device__ __forceinline__ float sumsq16(const float (&r)[16]) {
 // so the interval's ends are lo = floor(t) * step and hi = lo + step.  The
 // rule "up iff u < p" with p = t - floor(t) and u = n * 2^-24 (n = w >> 8)
 // picks ceil(t - u) * step: t - u lies in (floor(t), floor(t) + 1) when
-// u < p, and in (floor(t) - 1, floor(t)] otherwise.  t - u is evaluated as
-// one FMA rounded toward +inf, fma.rp(-n, 2^-24, t), and ceil(.) as the
-// round-up addition of M = 1.5 * 2^23, then M subtracted: t - u lies in
-// (-1, 3], so M + (t - u) stays inside [2^23, 2^24), where the spacing of
-// floats is exactly 1.  Both roundings are exact for ceil's purpose:
-// rounding up never passes an integer, and the integers involved are floats.
+// u < p, and in (floor(t) - 1, floor(t)] otherwise.  t - u is one FMA rounded
+// toward +inf, and ceil(.) the round-up addition of M = 1.5 * 2^23, then M
+// subtracted: t - u lies in (-1, 4), so M + (t - u) stays inside
+// [2^23, 2^24), where the spacing of floats is exactly 1.  Both roundings
+// are exact for ceil's purpose: rounding up never passes an integer, and the
+// integers involved are floats.
+// Evaluated scaled by step: rounding toward +inf commutes with multiplying
+// by a power of two while the results stay normal, so
+// fma.rp(n, -step * 2^-24, a) = step * fma.rp(-n, 2^-24, t), and the
+// round-up addition of step * M lands on multiples of step.  (With n = 0
+// nothing is rounded; with n >= 1 a nonzero a - n * step * 2^-24 is a
+// multiple of ulp(a) >= 2^-49, since a >= 2^-26 whenever it comes that
+// close to n * step * 2^-24 >= 2^-25: never subnormal.)  The products
+// -step * 2^-24 and step * M come from P = 2^e (e the exponent of
+// max(a, 1), step = P / 2) by two exact multiplies, so t, 1/step and the
+// final multiply by step are not needed.
 // a >= 6 is clamped to 6 first (t = 3 gives 6 for every u), as the rule
-// saturates; step is read off the exponent of max(a, 1): 2^e / 2, with
-// 1/step = 2 / 2^e, both formed on the exponent bits.
-__device__ __forceinline__ F2 sr_mag2(F2 aq, F2 negn) {
+// saturates.
+__device__ __forceinline__ F2 sr_mag2(F2 aq, F2 n) {
   const float a0 = fminf(aq.x, 6.0f), a1 = fminf(aq.y, 6.0f);
-  const uint32_t p0 = __float_as_uint(fmaxf(a0, 1.0f)) & 0x7F800000u;
-  const uint32_t p1 = __float_as_uint(fmaxf(a1, 1.0f)) & 0x7F800000u;
-  const F2 inv{__uint_as_float(0x7F800000u - p0), __uint_as_float(0x7F800000u - p1)};
-  const F2 step{__uint_as_float(p0 - 0x00800000u), __uint_as_float(p1 - 0x00800000u)};
-  const F2 t = mul2(F2{a0, a1}, inv);
-  F2 c;
-  asm("{\n\t.reg .b64 rn, rs, rt, rd, rm, rc;\n\t"
-      "mov.b64 rn, {%2, %3};\n\tmov.b64 rs, {%4, %4};\n\tmov.b64 rt, {%5, %6};\n\t"
-      "fma.rp.f32x2 rd, rn, rs, rt;\n\t"
-      "mov.b64 rm, {%7, %7};\n\t"
-      "add.rp.f32x2 rc, rd, rm;\n\t"
+  const F2 P{__uint_as_float(__float_as_uint(fmaxf(a0, 1.0f)) & 0x7F800000u),
+             __uint_as_float(__float_as_uint(fmaxf(a1, 1.0f)) & 0x7F800000u)};
+  F2 g;
+  asm("{\n\t.reg .b64 rn, rp, ra, rk, rs, rm, rx, rc;\n\t"
+      "mov.b64 rn, {%2, %3};\n\tmov.b64 rp, {%4, %5};\n\tmov.b64 ra, {%6, %7};\n\t"
+      "mov.b64 rk, {%8, %8};\n\tmov.b64 rm, {%9, %9};\n\t"
+      "mul.rn.f32x2 rs, rp, rk;\n\t"    // -step * 2^-24
+      "mul.rn.f32x2 rm, rp, rm;\n\t"    // step * M
+      "fma.rp.f32x2 rx, rn, rs, ra;\n\t"
+      "add.rp.f32x2 rc, rx, rm;\n\t"
       "sub.rn.f32x2 rc, rc, rm;\n\t"
       "mov.b64 {%0, %1}, rc;\n\t}"
-      : "=f"(c.x), "=f"(c.y)
-      : "f"(negn.x), "f"(negn.y), "f"(5.9604644775390625e-8f), "f"(t.x), "f"(t.y), "f"(12582912.0f));
-  return mul2(c, step);
+      : "=f"(g.x), "=f"(g.y)
+      : "f"(n.x), "f"(n.y), "f"(P.x), "f"(P.y), "f"(a0), "f"(a1), "f"(-2.98023223876953125e-8f),
+        "f"(6291456.0f));
+  return g;
 }
 
-// -n = -(w >> 8) of the 16 elements' words, once per block: both
-// candidates round with the same u = n * 2^-24.
-__device__ __forceinline__ void sr_negn16(const uint32_t (&w)[16], float (&negn)[16]) {
-#pragma unroll
-  for (int j = 0; j < 16; ++j) negn[j] = -(float)(w[j] >> 8);
-}
+// The draw of one element: n = w >> 8 of its Philox word, as a float (exact:
+// n < 2^24).  Both candidates round with the same u = n * 2^-24.
+__device__ __forceinline__ float sr_draw(uint32_t w) { return (float)(w >> 8); }
 
 // Stochastic-rounding codes of one candidate (yp: the block's values as
-// packed pairs; negn from sr_negn16).
-__device__ __forceinline__ float cand_sr16(const uint64_t (&yp)[8], float inv, const float (&negn)[16], uint32_t& lo,
+// packed pairs; n the elements' draws, sr_draw).
+__device__ __forceinline__ float cand_sr16(const uint64_t (&yp)[8], float inv, const float (&n)[16], uint32_t& lo,
                                            uint32_t& hi) {
   F2 acc{0.0f, 0.0f};
   uint32_t b[8];
@@ -490,7 +496,7 @@ __device__ __forceinline__ float cand_sr16(const uint64_t (&yp)[8], float inv, c
   for (int k = 0; k < 8; ++k) {
     const F2 q = mul2(unpack_f2(yp[k]), F2{inv, inv});
     const F2 aq{fabsf(q.x), fabsf(q.y)};
-    const F2 g = sr_mag2(aq, F2{negn[2 * k], negn[2 * k + 1]});
+    const F2 g = sr_mag2(aq, F2{n[2 * k], n[2 * k + 1]});
     // the grid value with q's sign converts exactly
     b[k] = e2m1x2(copysignf(g.x, q.x), copysignf(g.y, q.y));
     const F2 r = sub2(aq, g);

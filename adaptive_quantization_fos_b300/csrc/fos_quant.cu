@@ -224,16 +224,18 @@ __device__ __forceinline__ TensorConsts quant_prologue(const QuantParams& p, flo
   return tc;
 }
 
+// The stochastic-rounding draws n = w >> 8 (as floats, exact) of the 16
+// consecutive source elements starting at index i0.
 template <bool SR>
-__device__ __forceinline__ void sr_words16(uint64_t i0, const QuantParams& p, uint32_t (&w)[16]) {
+__device__ __forceinline__ void sr_draws16(uint64_t i0, const QuantParams& p, float (&n)[16]) {
   if constexpr (SR) {
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
-      U4 u = sr_words4(i0 + 4 * g, p.sr_k0, p.sr_k1);
-      w[4 * g] = u.x;
-      w[4 * g + 1] = u.y;
-      w[4 * g + 2] = u.z;
-      w[4 * g + 3] = u.w;
+      const U4 u = sr_words4(i0 + 4 * g, p.sr_k0, p.sr_k1);
+      n[4 * g] = sr_draw(u.x);
+      n[4 * g + 1] = sr_draw(u.y);
+      n[4 * g + 2] = sr_draw(u.z);
+      n[4 * g + 3] = sr_draw(u.w);
     }
   }
 }
@@ -276,12 +278,10 @@ __device__ __forceinline__ TensorConsts quant_prologue_rows(const QuantParams& p
 
 template <int RULE, bool SR>
 __device__ __forceinline__ void quant_block_tab(const uint64_t (&yp)[8], float ab, const TensorConsts& tc,
-                                                const float2* tab, const uint32_t (&w)[16], uint32_t& lo,
+                                                const float2* tab, const float (&n_sr)[16], uint32_t& lo,
                                                 uint32_t& hi, uint32_t& sf, bool& four) {
   const uint32_t pair = candidate_scales(ab, tc);
   const uint32_t sf6 = pair & 0xFFu, sf4 = pair >> 8;
-  float negn[16];
-  if (SR) sr_negn16(w, negn);
   uint32_t lo6 = 0, hi6 = 0, lo4 = 0, hi4 = 0;
   float E6 = 0.0f, E4 = 0.0f;
 #pragma unroll
@@ -292,7 +292,7 @@ __device__ __forceinline__ void quant_block_tab(const uint64_t (&yp)[8], float a
     uint32_t l, h;
     float S;
     if (SR) {
-      S = cand_sr16(yp, t.x, negn, l, h);
+      S = cand_sr16(yp, t.x, n_sr, l, h);
     } else {
       const uint64_t inv2 = pack_f2(t.x, t.x);
       uint64_t acc = 0ull;
@@ -637,11 +637,11 @@ __global__ void __launch_bounds__(MODE == kRowsChained ? 320 : 256, MODE == kRow
         for (int k = 0; k < 8; ++k) yp[k] = bf16x2_to_f32x2(wv[k]);
         ab = absmax16_bf16(wv);
       }
-      uint32_t w[16];
-      sr_words16<SR>((uint64_t)r * (uint64_t)p.cols + (uint64_t)(b_lane + 32 * j) * 16, p, w);
+      float n_sr[16];
+      sr_draws16<SR>((uint64_t)r * (uint64_t)p.cols + (uint64_t)(b_lane + 32 * j) * 16, p, n_sr);
       uint32_t lo, hi, sf;
       bool four;
-      quant_block_tab<RULE, SR>(yp, ab, tc, s_tab, w, lo, hi, sf, four);
+      quant_block_tab<RULE, SR>(yp, ab, tc, s_tab, n_sr, lo, hi, sf, four);
       *reinterpret_cast<uint2*>(code_dst + 256 * j) = make_uint2(lo, hi);
       // 32 blocks further along a row: 8 swizzled tiles (4096 bytes) further
       sf_dst[sf_step * j] = (uint8_t)sf;
@@ -787,8 +787,8 @@ __global__ void __launch_bounds__(256, 2) quant_cols_kernel(QuantParams p) {
         ph ^= 1u;
       }
       const int64_t rb = 4 * g + sub;
-      // the two columns' stochastic-rounding words
-      uint32_t w0[16], w1[16];
+      // the two columns' stochastic-rounding draws
+      float n0[16], n1[16];
       if (SR) {
         const bool odd = lane & 1;
         const uint64_t grp = (uint64_t)(c0 + 4 * (lane >> 1));
@@ -799,9 +799,9 @@ __global__ void __launch_bounds__(256, 2) quant_cols_kernel(QuantParams p) {
           const uint32_t r0 = __shfl_xor_sync(0xFFFFFFFFu, odd ? u.x : u.z, 1);
           const uint32_t r1 = __shfl_xor_sync(0xFFFFFFFFu, odd ? u.y : u.w, 1);
           if (odd) {
-            w0[q] = r0; w1[q] = r1; w0[q + 8] = u.z; w1[q + 8] = u.w;
+            n0[q] = sr_draw(r0); n1[q] = sr_draw(r1); n0[q + 8] = sr_draw(u.z); n1[q + 8] = sr_draw(u.w);
           } else {
-            w0[q] = u.x; w1[q] = u.y; w0[q + 8] = r0; w1[q + 8] = r1;
+            n0[q] = sr_draw(u.x); n1[q] = sr_draw(u.y); n0[q + 8] = sr_draw(r0); n1[q + 8] = sr_draw(r1);
           }
         }
       }
@@ -821,7 +821,7 @@ __global__ void __launch_bounds__(256, 2) quant_cols_kernel(QuantParams p) {
         for (int j = 0; j < 8; ++j) yp[j] = pack_f2(y[2 * j], y[2 * j + 1]);
         uint32_t lo, hi, sf;
         bool four;
-        quant_block_tab<RULE, SR>(yp, ab, tc, s_tab, (k & 1) ? w1 : w0, lo, hi, sf, four);
+        quant_block_tab<RULE, SR>(yp, ab, tc, s_tab, (k & 1) ? n1 : n0, lo, hi, sf, four);
         const int64_t orow = c0 + CPL * lane + k;  // output row = source column
         if (orow < p.cols) {
           *reinterpret_cast<uint2*>(p.codes + orow * p.ld_codes + rb * 8) = make_uint2(lo, hi);
@@ -909,10 +909,8 @@ __global__ void __launch_bounds__(256) quant_2d_kernel(QuantParams p) {
       for (int j = 0; j < 16; ++j) y[j] = __fmul_rn(y[j], 0.25f);
     }
     const float ab = half_max(absmax16(y));
-    uint32_t w[16];
-    sr_words16<SR>((uint64_t)r * (uint64_t)p.cols + (uint64_t)c0, p, w);
-    float negn[16];
-    if (SR) sr_negn16(w, negn);
+    float n_sr[16];
+    sr_draws16<SR>((uint64_t)r * (uint64_t)p.cols + (uint64_t)c0, p, n_sr);
     const uint32_t pair = candidate_scales(ab, tc);
     const uint32_t sf6 = pair & 0xFFu, sf4 = pair >> 8;
     uint64_t yp[8];
@@ -929,7 +927,7 @@ __global__ void __launch_bounds__(256) quant_2d_kernel(QuantParams p) {
       uint32_t l, h;
       float S;
       if (SR) {
-        S = cand_sr16(yp, tb.x, negn, l, h);
+        S = cand_sr16(yp, tb.x, n_sr, l, h);
       } else {
         const uint64_t inv2 = pack_f2(tb.x, tb.x);
         uint64_t acc = 0ull;
