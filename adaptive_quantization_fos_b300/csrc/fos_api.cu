@@ -55,6 +55,30 @@ int amax_tasks_grid(int64_t rows, int64_t cols, bool cols_kernel) {
 
 }  // namespace
 
+namespace fos {
+cudaError_t amax_plain_and_rht_cols(const void* x, int64_t rows, int64_t cols, int64_t ld, uint64_t hadamard_seed,
+                                    float* out, void* workspace, cudaStream_t s) {
+  AmaxParams a{};
+  a.x = static_cast<const uint16_t*>(x);
+  a.rows = rows;
+  a.cols = cols;
+  a.ld = ld;
+  a.hk0 = (uint32_t)hadamard_seed;
+  a.hk1 = (uint32_t)(hadamard_seed >> 32);
+  a.aligned32 = aligned(x, 32) && ld % 16 == 0;
+  // the two partial arrays share the workspace's partial-maxima region
+  a.partials = static_cast<float*>(workspace);
+  a.partials_plain = a.partials + kMaxAmaxPartials / 2;
+  int g = amax_tasks_grid(rows, cols, true);
+  if (g > kMaxAmaxPartials / 2) g = kMaxAmaxPartials / 2;
+  cudaError_t e = launch_amax(a, true, true, g, s);
+  if (e != cudaSuccess) return e;
+  amax_final_kernel<<<1, 256, 0, s>>>(a.partials_plain, g, out);
+  amax_final_kernel<<<1, 256, 0, s>>>(a.partials, g, out + 1);
+  return cudaGetLastError();
+}
+}  // namespace fos
+
 extern "C" {
 
 int32_t fos_abi_version(void) { return FOS_ABI_VERSION; }

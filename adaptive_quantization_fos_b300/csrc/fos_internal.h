@@ -28,6 +28,7 @@ struct AmaxParams {
   uint32_t hk0, hk1;  // RHT seed words
   bool aligned32;
   float* partials;
+  float* partials_plain;  // optional (RHT down columns only): also max |x| untransformed
 };
 
 struct QuantParams {
@@ -72,6 +73,13 @@ struct DequantParams {
 int amax_grid(int64_t n_warp_tasks);
 int quant_grid(int64_t n_warp_tasks, int kind);
 cudaError_t launch_amax(const AmaxParams& p, bool hadamard, bool transpose, int grid, cudaStream_t s);
+
+// From one read of x [rows, cols] (rows % 16 == 0, 16-byte aligned, ld % 8 == 0):
+// out[0] = max |x| and out[1] = max |y| for y the RHT of x down its columns
+// (blocks of 16 rows), each exactly what the separate amax passes give.
+// workspace: kQuantWorkspaceBytes of device scratch.
+cudaError_t amax_plain_and_rht_cols(const void* x, int64_t rows, int64_t cols, int64_t ld, uint64_t hadamard_seed,
+                                    float* out, void* workspace, cudaStream_t s);
 // kind: 0 rows (1D), 1 cols (1D transposed), 2 2D, 3 2D transposed
 // pdl: the launch may overlap the stream's previous kernel, which must be one
 // of this library's amax or row-quantize launches (the quantize kernel reads

@@ -32,7 +32,7 @@ int64_t sf_bytes(int64_t rows, int64_t cols) { return ((rows + 127) / 128) * 128
 // Where each part of the workspace lies.
 struct Layout {
   int64_t rows[4], cols[4];
-  size_t codes[4], sf[4], scales, scratch, total;
+  size_t codes[4], sf[4], scales, amax, scratch, total;
 };
 
 bool valid_shape(int64_t M, int64_t N, int64_t K) {
@@ -54,6 +54,8 @@ Layout layout(int64_t M, int64_t N, int64_t K) {
   }
   L.scales = o;
   o = up(o + 4 * sizeof(float));
+  L.amax = o;  // dY's two tensor maxima when both products are computed
+  o = up(o + 2 * sizeof(float));
   L.scratch = o;
   L.total = o + fos::kQuantWorkspaceBytes;
   return L;
@@ -163,15 +165,32 @@ fos_status fos_linear_backward(const void* dy, int64_t ld_dy, const void* x, int
                         scratch_bytes, stream);
   };
 
+  // With both products, dY is quantized twice (along N and, transposed, along
+  // M).  Its two tensor maxima -- of dY, and of its RHT down the columns when
+  // the wgrad operands get the RHT -- then come from one read of dY, and both
+  // quantizations take them as supplied maxima (the same values their own
+  // amax passes would find).
+  const bool both = dx && dw;
+  float* amax_dy = reinterpret_cast<float*>(base + L.amax);  // [max|dY|, max|RHT_M(dY)|]
+  if (both) {
+    if (opt->wgrad_hadamard) {
+      if (fos::amax_plain_and_rht_cols(dy, M, N, ld_dy, opt->hadamard_seed, amax_dy, scratch, stream) != cudaSuccess)
+        return FOS_ERR_CUDA;
+    } else if ((st = fos_tensor_amax(dy, M, N, ld_dy, 0, 0, 0, amax_dy, scratch, scratch_bytes, stream)) != FOS_OK) {
+      return st;
+    }
+  }
   if (dx) {
-    const fos_quant_options o_dy = opts(opt->grad_rounding, 0, 0, 0);
+    fos_quant_options o_dy = opts(opt->grad_rounding, 0, 0, 0);
+    if (both) o_dy.tensor_amax = amax_dy;
     const fos_quant_options o_w = opts(FOS_ROUND_RNE, 1, 0, opt->weight_2d);
     if ((st = quant(0, dy, M, N, ld_dy, o_dy)) != FOS_OK) return st;
     if ((st = quant(1, w, N, K, ld_w, o_w)) != FOS_OK) return st;
     if ((st = fos_gemm(&ops[0], &ops[1], dx, ld_dx, dev_status, stream)) != FOS_OK) return st;
   }
   if (dw) {
-    const fos_quant_options o_dyt = opts(opt->grad_rounding, 1, opt->wgrad_hadamard, 0);
+    fos_quant_options o_dyt = opts(opt->grad_rounding, 1, opt->wgrad_hadamard, 0);
+    if (both) o_dyt.tensor_amax = opt->wgrad_hadamard ? amax_dy + 1 : amax_dy;
     const fos_quant_options o_xt = opts(FOS_ROUND_RNE, 1, opt->wgrad_hadamard, 0);
     if ((st = quant(2, dy, M, N, ld_dy, o_dyt)) != FOS_OK) return st;
     if ((st = quant(3, x, M, K, ld_x, o_xt)) != FOS_OK) return st;

@@ -174,7 +174,10 @@ __global__ void __launch_bounds__(256) amax_rows_kernel(AmaxParams p) {
   if (threadIdx.x == 0) p.partials[blockIdx.x] = m;
 }
 
-// RHT down columns: a lane owns 4 adjacent columns x 16 rows.
+// RHT down columns: a lane owns 4 adjacent columns x 16 rows.  With PLAIN,
+// the same pass also takes max |x| of the untransformed values (the integer
+// maximum of the bf16 magnitude bits) into p.partials_plain.
+template <bool PLAIN>
 __global__ void __launch_bounds__(256) amax_cols_kernel(AmaxParams p) {
   __shared__ float s_red[33];
   pdl_launch_dependents();  // the quantize launch may start its own reads meanwhile
@@ -184,12 +187,17 @@ __global__ void __launch_bounds__(256) amax_cols_kernel(AmaxParams p) {
   const int64_t n_tasks = (p.rows >> 4) * ngroups;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   float m = 0.0f;
+  uint32_t mp = 0u;  // PLAIN: magnitude bits, two bf16 halves
   for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n_tasks; t += nwarps) {
     int64_t rb = t / ngroups, c0 = (t - rb * ngroups) * 128 + 4 * lane;
     if (c0 >= p.cols) continue;
     uint2 d[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) d[i] = __ldg(reinterpret_cast<const uint2*>(p.x + (rb * 16 + i) * p.ld + c0));
+    if (PLAIN) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) mp = max_u16x2(mp, max_u16x2(d[i].x & 0x7FFF7FFFu, d[i].y & 0x7FFF7FFFu));
+    }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       float y[16];
@@ -206,6 +214,10 @@ __global__ void __launch_bounds__(256) amax_cols_kernel(AmaxParams p) {
   m = unscaled_to_amax(m);
   m = block_max(m, s_red);
   if (threadIdx.x == 0) p.partials[blockIdx.x] = m;
+  if (PLAIN) {
+    const float mpl = block_max(fmaxf(bf16lo(mp), bf16hi(mp)), s_red);
+    if (threadIdx.x == 0) p.partials_plain[blockIdx.x] = mpl;
+  }
 }
 
 // ------------------------------------------------------- quantize prologue
@@ -1070,7 +1082,10 @@ int amax_grid(int64_t n_warp_tasks) {
 
 cudaError_t launch_amax(const AmaxParams& p, bool hadamard, bool transpose, int grid, cudaStream_t s) {
   if (hadamard && transpose)
-    amax_cols_kernel<<<grid, 256, 0, s>>>(p);
+    if (p.partials_plain)
+      amax_cols_kernel<true><<<grid, 256, 0, s>>>(p);
+    else
+      amax_cols_kernel<false><<<grid, 256, 0, s>>>(p);
   else if (hadamard)
     amax_rows_kernel<true><<<grid, 256, 0, s>>>(p);
   else
