@@ -49,7 +49,8 @@ __global__ void amax_final_kernel(const float* partials, int n, float* out) {
 }
 
 int amax_tasks_grid(int64_t rows, int64_t cols, bool cols_kernel) {
-  int64_t tasks = cols_kernel ? (rows / 16) * ((cols + 127) / 128) : rows * ((cols / 16 + 31) / 32);
+  int64_t tasks = cols_kernel ? (rows / 16) * ((cols + fos::kAmaxColTask - 1) / fos::kAmaxColTask)
+                              : rows * ((cols / 16 + 31) / 32);
   return fos::amax_grid(tasks);
 }
 

@@ -12,6 +12,10 @@ namespace fos {
 // Upper bound on the number of CTAs of the amax pass (= partial maxima the
 // quantize kernels reduce in their prologue).
 constexpr int kMaxAmaxPartials = 2048;
+// The column amax pass (the RHT down columns): adjacent source columns per
+// lane, and per warp task.
+constexpr int kAmaxColCPL = 8;
+constexpr int kAmaxColTask = 32 * kAmaxColCPL;
 // Workspace: the partial maxima, then (at kBarrierOffset) the words of the
 // one-launch row quantizer: the grid barrier's arrival counter, a flag that a
 // CTA which gave up on a wait raises, and the counter of CTAs that finished

@@ -174,39 +174,48 @@ __global__ void __launch_bounds__(256) amax_rows_kernel(AmaxParams p) {
   if (threadIdx.x == 0) p.partials[blockIdx.x] = m;
 }
 
-// RHT down columns: a lane owns 4 adjacent columns x 16 rows.  With PLAIN,
-// the same pass also takes max |x| of the untransformed values (the integer
-// maximum of the bf16 magnitude bits) into p.partials_plain.
+// RHT down columns: a lane owns kAmaxColCPL adjacent columns x 16 rows, so a
+// warp reads 64 * kAmaxColCPL contiguous bytes of each of the 16 rows.  With
+// PLAIN, the same pass also takes max |x| of the untransformed values (the
+// column's magnitudes before the butterflies: the sign flips do not change
+// them) into p.partials_plain.  Two CTAs per SM at 128 registers (a few bytes
+// spilled) measured faster than one at 142, and than 4 columns per lane.
 template <bool PLAIN>
-__global__ void __launch_bounds__(256) amax_cols_kernel(AmaxParams p) {
+__global__ void __launch_bounds__(256, 2) amax_cols_kernel(AmaxParams p) {
+  constexpr int W = kAmaxColCPL / 2;  // words per row and lane
   __shared__ float s_red[33];
   pdl_launch_dependents();  // the quantize launch may start its own reads meanwhile
   const int lane = threadIdx.x & 31;
   const uint32_t rht_mask = rht_sign_mask(p.hk0, p.hk1);
-  const int64_t ngroups = (p.cols + 127) >> 7;  // 128 columns per warp task
+  const int64_t ngroups = (p.cols + kAmaxColTask - 1) / kAmaxColTask;
   const int64_t n_tasks = (p.rows >> 4) * ngroups;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  float m = 0.0f;
-  uint32_t mp = 0u;  // PLAIN: magnitude bits, two bf16 halves
+  float m = 0.0f, mp = 0.0f;  // mp: PLAIN's maximum
   for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n_tasks; t += nwarps) {
-    int64_t rb = t / ngroups, c0 = (t - rb * ngroups) * 128 + 4 * lane;
-    if (c0 >= p.cols) continue;
-    uint2 d[16];
+    int64_t rb = t / ngroups, c0 = (t - rb * ngroups) * kAmaxColTask + kAmaxColCPL * lane;
+    if (c0 >= p.cols) continue;  // cols % 16 == 0: the lane's columns all exist
+    uint32_t d[16][W];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) d[i] = __ldg(reinterpret_cast<const uint2*>(p.x + (rb * 16 + i) * p.ld + c0));
-    if (PLAIN) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) mp = max_u16x2(mp, max_u16x2(d[i].x & 0x7FFF7FFFu, d[i].y & 0x7FFF7FFFu));
+    for (int i = 0; i < 16; ++i) {
+      const uint16_t* src = p.x + (rb * 16 + i) * p.ld + c0;
+      if constexpr (W == 4) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
+        d[i][0] = v.x; d[i][W - 3] = v.y; d[i][W - 2] = v.z; d[i][W - 1] = v.w;
+      } else {
+        const uint2 v = __ldg(reinterpret_cast<const uint2*>(src));
+        d[i][0] = v.x; d[i][W - 1] = v.y;
+      }
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kAmaxColCPL; ++k) {
       float y[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        uint32_t wv = (k < 2) ? d[i].x : d[i].y;
-        uint32_t s = ((rht_mask >> i) & 1u) << 31;
+        const uint32_t wv = d[i][k >> 1];
+        const uint32_t s = ((rht_mask >> i) & 1u) << 31;
         y[i] = __uint_as_float(((k & 1) ? (wv & 0xFFFF0000u) : (wv << 16)) ^ s);
       }
+      if (PLAIN) mp = fmaxf(mp, absmax16(y));
       butterflies16(y);  // 1/4 applied to the maximum below
       m = fmaxf(m, absmax16(y));
     }
@@ -215,8 +224,8 @@ __global__ void __launch_bounds__(256) amax_cols_kernel(AmaxParams p) {
   m = block_max(m, s_red);
   if (threadIdx.x == 0) p.partials[blockIdx.x] = m;
   if (PLAIN) {
-    const float mpl = block_max(fmaxf(bf16lo(mp), bf16hi(mp)), s_red);
-    if (threadIdx.x == 0) p.partials_plain[blockIdx.x] = mpl;
+    mp = block_max(mp, s_red);
+    if (threadIdx.x == 0) p.partials_plain[blockIdx.x] = mp;
   }
 }
 
