@@ -516,20 +516,33 @@ def _time_calls(torch, fn, reps: int) -> float:
     return e0.elapsed_time(e1) / reps
 
 
+def _time_flushed(torch, flush, fn, reps: int) -> float:
+    """Average ms of fn() alone with a cold L2: before each call a write of
+    `flush` (larger than L2), then a short spin (torch.cuda._sleep, no memory
+    traffic) that keeps the GPU busy while the host enqueues the start event
+    and fn; CUDA events on the current stream bracket fn alone."""
+    fn()
+    torch.cuda.synchronize()
+    ev = _events(torch, 2 * reps)
+    for i in range(reps):
+        flush.fill_(1)
+        torch.cuda._sleep(100000)  # about 50 us at 2 GHz
+        ev[2 * i].record()
+        fn()
+        ev[2 * i + 1].record()
+    torch.cuda.synchronize()
+    return sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(reps)) / reps
+
+
 def secondary(torch, fos, dev, pk) -> dict:
     res = {}
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > L2, written between calls
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > L2, written before each call
 
-    def measure(name, bits, reps=10, **opts):
+    def measure(name, bits, reps=20, **opts):
         x = _to_dev(torch, bits, dev)
         q = fos.Quantizer(*x.shape, device=dev, **opts)
 
-        def call():
-            flush.fill_(1)
-            q(x)
-
-        t_flush = _time_calls(torch, lambda: flush.fill_(1), reps)
-        t = _time_calls(torch, call, reps) - t_flush
+        t = _time_flushed(torch, flush, lambda: q(x), reps)
         n = x.numel()
         gbs = n * BYTES_PER_ELEM_QUANT / (t * 1e-3) / 1e9
         res[name] = {"ms": round(t, 4), "gelem_s": round(n / (t * 1e-3) / 1e9, 2),
@@ -541,12 +554,7 @@ def secondary(torch, fos, dev, pk) -> dict:
             amax = fos.tensor_amax(x, hadamard=opts.get("hadamard", False), transpose=opts.get("transpose", False),
                                    hadamard_seed=opts.get("hadamard_seed", 0))
             qd = fos.Quantizer(*x.shape, device=dev, tensor_amax=amax, **opts)
-
-            def call_d():
-                flush.fill_(1)
-                qd(x)
-
-            td = _time_calls(torch, call_d, reps) - t_flush
+            td = _time_flushed(torch, flush, lambda: qd(x), reps)
             gd = n * BYTES_PER_ELEM_QUANT / (td * 1e-3) / 1e9
             res[name]["amax_supplied"] = {"ms": round(td, 4), "gelem_s": round(n / (td * 1e-3) / 1e9, 2),
                                           "algorithmic_gbs": round(gd, 1), "frac_of_hbm": round(gd / pk["hbm_gbs"], 4)}
@@ -563,9 +571,10 @@ def secondary(torch, fos, dev, pk) -> dict:
     # MXFP4 with the 4/6 choice: no tensor scale, so one pass; 2 + 0.5 + 1/32
     # algorithmic bytes per value
     g = _to_dev(torch, grad, dev)
-    fos.quantize_mxfp4(g)
-    t_flush = _time_calls(torch, lambda: flush.fill_(1), 10)
-    t = _time_calls(torch, lambda: (flush.fill_(1), fos.quantize_mxfp4(g)), 10) - t_flush
+    mq = fos.quantize_mxfp4(g)  # outputs reused: the call below is the C entry point alone
+    t = _time_flushed(torch, flush, lambda: fos.fos_quantize_mxfp4(
+        g.data_ptr(), g.shape[0], g.shape[1], g.stride(0), fos.FOS_SCALE_4OVER6, mq.sf_layout, mq.codes.data_ptr(),
+        mq.codes.stride(0), mq.scales.data_ptr(), 0, torch.cuda.current_stream().cuda_stream), 10)
     gbs = g.numel() * (2 + 0.5 + 1 / 32) / (t * 1e-3) / 1e9
     res["gradient_mxfp4"] = {"ms": round(t, 4), "gelem_s": round(g.numel() / (t * 1e-3) / 1e9, 2),
                              "algorithmic_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4),
