@@ -117,6 +117,21 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
   return r;
 }
 
+// Four pairs of signed grid values -> one word of E2M1 codes (byte k: pair k,
+// the even element in the low nibble); exact for grid values.
+__device__ __forceinline__ uint32_t e2m1x8(F2 g0, F2 g1, F2 g2, F2 g3) {
+  uint32_t w;
+  asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c3, %8, %7;\n\t"
+      "mov.b32 %0, {c0, c1, c2, c3};\n\t}"
+      : "=r"(w)
+      : "f"(g0.x), "f"(g0.y), "f"(g1.x), "f"(g1.y), "f"(g2.x), "f"(g2.y), "f"(g3.x), "f"(g3.y));
+  return w;
+}
+
 // ------------------------------------------------ float pairs in 64 bits
 // A value pair (element 2k in the low half) kept in one 64-bit register, the
 // operand form of the packed f32x2 instructions.
@@ -486,24 +501,38 @@ __device__ __forceinline__ F2 sr_mag2(F2 aq, F2 n) {
 // n < 2^24).  Both candidates round with the same u = n * 2^-24.
 __device__ __forceinline__ float sr_draw(uint32_t w) { return (float)(w >> 8); }
 
-// Stochastic-rounding codes of one candidate (yp: the block's values as
-// packed pairs; n the elements' draws, sr_draw).
-__device__ __forceinline__ float cand_sr16(const uint64_t (&yp)[8], float inv, const float (&n)[16], uint32_t& lo,
-                                           uint32_t& hi) {
-  F2 acc{0.0f, 0.0f};
-  uint32_t b[8];
+// A block's magnitudes |y| and signs (+-1.0 with y's sign bit) as pairs,
+// once per block: both stochastic-rounding candidates use them.
+__device__ __forceinline__ void sr_split16(const uint64_t (&yp)[8], F2 (&ay)[8], F2 (&sg)[8]) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const F2 q = mul2(unpack_f2(yp[k]), F2{inv, inv});
-    const F2 aq{fabsf(q.x), fabsf(q.y)};
-    const F2 g = sr_mag2(aq, F2{n[2 * k], n[2 * k + 1]});
-    // the grid value with q's sign converts exactly
-    b[k] = e2m1x2(copysignf(g.x, q.x), copysignf(g.y, q.y));
-    const F2 r = sub2(aq, g);
-    acc = fma2(r, r, acc);
+    const F2 v = unpack_f2(yp[k]);
+    ay[k] = F2{fabsf(v.x), fabsf(v.y)};
+    sg[k] = F2{copysignf(1.0f, v.x), copysignf(1.0f, v.y)};
   }
-  lo = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-  hi = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+}
+
+// Stochastic-rounding codes of one candidate (ay, sg from sr_split16; n the
+// elements' draws, sr_draw).  |q| = |y| * inv exactly (inv > 0), and the
+// signed grid value g * sign carries q's sign, zeros included, as the codes
+// need.
+__device__ __forceinline__ float cand_sr16(const F2 (&ay)[8], const F2 (&sg)[8], float inv, const float (&n)[16],
+                                           uint32_t& lo, uint32_t& hi) {
+  F2 acc{0.0f, 0.0f};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {  // each code word as soon as its 4 pairs are done
+    F2 gs[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int k = 4 * h + j;
+      const F2 aq = mul2(ay[k], F2{inv, inv});
+      const F2 g = sr_mag2(aq, F2{n[2 * k], n[2 * k + 1]});
+      gs[j] = mul2(g, sg[k]);
+      const F2 r = sub2(aq, g);
+      acc = fma2(r, r, acc);
+    }
+    (h ? hi : lo) = e2m1x8(gs[0], gs[1], gs[2], gs[3]);
+  }
   return __fadd_rn(acc.x, acc.y);
 }
 

@@ -303,6 +303,8 @@ __device__ __forceinline__ void quant_block_tab(const uint64_t (&yp)[8], float a
                                                 uint32_t& hi, uint32_t& sf, bool& four) {
   const uint32_t pair = candidate_scales(ab, tc);
   const uint32_t sf6 = pair & 0xFFu, sf4 = pair >> 8;
+  F2 ay[8], sg[8];
+  if (SR) sr_split16(yp, ay, sg);
   uint32_t lo6 = 0, hi6 = 0, lo4 = 0, hi4 = 0;
   float E6 = 0.0f, E4 = 0.0f;
 #pragma unroll
@@ -313,7 +315,7 @@ __device__ __forceinline__ void quant_block_tab(const uint64_t (&yp)[8], float a
     uint32_t l, h;
     float S;
     if (SR) {
-      S = cand_sr16(yp, t.x, n_sr, l, h);
+      S = cand_sr16(ay, sg, t.x, n_sr, l, h);
     } else {
       const uint64_t inv2 = pack_f2(t.x, t.x);
       uint64_t acc = 0ull;
@@ -879,8 +881,12 @@ __device__ __forceinline__ float half_tree_sum(float v) {
   return v;
 }
 
+// The stochastic-rounding forms are held to three CTAs per SM (80 registers):
+// unbounded, the compiler gives the 4/6 one 124 and it runs two.  The RNE
+// forms get no bound (0): an explicit one, even 1 or 4, changed their code
+// and measured slower.
 template <int RULE, bool RHT, bool SR, bool TRANS>
-__global__ void __launch_bounds__(256) quant_2d_kernel(QuantParams p) {
+__global__ void __launch_bounds__(256, SR ? 3 : 0) quant_2d_kernel(QuantParams p) {
   __shared__ float s_red[33];
   __shared__ float2 s_tab[128];
   pdl_wait();  // the partial maxima come from the amax launch before this one
@@ -948,7 +954,11 @@ __global__ void __launch_bounds__(256) quant_2d_kernel(QuantParams p) {
       uint32_t l, h;
       float S;
       if (SR) {
-        S = cand_sr16(yp, tb.x, n_sr, l, h);
+        // split per candidate here: kept across both, it cost this kernel a
+        // CTA per SM (125 registers)
+        F2 ay[8], sg[8];
+        sr_split16(yp, ay, sg);
+        S = cand_sr16(ay, sg, tb.x, n_sr, l, h);
       } else {
         const uint64_t inv2 = pack_f2(tb.x, tb.x);
         uint64_t acc = 0ull;
