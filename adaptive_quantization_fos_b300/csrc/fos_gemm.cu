@@ -76,6 +76,7 @@ struct GemmArgs {
   const float* stb;
   uint16_t* c;
   int64_t ldc;
+  int32_t c32;           // C 32-byte aligned with ldc % 16 == 0: 32-byte stores
   int32_t m, n, k;       // k in values
   int32_t tiles_m, tiles_n, num_kb;
   int64_t sf_ktiles;     // 512-byte scale chunks per 128-row tile (K / 64 NVFP4, ceil(K / 128) MXFP4)
@@ -232,6 +233,13 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
   return v;
+}
+
+// 32 bytes to global memory with the streaming (evict-first) hint; p 32-byte aligned.
+__device__ __forceinline__ void st_cs_v8(void* p, const uint4& a, const uint4& b) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z),
+               "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -573,23 +581,30 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_a, const CUtenso
       for (int jh = 0; jh < 8; ++jh) {
         const int j = jh >> 1;
         if (row < args.m) {
+          // columns 16 * (jh & 1) .. +15 of this 32-column group: 32 bytes of C
+          uint4 o[2];
 #pragma unroll
-          for (int g = 2 * (jh & 1); g < 2 * (jh & 1) + 2; ++g) {
-            const int col = col0 + 32 * j + 8 * g;
-            if (col < args.n) {
-              uint4 o;
-              o.x = pack_bf16x2(__fmul_rn(__uint_as_float(v[j][8 * g + 0]), alpha),
-                                __fmul_rn(__uint_as_float(v[j][8 * g + 1]), alpha));
-              o.y = pack_bf16x2(__fmul_rn(__uint_as_float(v[j][8 * g + 2]), alpha),
-                                __fmul_rn(__uint_as_float(v[j][8 * g + 3]), alpha));
-              o.z = pack_bf16x2(__fmul_rn(__uint_as_float(v[j][8 * g + 4]), alpha),
-                                __fmul_rn(__uint_as_float(v[j][8 * g + 5]), alpha));
-              o.w = pack_bf16x2(__fmul_rn(__uint_as_float(v[j][8 * g + 6]), alpha),
-                                __fmul_rn(__uint_as_float(v[j][8 * g + 7]), alpha));
-              // streaming store: C is written once, and keeping it out of
-              // L2's way keeps the operand tiles there for the next tiles
-              __stcs(reinterpret_cast<uint4*>(dst + 32 * j + 8 * g), o);
-            }
+          for (int e = 0; e < 2; ++e) {
+            const int g = 2 * (jh & 1) + e;
+            o[e].x = pack_bf16x2(__fmul_rn(__uint_as_float(v[j][8 * g + 0]), alpha),
+                                 __fmul_rn(__uint_as_float(v[j][8 * g + 1]), alpha));
+            o[e].y = pack_bf16x2(__fmul_rn(__uint_as_float(v[j][8 * g + 2]), alpha),
+                                 __fmul_rn(__uint_as_float(v[j][8 * g + 3]), alpha));
+            o[e].z = pack_bf16x2(__fmul_rn(__uint_as_float(v[j][8 * g + 4]), alpha),
+                                 __fmul_rn(__uint_as_float(v[j][8 * g + 5]), alpha));
+            o[e].w = pack_bf16x2(__fmul_rn(__uint_as_float(v[j][8 * g + 6]), alpha),
+                                 __fmul_rn(__uint_as_float(v[j][8 * g + 7]), alpha));
+          }
+          // streaming stores: C is written once, and keeping it out of L2's
+          // way keeps the operand tiles there for the next tiles; a whole
+          // 32-byte sector per store where C's alignment allows it
+          const int col = col0 + 32 * j + 16 * (jh & 1);
+          uint16_t* p = dst + 32 * j + 16 * (jh & 1);
+          if (args.c32 && col + 16 <= args.n) {
+            st_cs_v8(p, o[0], o[1]);
+          } else {
+            if (col < args.n) __stcs(reinterpret_cast<uint4*>(p), o[0]);
+            if (col + 8 < args.n) __stcs(reinterpret_cast<uint4*>(p + 8), o[1]);
           }
         }
         __syncwarp();
@@ -777,6 +792,7 @@ fos_status launch_gemm(const Operand& A, const Operand& B, void* Cout, int64_t l
   a.stb = B.tensor_scale;
   a.c = static_cast<uint16_t*>(Cout);
   a.ldc = ldc;
+  a.c32 = aligned(Cout, 32) && ldc % 16 == 0;
   a.m = (int32_t)A.rows;
   a.n = (int32_t)B.rows;
   a.k = (int32_t)A.cols;

@@ -108,6 +108,29 @@ def test_gemm_options_and_zero_rows():
     check_rows(C, oracle.dequantize(qa), oracle.dequantize(qw), np.arange(M))
 
 
+@pytest.mark.parametrize("N,ld", [(264, 272), (256, 264), (384, 400)])
+def test_gemm_output_inside_wider_rows(N, ld):
+    """C as a view into wider rows: 32-byte stores where the row stride and the
+    columns allow them (ld % 16 == 0), 16-byte stores otherwise and at a
+    ragged right edge; the columns past N must stay untouched."""
+    import torch
+
+    import adaptive_quantization_fos_b300 as fos
+    import oracle
+
+    M, K = 200, 256
+    qa = oracle.quantize(mixed_bits(M, K, seed=N + ld))
+    qw = oracle.quantize(workloads.student_t(N, K, seed=N + 2 * ld))
+    full = torch.full((M, ld), float("nan"), dtype=torch.bfloat16, device="cuda")
+    C = full[:, :N]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fos.gemm(upload(qa), upload(qw), out=C, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.isnan(full[:, N:]).all(), "columns past N were written"
+    check_rows(C, oracle.dequantize(qa), oracle.dequantize(qw), np.arange(M))
+
+
 def test_gemm_many_tiles_per_cta():
     """More output tiles than SMs: each persistent CTA runs several tiles and
     the accumulator barrier phases wrap."""
