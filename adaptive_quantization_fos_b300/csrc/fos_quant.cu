@@ -716,13 +716,26 @@ __global__ void __launch_bounds__(MODE == kRowsChained ? 320 : 256, MODE == kRow
 // arrivals); a lane reads each row's 2*CPL bytes from shared memory.
 // Stochastic rounding: the Philox call for (row, 4-column group j) serves
 // lanes 2j and 2j+1; lane 2j computes rows 0-7 of the block-row and lane
-// 2j+1 rows 8-15, and each pair swaps the two words the other needs.  Each
-// block's 8 code bytes and scale byte are stored as soon as it is done; the
-// task's 4 block-rows fill 32 contiguous code bytes of each output row, which
-// L2 merges.
+// 2j+1 rows 8-15, and each pair swaps the two words the other needs.  A
+// task's 4 block-rows give each output row 32 contiguous code bytes: a lane
+// parks each block's 8 bytes in its own entries of the warp's output buffer
+// (entry (k, lane) holds output row CPL * lane + k; 40-byte entries, so the
+// 8-byte writes of a warp and its 32-byte reads fall on distinct banks) and
+// keeps the scale bytes in a word, then stores each output row's 32 code
+// bytes and 4 scale bytes at once after the task's last block-row: whole
+// sectors rather than four 8-byte pieces each.
 constexpr int kColWarps = 8;
-constexpr int kColWarpSmem = 8192;  // ring bytes per warp: 4 slots x 2 KB (CPL 2) or 2 x 4 KB (CPL 4)
-constexpr int kColSmemBytes = kColWarps * kColWarpSmem;
+constexpr int kColWarpSmem = 8192;   // ring bytes per warp: 4 slots x 2 KB (CPL 2) or 2 x 4 KB (CPL 4)
+constexpr int kColOutPitch = 40;     // bytes per output-buffer entry (32 used)
+constexpr int kColWarpOut = 4 * 32 * kColOutPitch;  // up to CPL = 4 entries per lane
+constexpr int kColSmemBytes = kColWarps * (kColWarpSmem + kColWarpOut);
+
+// 32 bytes to global memory; p 32-byte aligned.
+__device__ __forceinline__ void st_v8(void* p, const uint4& a, const uint4& b) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w),
+               "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
 
 template <int RULE, bool RHT, bool SR>
 __global__ void __launch_bounds__(256, 2) quant_cols_kernel(QuantParams p) {
@@ -747,6 +760,7 @@ __global__ void __launch_bounds__(256, 2) quant_cols_kernel(QuantParams p) {
   const int64_t gw = (int64_t)blockIdx.x * kColWarps + warp;
   const uint64_t stream_once = l2_policy_evict_first();
   uint8_t* slots = c_smem + warp * (kColSlots * kColSlotBytes);
+  uint8_t* obuf = c_smem + kColWarps * kColWarpSmem + warp * kColWarpOut + lane * kColOutPitch;
   const uint32_t bar0 = smem_addr(&s_bar[warp * kColSlots]);
 
   // producer cursor (all lanes): the next (task, block-row) to fetch
@@ -784,6 +798,9 @@ __global__ void __launch_bounds__(256, 2) quant_cols_kernel(QuantParams p) {
     const int64_t g = t / nch, ch = t - g * nch;
     const int64_t c0 = ch * kCW;
     const int nsub = nbr - 4 * g < 4 ? (int)(nbr - 4 * g) : 4;
+    uint32_t sfw[CPL];  // the task's scale bytes of each output row, block-row sub in byte sub
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) sfw[k] = 0u;
     for (int sub = 0; sub < nsub; ++sub) {
       if (!__all_sync(0xFFFFFFFFu, mbar_wait_for(bar0 + 8u * slot, ph, p.timeout_ns))) {
         failed = true;
@@ -845,12 +862,39 @@ __global__ void __launch_bounds__(256, 2) quant_cols_kernel(QuantParams p) {
         uint32_t lo, hi, sf;
         bool four;
         quant_block_tab<RULE, SR>(yp, ab, tc, s_tab, (k & 1) ? n1 : n0, lo, hi, sf, four);
+        *reinterpret_cast<uint2*>(obuf + k * 32 * kColOutPitch + 8 * sub) = make_uint2(lo, hi);
+        sfw[k] |= sf << (8 * sub);
         const int64_t orow = c0 + CPL * lane + k;  // output row = source column
-        if (orow < p.cols) {
-          *reinterpret_cast<uint2*>(p.codes + orow * p.ld_codes + rb * 8) = make_uint2(lo, hi);
-          p.sf[sf_off(orow, rb, nbr, p.sf_layout)] = (uint8_t)sf;
-          if (p.choice) p.choice[orow * nbr + rb] = four ? 1 : 0;
-        }
+        if (p.choice && orow < p.cols) p.choice[orow * nbr + rb] = four ? 1 : 0;
+      }
+    }
+    if (failed) break;
+    // the task's output: each row's codes for block-rows 4g .. 4g + nsub - 1
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) {
+      const int64_t orow = c0 + CPL * lane + k;
+      if (orow >= p.cols) continue;
+      const uint8_t* e = obuf + k * 32 * kColOutPitch;
+      uint8_t* dst = p.codes + orow * p.ld_codes + 4 * g * 8;
+      const uint2 d0 = *reinterpret_cast<const uint2*>(e), d1 = *reinterpret_cast<const uint2*>(e + 8);
+      const uint2 d2 = *reinterpret_cast<const uint2*>(e + 16), d3 = *reinterpret_cast<const uint2*>(e + 24);
+      if (nsub == 4 && (reinterpret_cast<uintptr_t>(dst) & 31) == 0) {
+        st_v8(dst, make_uint4(d0.x, d0.y, d1.x, d1.y), make_uint4(d2.x, d2.y, d3.x, d3.y));
+      } else {
+        const uint2 d[4] = {d0, d1, d2, d3};
+#pragma unroll
+        for (int sub = 0; sub < 4; ++sub)
+          if (sub < nsub) *reinterpret_cast<uint2*>(dst + 8 * sub) = d[sub];
+      }
+      // the 4 scale bytes of block-rows 4g .. 4g+3 are one aligned word in both
+      // layouts (row-major when the output rows' scale counts are a multiple of 4)
+      const int64_t so = sf_off(orow, 4 * g, nbr, p.sf_layout);
+      if (nsub == 4 && (p.sf_layout == FOS_SF_SWIZZLED_128x4 || (nbr & 3) == 0)) {
+        *reinterpret_cast<uint32_t*>(p.sf + so) = sfw[k];
+      } else {
+#pragma unroll
+        for (int sub = 0; sub < 4; ++sub)
+          if (sub < nsub) p.sf[sf_off(orow, 4 * g + sub, nbr, p.sf_layout)] = (uint8_t)(sfw[k] >> (8 * sub));
       }
     }
   }
