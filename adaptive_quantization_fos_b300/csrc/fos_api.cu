@@ -194,7 +194,10 @@ fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
   int64_t tasks;
   if (two_d) {
     kind = tr ? 3 : 2;
-    tasks = (rows / 16) * ((cols / 16 + 1) / 2);
+    // warp tasks of 16 source rows x 4 tiles (stochastic rounding, not
+    // transposed) or 2
+    const int tpt = (!tr && opt->rounding == FOS_ROUND_STOCHASTIC) ? 4 : 2;
+    tasks = (rows / 16) * ((cols / 16 + tpt - 1) / tpt);
   } else if (tr) {
     kind = 1;
     // warp tasks of 64 source rows x 128 (RNE) or 64 (stochastic) source columns

@@ -939,115 +939,168 @@ __global__ void __launch_bounds__(256, SR ? 3 : 0) quant_2d_kernel(QuantParams p
   __syncthreads();
   const uint32_t rht_mask = RHT ? rht_sign_mask(p.hk0, p.hk1) : 0u;
   const int lane = threadIdx.x & 31, i = lane & 15, half = lane >> 4;
-  const int64_t ntc = p.cols >> 4;               // tiles along source columns
-  const int64_t npair = (ntc + 1) >> 1;
-  const int64_t n_tasks = (p.rows >> 4) * npair;
+  const int64_t ntc = p.cols >> 4;  // tiles along source columns
+  // warp task: 16 source rows x 2 * kSteps tiles, two tiles per step (one per
+  // half).  With stochastic rounding a row-major task takes 4 tiles, so that
+  // each source row's 32 code bytes and 4 scale bytes of the task are stored
+  // at once after the second step: whole sectors rather than 8-byte pieces.
+  // The RNE form stores per tile: the two steps' registers cost it a CTA per
+  // SM and measured slower.  Transposed output rows differ between the
+  // halves, so there a task is one step.
+  constexpr bool kBand = SR && !TRANS;
+  constexpr int kSteps = kBand ? 2 : 1;
+  const int64_t ngrp = (ntc + 2 * kSteps - 1) / (2 * kSteps);
+  const int64_t n_tasks = (p.rows >> 4) * ngrp;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n_tasks; t += nwarps) {
-    const int64_t tr = t / npair, tcol = (t - tr * npair) * 2 + half;
-    const bool valid = tcol < ntc;  // uniform within each 16-lane half
-    const int64_t r = tr * 16 + i, c0 = tcol * 16;
-    uint32_t wv[8];
-    float y[16];
-    if (valid) {
-      load_block16(p.x + r * p.ld + c0, p.aligned32, wv);
-    } else {
+    const int64_t tr = t / ngrp, tile0 = (t - tr * ngrp) * 2 * kSteps;
+    const int nt = ntc - tile0 < 2 * kSteps ? (int)(ntc - tile0) : 2 * kSteps;  // tiles of this task
+    uint32_t lo0 = 0, hi0 = 0, sf0 = 0, lo1 = 0, hi1 = 0, sf1 = 0;  // kBand: each step's results
+    auto step = [&](const int s2) {  // tiles tile0 + 2 * s2 (first half) and + 1 (second)
+      const int64_t tcol = tile0 + 2 * s2 + half;
+      const bool valid = 2 * s2 + half < nt;  // uniform within each 16-lane half
+      const int64_t r = tr * 16 + i, c0 = tcol * 16;
+      uint32_t wv[8];
+      float y[16];
+      if (valid) {
+        load_block16(p.x + r * p.ld + c0, p.aligned32, wv);
+      } else {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) wv[k] = 0u;
-    }
-    if (RHT && !TRANS) {
-      unpack16(wv, rht_mask, y);
-      hadamard16(y);
-    } else {
-      unpack16(wv, 0u, y);
-    }
-    if (RHT && TRANS) {
-      // transform down the 16 source rows of each column: across lanes
-      if ((rht_mask >> i) & 1u) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) y[j] = -y[j];
+        for (int k = 0; k < 8; ++k) wv[k] = 0u;
       }
+      if (RHT && !TRANS) {
+        unpack16(wv, rht_mask, y);
+        hadamard16(y);
+      } else {
+        unpack16(wv, 0u, y);
+      }
+      if (RHT && TRANS) {
+        // transform down the 16 source rows of each column: across lanes
+        if ((rht_mask >> i) & 1u) {
 #pragma unroll
-      for (int h = 1; h < 16; h <<= 1) {
-        const bool upper = (i & h) != 0;
+          for (int j = 0; j < 16; ++j) y[j] = -y[j];
+        }
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          float o = __shfl_xor_sync(0xFFFFFFFFu, y[j], h);
-          y[j] = upper ? __fsub_rn(o, y[j]) : __fadd_rn(y[j], o);
+        for (int h = 1; h < 16; h <<= 1) {
+          const bool upper = (i & h) != 0;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float o = __shfl_xor_sync(0xFFFFFFFFu, y[j], h);
+            y[j] = upper ? __fsub_rn(o, y[j]) : __fadd_rn(y[j], o);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) y[j] = __fmul_rn(y[j], 0.25f);
+      }
+      const float ab = half_max(absmax16(y));
+      float n_sr[16];
+      sr_draws16<SR>((uint64_t)r * (uint64_t)p.cols + (uint64_t)c0, p, n_sr);
+      const uint32_t pair = candidate_scales(ab, tc);
+      const uint32_t sf6 = pair & 0xFFu, sf4 = pair >> 8;
+      uint64_t yp[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) yp[j] = pack_f2(y[2 * j], y[2 * j + 1]);
+      uint32_t lo6 = 0, hi6 = 0, lo4 = 0, hi4 = 0;
+      float E6 = 0.0f, E4 = 0.0f;
+#pragma unroll
+      for (int cnd = 0; cnd < 2; ++cnd) {
+        if (cnd == 0 && RULE == FOS_SCALE_4) continue;
+        if (cnd == 1 && RULE == FOS_SCALE_6) continue;
+        const uint32_t sfc = cnd == 0 ? sf6 : sf4;
+        const float2 tb = s_tab[sfc];
+        uint32_t l, h;
+        float S;
+        if (SR) {
+          // split per candidate here: kept across both, it cost this kernel a
+          // CTA per SM (125 registers)
+          F2 ay[8], sg[8];
+          sr_split16(yp, ay, sg);
+          S = cand_sr16(ay, sg, tb.x, n_sr, l, h);
+        } else {
+          const uint64_t inv2 = pack_f2(tb.x, tb.x);
+          uint64_t acc = 0ull;
+          const uint64_t a[4] = {yp[0], yp[1], yp[2], yp[3]}, b[4] = {yp[4], yp[5], yp[6], yp[7]};
+          l = cand_rne8(a, inv2, acc);
+          h = cand_rne8(b, inv2, acc);
+          const F2 e = unpack_f2(acc);
+          S = __fadd_rn(e.x, e.y);
+        }
+        if (sfc == 0) S = sumsq16(y);  // a zero scale flushes the row: its error is sum y^2
+        S = half_tree_sum(S);
+        const float E = sfc ? __fmul_rn(S, tb.y) : S;
+        if (cnd == 0) {
+          lo6 = l; hi6 = h; E6 = E;
+        } else {
+          lo4 = l; hi4 = h; E4 = E;
         }
       }
-#pragma unroll
-      for (int j = 0; j < 16; ++j) y[j] = __fmul_rn(y[j], 0.25f);
-    }
-    const float ab = half_max(absmax16(y));
-    float n_sr[16];
-    sr_draws16<SR>((uint64_t)r * (uint64_t)p.cols + (uint64_t)c0, p, n_sr);
-    const uint32_t pair = candidate_scales(ab, tc);
-    const uint32_t sf6 = pair & 0xFFu, sf4 = pair >> 8;
-    uint64_t yp[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) yp[j] = pack_f2(y[2 * j], y[2 * j + 1]);
-    uint32_t lo6 = 0, hi6 = 0, lo4 = 0, hi4 = 0;
-    float E6 = 0.0f, E4 = 0.0f;
-#pragma unroll
-    for (int cnd = 0; cnd < 2; ++cnd) {
-      if (cnd == 0 && RULE == FOS_SCALE_4) continue;
-      if (cnd == 1 && RULE == FOS_SCALE_6) continue;
-      const uint32_t sfc = cnd == 0 ? sf6 : sf4;
-      const float2 tb = s_tab[sfc];
-      uint32_t l, h;
-      float S;
-      if (SR) {
-        // split per candidate here: kept across both, it cost this kernel a
-        // CTA per SM (125 registers)
-        F2 ay[8], sg[8];
-        sr_split16(yp, ay, sg);
-        S = cand_sr16(ay, sg, tb.x, n_sr, l, h);
+      const bool four = (RULE == FOS_SCALE_4) || (RULE == FOS_SCALE_4OVER6 && E4 < E6);
+      const uint32_t lo = four ? lo4 : lo6, hi = four ? hi4 : hi6, sf = four ? sf4 : sf6;
+      if (kBand) {
+        if (valid && p.choice) p.choice[r * p.nb + tcol] = four ? 1 : 0;
+        if (s2 == 0) {
+          lo0 = lo; hi0 = hi; sf0 = sf;
+        } else {
+          lo1 = lo; hi1 = hi; sf1 = sf;
+        }
+      } else if (!TRANS) {
+        if (valid) {
+          *reinterpret_cast<uint2*>(p.codes + r * p.ld_codes + tcol * 8) = make_uint2(lo, hi);
+          p.sf[sf_off(r, tcol, p.nb, p.sf_layout)] = (uint8_t)sf;
+          if (p.choice) p.choice[r * p.nb + tcol] = four ? 1 : 0;
+        }
       } else {
-        const uint64_t inv2 = pack_f2(tb.x, tb.x);
-        uint64_t acc = 0ull;
-        const uint64_t a[4] = {yp[0], yp[1], yp[2], yp[3]}, b[4] = {yp[4], yp[5], yp[6], yp[7]};
-        l = cand_rne8(a, inv2, acc);
-        h = cand_rne8(b, inv2, acc);
-        const F2 e = unpack_f2(acc);
-        S = __fadd_rn(e.x, e.y);
-      }
-      if (sfc == 0) S = sumsq16(y);  // a zero scale flushes the row: its error is sum y^2
-      S = half_tree_sum(S);
-      const float E = sfc ? __fmul_rn(S, tb.y) : S;
-      if (cnd == 0) {
-        lo6 = l; hi6 = h; E6 = E;
-      } else {
-        lo4 = l; hi4 = h; E4 = E;
-      }
-    }
-    const bool four = (RULE == FOS_SCALE_4) || (RULE == FOS_SCALE_4OVER6 && E4 < E6);
-    const uint32_t lo = four ? lo4 : lo6, hi = four ? hi4 : hi6, sf = four ? sf4 : sf6;
-    if (!TRANS) {
-      if (valid) {
-        *reinterpret_cast<uint2*>(p.codes + r * p.ld_codes + tcol * 8) = make_uint2(lo, hi);
-        p.sf[sf_off(r, tcol, p.nb, p.sf_layout)] = (uint8_t)sf;
-        if (p.choice) p.choice[r * p.nb + tcol] = four ? 1 : 0;
-      }
-    } else {
-      // lane i collects output row (source column) c0 + i: nibble i of every
-      // source row j of its tile, j = 0..15 in order along the output row
-      uint32_t olo = 0, ohi = 0;
+        // lane i collects output row (source column) c0 + i: nibble i of every
+        // source row j of its tile, j = 0..15 in order along the output row
+        uint32_t olo = 0, ohi = 0;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        uint32_t slo = __shfl_sync(0xFFFFFFFFu, lo, (half << 4) | j);
-        uint32_t shi = __shfl_sync(0xFFFFFFFFu, hi, (half << 4) | j);
-        uint32_t nib = ((i < 8 ? slo : shi) >> (4 * (i & 7))) & 15u;
-        if (j < 8)
-          olo |= nib << (4 * j);
-        else
-          ohi |= nib << (4 * (j - 8));
+        for (int j = 0; j < 16; ++j) {
+          uint32_t slo = __shfl_sync(0xFFFFFFFFu, lo, (half << 4) | j);
+          uint32_t shi = __shfl_sync(0xFFFFFFFFu, hi, (half << 4) | j);
+          uint32_t nib = ((i < 8 ? slo : shi) >> (4 * (i & 7))) & 15u;
+          if (j < 8)
+            olo |= nib << (4 * j);
+          else
+            ohi |= nib << (4 * (j - 8));
+        }
+        if (valid) {
+          const int64_t orow = c0 + i;
+          *reinterpret_cast<uint2*>(p.codes + orow * p.ld_codes + tr * 8) = make_uint2(olo, ohi);
+          p.sf[sf_off(orow, tr, p.nb, p.sf_layout)] = (uint8_t)sf;
+          if (p.choice) p.choice[orow * p.nb + tr] = four ? 1 : 0;
+        }
       }
-      if (valid) {
-        const int64_t orow = c0 + i;
-        *reinterpret_cast<uint2*>(p.codes + orow * p.ld_codes + tr * 8) = make_uint2(olo, ohi);
-        p.sf[sf_off(orow, tr, p.nb, p.sf_layout)] = (uint8_t)sf;
-        if (p.choice) p.choice[orow * p.nb + tr] = four ? 1 : 0;
+    };
+    step(0);
+    if (kBand && nt > 2) step(1);
+    if (kBand) {
+      // lane i of the first half stores source row i's tiles tile0 .. tile0+3:
+      // its own (steps 0 and 1) and its partner's in the second half
+      const uint32_t plo0 = __shfl_down_sync(0xFFFFFFFFu, lo0, 16), phi0 = __shfl_down_sync(0xFFFFFFFFu, hi0, 16);
+      const uint32_t psf0 = __shfl_down_sync(0xFFFFFFFFu, sf0, 16), plo1 = __shfl_down_sync(0xFFFFFFFFu, lo1, 16);
+      const uint32_t phi1 = __shfl_down_sync(0xFFFFFFFFu, hi1, 16), psf1 = __shfl_down_sync(0xFFFFFFFFu, sf1, 16);
+      if (half == 0) {
+        const int64_t r = tr * 16 + i;
+        uint8_t* cd = p.codes + r * p.ld_codes + tile0 * 8;
+        if (nt == 4 && (reinterpret_cast<uintptr_t>(cd) & 31) == 0) {
+          st_v8(cd, make_uint4(lo0, hi0, plo0, phi0), make_uint4(lo1, hi1, plo1, phi1));
+        } else {
+          const uint2 c[4] = {make_uint2(lo0, hi0), make_uint2(plo0, phi0), make_uint2(lo1, hi1),
+                              make_uint2(plo1, phi1)};
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (k < nt) *reinterpret_cast<uint2*>(cd + 8 * k) = c[k];
+        }
+        // tile0 % 4 == 0: the 4 scale bytes are one aligned word in both
+        // layouts (row-major when the rows' scale counts are a multiple of 4)
+        const uint32_t sfw = sf0 | (psf0 << 8) | (sf1 << 16) | (psf1 << 24);
+        if (nt == 4 && (p.sf_layout == FOS_SF_SWIZZLED_128x4 || (p.nb & 3) == 0)) {
+          *reinterpret_cast<uint32_t*>(p.sf + sf_off(r, tile0, p.nb, p.sf_layout)) = sfw;
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (k < nt) p.sf[sf_off(r, tile0 + k, p.nb, p.sf_layout)] = (uint8_t)(sfw >> (8 * k));
+        }
       }
     }
   }
