@@ -407,6 +407,18 @@ def test_sf_swizzle_offsets_by_hand(orc):
     assert not a.sf[mask].any(), "pad bytes must be zero"
 
 
+@pytest.mark.parametrize("rows,nb", [(1, 1), (3, 3), (127, 4), (128, 5), (130, 33), (300, 9), (257, 128)])
+def test_sf_to_rowmajor_is_the_offset_map(orc, rows, nb):
+    """The tests' gather from a 128x4-tiled scale buffer (used for NVFP4 and for
+    MXFP4's cols/32 scale columns alike) reads, for every (row, column), the
+    byte the C oracle's offset names, and reaches every real byte once."""
+    size = orc.sf_bytes(rows, nb)
+    where = orc.sf_to_rowmajor(np.arange(size), rows, nb)
+    want = np.array([[orc.sf_offset(r, c, nb) for c in range(nb)] for r in range(rows)])
+    assert np.array_equal(where, want)
+    assert np.unique(where).size == rows * nb and where.max() < size
+
+
 def test_gemm_reference_closed_form(orc):
     K, M, N = 64, 3, 5
     A = np.full((M, K), 1.5, np.float32)
