@@ -10,7 +10,8 @@ pytestmark = pytest.mark.gpu
 
 RNE, SR = 0, 1
 SHAPES_1D = [(1, 16), (3, 48), (300, 1040), (129, 512), (64, 4096), (256, 256)]
-SHAPES_16 = [(16, 16), (48, 80), (304, 1040), (128, 4096)]
+# cols / 16 = 1, 5, 6, 7, 65, 256: a 2D row band of 4 tiles ends with 1, 2, 3 or 0 over
+SHAPES_16 = [(16, 16), (48, 80), (32, 96), (64, 112), (304, 1040), (128, 4096)]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -62,12 +63,15 @@ def test_2d(shape, transpose, rounding, hadamard):
           sr_seed=5, hadamard=hadamard, hadamard_seed=7)
 
 
-@pytest.mark.parametrize("kind", [dict(), dict(transpose=True), dict(block_2d=True), dict(hadamard=True)])
+@pytest.mark.parametrize("kind", [dict(), dict(transpose=True), dict(block_2d=True), dict(hadamard=True),
+                                  dict(block_2d=True, rounding=SR, sr_seed=5),
+                                  dict(transpose=True, rounding=SR, sr_seed=5)])
 def test_rowmajor_scale_layout(kind):
     check(mixed_bits(304, 1040, seed=51), sf_layout=1, **kind)
 
 
-@pytest.mark.parametrize("kind", [dict(), dict(transpose=True), dict(block_2d=True)])
+@pytest.mark.parametrize("kind", [dict(), dict(transpose=True), dict(block_2d=True),
+                                  dict(block_2d=True, rounding=SR, sr_seed=6)])
 def test_padded_source_rows(kind):
     check(mixed_bits(48, 160, seed=61), ld_x=168, **kind)
 
