@@ -108,11 +108,12 @@ def test_gemm_options_and_zero_rows():
     check_rows(C, oracle.dequantize(qa), oracle.dequantize(qw), np.arange(M))
 
 
-@pytest.mark.parametrize("N,ld", [(264, 272), (256, 264), (384, 400)])
-def test_gemm_output_inside_wider_rows(N, ld):
-    """C as a view into wider rows: 32-byte stores where the row stride and the
-    columns allow them (ld % 16 == 0), 16-byte stores otherwise and at a
-    ragged right edge; the columns past N must stay untouched."""
+@pytest.mark.parametrize("N,ld,off", [(264, 272, 0), (256, 264, 0), (384, 400, 0), (256, 272, 8)])
+def test_gemm_output_inside_wider_rows(N, ld, off):
+    """C as a view into wider rows, starting `off` columns in: 32-byte stores
+    where C's start and row stride allow them (32-byte aligned, ld % 16 == 0),
+    16-byte stores otherwise (off = 8: a 16-byte aligned start) and at a ragged
+    right edge; the columns outside C must stay untouched."""
     import torch
 
     import adaptive_quantization_fos_b300 as fos
@@ -122,12 +123,12 @@ def test_gemm_output_inside_wider_rows(N, ld):
     qa = oracle.quantize(mixed_bits(M, K, seed=N + ld))
     qw = oracle.quantize(workloads.student_t(N, K, seed=N + 2 * ld))
     full = torch.full((M, ld), float("nan"), dtype=torch.bfloat16, device="cuda")
-    C = full[:, :N]
+    C = full[:, off:off + N]
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     fos.gemm(upload(qa), upload(qw), out=C, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    assert torch.isnan(full[:, N:]).all(), "columns past N were written"
+    assert torch.isnan(full[:, :off]).all() and torch.isnan(full[:, off + N:]).all(), "columns outside C were written"
     check_rows(C, oracle.dequantize(qa), oracle.dequantize(qw), np.arange(M))
 
 

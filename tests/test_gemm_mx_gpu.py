@@ -123,6 +123,29 @@ def test_gemm_mx_scale_per_32_values():
         assert np.array_equal(C.float().cpu().numpy(), ref.astype(np.float32)), f"rule {rule}"
 
 
+@pytest.mark.parametrize("N,ld,off", [(264, 272, 0), (256, 272, 8)])
+def test_gemm_mx_output_inside_wider_rows(N, ld, off):
+    """The MXFP4 contraction's C as a view into wider rows: the 32-byte stores
+    with a ragged last group, and the 16-byte path from a start that is only
+    16-byte aligned; the columns outside C stay untouched."""
+    import torch
+
+    import adaptive_quantization_fos_b300 as fos
+    import oracle
+
+    M, K = 200, 256
+    qa = oracle.quantize_mx(mixed_bits(M, K, seed=N + ld + off))
+    qw = oracle.quantize_mx(workloads.student_t(N, K, seed=N + 3 * ld))
+    full = torch.full((M, ld), float("nan"), dtype=torch.bfloat16, device="cuda")
+    C = full[:, off:off + N]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fos.gemm_mxfp4(upload(qa), upload(qw), out=C, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.isnan(full[:, :off]).all() and torch.isnan(full[:, off + N:]).all(), "columns outside C were written"
+    check_rows(C, oracle.dequantize_mx(qa), oracle.dequantize_mx(qw), np.arange(M))
+
+
 def test_gemm_mx_many_tiles_per_cta():
     """More output tiles than SMs: each persistent CTA runs several tiles."""
     import oracle
