@@ -50,7 +50,7 @@ __global__ void amax_final_kernel(const float* partials, int n, float* out) {
 
 int amax_tasks_grid(int64_t rows, int64_t cols, bool cols_kernel) {
   int64_t tasks = cols_kernel ? (rows / 16) * ((cols + fos::kAmaxColTask - 1) / fos::kAmaxColTask)
-                              : rows * ((cols / 16 + 31) / 32);
+                              : rows * ((cols / 16 + fos::kAmaxRowBlocks - 1) / fos::kAmaxRowBlocks);
   return fos::amax_grid(tasks);
 }
 

@@ -16,6 +16,8 @@ constexpr int kMaxAmaxPartials = 2048;
 // lane, and per warp task.
 constexpr int kAmaxColCPL = 8;
 constexpr int kAmaxColTask = 32 * kAmaxColCPL;
+// The row amax pass: blocks per warp task (4 per lane in flight).
+constexpr int kAmaxRowBlocks = 128;
 // Workspace: the partial maxima, then (at kBarrierOffset) the words of the
 // one-launch row quantizer: the grid barrier's arrival counter, a flag that a
 // CTA which gave up on a wait raises, and the counter of CTAs that finished

@@ -144,6 +144,8 @@ __device__ __forceinline__ float absmax16(const float (&y)[16]) {
   return fmaxf(max3abs(m0, m1, m2), max3abs(m3, m4, y[15]));
 }
 
+// A warp task is a row segment of up to kAmaxRowBlocks blocks (4 KB): each
+// lane has its blocks' four 32-byte loads in flight before it reduces them.
 template <bool RHT>
 __global__ void __launch_bounds__(256) amax_rows_kernel(AmaxParams p) {
   __shared__ float s_red[33];
@@ -151,22 +153,29 @@ __global__ void __launch_bounds__(256) amax_rows_kernel(AmaxParams p) {
   const int lane = threadIdx.x & 31;
   const uint32_t rht_mask = RHT ? rht_sign_mask(p.hk0, p.hk1) : 0u;
   const int64_t nb = p.cols >> 4;
-  const int64_t wpr = (nb + 31) >> 5;
+  const int64_t wpr = (nb + kAmaxRowBlocks - 1) / kAmaxRowBlocks;
   const int64_t n_tasks = p.rows * wpr;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   float m = 0.0f;
   for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n_tasks; t += nwarps) {
-    int64_t r = t / wpr, b = (t - r * wpr) * 32 + lane;
-    if (b >= nb) continue;
-    uint32_t w[8];
-    load_block16(p.x + r * p.ld + b * 16, p.aligned32, w);
-    if (!RHT) {
-      m = fmaxf(m, absmax16_bits(w));
-    } else {
-      float y[16];
-      unpack16(w, rht_mask, y);
-      butterflies16(y);  // 1/4 applied to the maximum below
-      m = fmaxf(m, absmax16(y));
+    const int64_t r = t / wpr, c0 = (t - r * wpr) * kAmaxRowBlocks;
+    const int nblk = nb - c0 < kAmaxRowBlocks ? (int)(nb - c0) : kAmaxRowBlocks;
+    const uint16_t* src = p.x + r * p.ld + (c0 + lane) * 16;
+    uint32_t w[kAmaxRowBlocks / 32][8];
+#pragma unroll
+    for (int j = 0; j < kAmaxRowBlocks / 32; ++j)
+      if (lane + 32 * j < nblk) load_block16(src + 512 * j, p.aligned32, w[j]);
+#pragma unroll
+    for (int j = 0; j < kAmaxRowBlocks / 32; ++j) {
+      if (lane + 32 * j >= nblk) break;
+      if (!RHT) {
+        m = fmaxf(m, absmax16_bits(w[j]));
+      } else {
+        float y[16];
+        unpack16(w[j], rht_mask, y);
+        butterflies16(y);  // 1/4 applied to the maximum below
+        m = fmaxf(m, absmax16(y));
+      }
     }
   }
   if (RHT) m = unscaled_to_amax(m);
