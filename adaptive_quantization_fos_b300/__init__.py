@@ -41,7 +41,7 @@ class fos_quant_options(ctypes.Structure):
         ("transpose", ctypes.c_int32),
         ("hadamard", ctypes.c_int32),
         ("sf_layout", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("one_launch", ctypes.c_int32),
         ("sr_seed", ctypes.c_uint64),
         ("hadamard_seed", ctypes.c_uint64),
         ("tensor_amax", ctypes.c_void_p),
@@ -248,7 +248,7 @@ def _stream_ptr(stream=None) -> int:
 
 def options(*, scale_rule=FOS_SCALE_4OVER6, rounding=FOS_ROUND_RNE, block_2d=False, transpose=False,
             hadamard=False, sf_layout=FOS_SF_SWIZZLED_128x4, sr_seed=0, hadamard_seed=0,
-            tensor_amax=None) -> fos_quant_options:
+            tensor_amax=None, one_launch=False) -> fos_quant_options:
     o = fos_quant_options()
     o.struct_size = ctypes.sizeof(fos_quant_options)
     o.scale_rule = scale_rule
@@ -257,7 +257,7 @@ def options(*, scale_rule=FOS_SCALE_4OVER6, rounding=FOS_ROUND_RNE, block_2d=Fal
     o.transpose = int(bool(transpose))
     o.hadamard = int(bool(hadamard))
     o.sf_layout = sf_layout
-    o.reserved = 0
+    o.one_launch = int(bool(one_launch))
     o.sr_seed = sr_seed
     o.hadamard_seed = hadamard_seed
     o.tensor_amax = None if tensor_amax is None else int(tensor_amax.data_ptr())

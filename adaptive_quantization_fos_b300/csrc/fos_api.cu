@@ -19,7 +19,7 @@ bool valid_options(const fos_quant_options* o) {
   if (o->rounding != FOS_ROUND_RNE && o->rounding != FOS_ROUND_STOCHASTIC) return false;
   if ((o->block_2d | o->transpose | o->hadamard) & ~1) return false;
   if (o->sf_layout != FOS_SF_SWIZZLED_128x4 && o->sf_layout != FOS_SF_ROWMAJOR) return false;
-  return o->reserved == 0;
+  return (o->one_launch & ~1) == 0;
 }
 
 int64_t sf_bytes_of(int64_t R, int64_t nb, int32_t layout) {
@@ -147,7 +147,8 @@ fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
   const bool aligned32 = aligned(x, 32) && ld_x % 16 == 0;
   const bool cols_amax = rht && tr;
   // 1D blocks along rows without a supplied amax: one launch does both passes
-  const bool fused = !tr && !two_d && !opt->tensor_amax;
+  // the one-launch form only on request: two launches measure faster
+  const bool fused = opt->one_launch && !tr && !two_d && !opt->tensor_amax;
   int n_partials = 0;
   if (!opt->tensor_amax && !fused) {
     fos::AmaxParams a{};

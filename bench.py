@@ -770,6 +770,13 @@ def run_case(args) -> None:
         # 12288 x 4096 bf16 (100.7 MB, the gate/up projection shape), no amax
         # supplied: the one-launch quantizer (amax pass, barrier, quantize pass)
         x = _to_dev(torch, workloads.student_t(12288, 4096, seed=9002), dev)
+        q = fos.Quantizer(*x.shape, device=dev, one_launch=True)
+        for _ in range(3):
+            q(x)
+    elif args.case == "quant_rows_two_launch":
+        # the same matrix through the default form: amax pass, then the
+        # quantize pass as its programmatic dependent
+        x = _to_dev(torch, workloads.student_t(12288, 4096, seed=9002), dev)
         q = fos.Quantizer(*x.shape, device=dev)
         for _ in range(3):
             q(x)

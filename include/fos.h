@@ -92,7 +92,8 @@ typedef struct fos_quant_options {
   int32_t transpose;     /* 1: the output describes X^T (blocks run along X's rows) */
   int32_t hadamard;      /* 1: apply the random Hadamard transform first */
   int32_t sf_layout;     /* fos_sf_layout */
-  int32_t reserved;      /* must be 0 */
+  int32_t one_launch;    /* 1: 1D blocks along rows without a supplied amax in one
+                            cooperative launch (fos_quantize); 0: two launches */
   uint64_t sr_seed;      /* key of the stochastic-rounding Philox stream */
   uint64_t hadamard_seed;/* key of the RHT sign vector */
   const float* tensor_amax; /* optional device pointer: use this amax and skip the amax pass */
@@ -155,12 +156,15 @@ fos_status fos_tensor_amax(const void* x, int64_t rows, int64_t cols, int64_t ld
  *             initialisation, and calls sharing one workspace must not
  *             overlap on the GPU.
  * The RHT output is not undone: codes describe the transformed values.
- * 1D blocks along rows without a supplied amax run as one cooperative launch
- * (amax pass, grid barrier in the workspace -- its counter is cleared by a
- * 4-byte cudaMemsetAsync on `stream` first -- and a quantize pass that
- * re-reads the input mostly from L2).  A device wait that runs out (a copy or the grid
- * barrier taking over a second) leaves *tensor_scale = NaN: the outputs are
- * then not valid.
+ * Without a supplied amax the call runs an amax pass, then the quantize pass as
+ * its programmatic dependent (it reads the pass's partial maxima from the
+ * workspace).  With opt->one_launch, 1D blocks along rows run both passes in
+ * one cooperative launch instead (amax pass, grid barrier in the workspace --
+ * its three words are cleared by a 12-byte cudaMemsetAsync on `stream` first
+ * -- and a quantize pass that re-reads the input mostly from L2); the two
+ * launches measure faster on B300.  A device wait that runs out (a copy or the
+ * grid barrier taking over a second) leaves *tensor_scale = NaN: the outputs
+ * are then not valid.
  */
 fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
                         const fos_quant_options* opt, uint8_t* codes, int64_t ld_codes, uint8_t* sf,

@@ -90,6 +90,9 @@ def test_validation_rejects_without_launch(fos):
     bad = fos.options()
     bad.struct_size = 8
     assert q(opt=bad) == INVALID
+    bad = fos.options()
+    bad.one_launch = 2
+    assert q(opt=bad) == INVALID
     t = fos.fos_nvfp4_tensor()
     assert fos.fos_dequantize(t, fake, 0, 64, 0) == INVALID
     assert fos.fos_e2m1_encode(0, 5, 0, 0) == INVALID

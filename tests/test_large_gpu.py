@@ -1,9 +1,11 @@
 """Maximum sizes.  The row quantizer at a size where element indices pass
 2^34, so the stochastic-rounding Philox counter (i / 4) needs its high word,
 and byte offsets pass 2^31: a 262208 x 65536 bf16 gradient (17.2 G values, 34 GB on the
-device), quantized with SR through the one-launch path (amax pass, grid
-barrier, quantize pass).  Rows on both sides of index 2^34 are compared with
-the oracle's quantization of the same rows at the same source indices.
+device), quantized with SR through both forms of the row path: the default
+two launches (amax pass, then the quantize pass) and the one cooperative launch
+(amax pass, grid barrier, quantize pass).  Rows on both sides of index 2^34 are
+compared with the oracle's quantization of the same rows at the same source
+indices.
 
 The matrix repeats one seeded 64-row block, so its amax is the block's; the
 stochastic-rounding words still differ everywhere (they depend on the index).
@@ -41,22 +43,28 @@ def test_sr_rows_beyond_2_pow_34(fos):
     dev_base = torch.from_numpy(base.view(np.int16)).view(torch.bfloat16).cuda()
     x = dev_base.repeat(ROWS // BLOCK_ROWS + 1, 1)[:ROWS]
     assert x.is_contiguous() and x.shape == (ROWS, COLS)
-    q = fos.quantize(x, rounding=fos.FOS_ROUND_STOCHASTIC, sr_seed=77, sf_layout=fos.FOS_SF_ROWMAJOR)
-    torch.cuda.synchronize()
     amax = float(np.abs(workloads.bf16_to_f32(base)).max())
-    # the tensor amax is the block's (the matrix repeats it)
-    assert np.float32(q.tensor_scale.item()) == np.float32(oracle.quantize(base[:1], amax=amax).tensor_scale)
     nb = COLS // 16
     first_beyond = (1 << 34) // COLS  # the first row whose indices reach 2^34
+    expect = {}
     for r in (0, 1, first_beyond - 1, first_beyond, ROWS - 1):
-        row = base[r % BLOCK_ROWS][None, :]
-        o = oracle.quantize(row, rounding=oracle.ROUND_SR, sr_seed=77, amax=amax, sf_layout=oracle.SF_ROWMAJOR,
-                            src_row0=r, src_cols=COLS)
-        got_codes = q.codes[r, : COLS // 2].cpu().numpy()
-        got_sf = q.sf[r * nb:(r + 1) * nb].cpu().numpy()
-        assert np.array_equal(got_codes, o.codes[0]), f"row {r}: codes differ"
-        assert np.array_equal(got_sf, o.sf[:nb]), f"row {r}: scales differ"
-    del x, q
+        expect[r] = oracle.quantize(base[r % BLOCK_ROWS][None, :], rounding=oracle.ROUND_SR, sr_seed=77, amax=amax,
+                                    sf_layout=oracle.SF_ROWMAJOR, src_row0=r, src_cols=COLS)
+    for one_launch in (False, True):
+        q = fos.quantize(x, rounding=fos.FOS_ROUND_STOCHASTIC, sr_seed=77, sf_layout=fos.FOS_SF_ROWMAJOR,
+                         one_launch=one_launch)
+        torch.cuda.synchronize()
+        form = "one launch" if one_launch else "two launches"
+        # the tensor amax is the block's (the matrix repeats it)
+        assert np.float32(q.tensor_scale.item()) == np.float32(oracle.quantize(base[:1], amax=amax).tensor_scale), form
+        for r, o in expect.items():
+            got_codes = q.codes[r, : COLS // 2].cpu().numpy()
+            got_sf = q.sf[r * nb:(r + 1) * nb].cpu().numpy()
+            assert np.array_equal(got_codes, o.codes[0]), f"{form}, row {r}: codes differ"
+            assert np.array_equal(got_sf, o.sf[:nb]), f"{form}, row {r}: scales differ"
+        del q
+        torch.cuda.empty_cache()
+    del x
     torch.cuda.empty_cache()
 
 

@@ -46,6 +46,16 @@ def test_rows_hadamard(shape, rounding):
     check(mixed_bits(*shape, seed=21 + shape[1]), hadamard=True, hadamard_seed=12345, rounding=rounding, sr_seed=3)
 
 
+@pytest.mark.parametrize("shape", SHAPES_1D)
+@pytest.mark.parametrize("kind", [dict(), dict(scale_rule=1), dict(rounding=SR, sr_seed=9),
+                                  dict(hadamard=True, hadamard_seed=4, rounding=SR, sr_seed=2)])
+def test_rows_one_launch(shape, kind):
+    """The cooperative one-launch form of the row quantizer (amax pass, grid
+    barrier, quantize pass) against the oracle, like the two-launch default."""
+    bits = mixed_bits(*shape, seed=61 + shape[0] + shape[1])
+    assert_same(gpu_quantize(bits, one_launch=True, **kind), oracle_quantize(bits, **kind), repr(kind))
+
+
 @pytest.mark.parametrize("shape", SHAPES_16)
 @pytest.mark.parametrize("rounding", [RNE, SR])
 @pytest.mark.parametrize("hadamard", [False, True])
