@@ -48,10 +48,13 @@ __global__ void amax_final_kernel(const float* partials, int n, float* out) {
   if (threadIdx.x == 0) *out = s[0];
 }
 
-int amax_tasks_grid(int64_t rows, int64_t cols, bool cols_kernel) {
+// the grid of launch_amax(hadamard, transpose): the RHT down the columns runs
+// the column kernel, everything else the row kernel
+int amax_tasks_grid(int64_t rows, int64_t cols, bool hadamard, bool transpose) {
+  const bool cols_kernel = hadamard && transpose;
   int64_t tasks = cols_kernel ? (rows / 16) * ((cols + fos::kAmaxColTask - 1) / fos::kAmaxColTask)
                               : rows * ((cols / 16 + fos::kAmaxRowBlocks - 1) / fos::kAmaxRowBlocks);
-  return fos::amax_grid(tasks);
+  return fos::amax_grid(tasks, hadamard, transpose);
 }
 
 }  // namespace
@@ -70,7 +73,7 @@ cudaError_t amax_plain_and_rht_cols(const void* x, int64_t rows, int64_t cols, i
   // the two partial arrays share the workspace's partial-maxima region
   a.partials = static_cast<float*>(workspace);
   a.partials_plain = a.partials + kMaxAmaxPartials / 2;
-  int g = amax_tasks_grid(rows, cols, true);
+  int g = amax_tasks_grid(rows, cols, true, true);
   if (g > kMaxAmaxPartials / 2) g = kMaxAmaxPartials / 2;
   cudaError_t e = launch_amax(a, true, true, g, s);
   if (e != cudaSuccess) return e;
@@ -113,7 +116,6 @@ fos_status fos_tensor_amax(const void* x, int64_t rows, int64_t cols, int64_t ld
                            size_t workspace_bytes, cudaStream_t stream) {
   if (!valid_source(x, rows, cols, ld_x, hadamard && transpose) || !amax_out) return FOS_ERR_INVALID_ARG;
   if (!workspace || workspace_bytes < fos::kQuantWorkspaceBytes || !aligned(workspace, 4)) return FOS_ERR_INVALID_ARG;
-  const bool cols_kernel = hadamard && transpose;
   fos::AmaxParams a{};
   a.x = static_cast<const uint16_t*>(x);
   a.rows = rows;
@@ -123,7 +125,7 @@ fos_status fos_tensor_amax(const void* x, int64_t rows, int64_t cols, int64_t ld
   a.hk1 = (uint32_t)(hadamard_seed >> 32);
   a.aligned32 = aligned(x, 32) && ld_x % 16 == 0;
   a.partials = static_cast<float*>(workspace);
-  const int g = amax_tasks_grid(rows, cols, cols_kernel);
+  const int g = amax_tasks_grid(rows, cols, hadamard != 0, transpose != 0);
   cudaError_t e = fos::launch_amax(a, hadamard != 0, transpose != 0, g, stream);
   if (e != cudaSuccess) return FOS_ERR_CUDA;
   amax_final_kernel<<<1, 256, 0, stream>>>(a.partials, g, amax_out);
@@ -145,9 +147,8 @@ fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
     return FOS_ERR_INVALID_ARG;
 
   const bool aligned32 = aligned(x, 32) && ld_x % 16 == 0;
-  const bool cols_amax = rht && tr;
-  // 1D blocks along rows without a supplied amax: one launch does both passes
-  // the one-launch form only on request: two launches measure faster
+  // 1D blocks along rows without a supplied amax: both passes in one launch
+  // only on request (two launches measure faster)
   const bool fused = opt->one_launch && !tr && !two_d && !opt->tensor_amax;
   int n_partials = 0;
   if (!opt->tensor_amax && !fused) {
@@ -160,7 +161,7 @@ fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
     a.hk1 = (uint32_t)(opt->hadamard_seed >> 32);
     a.aligned32 = aligned32;
     a.partials = static_cast<float*>(workspace);
-    n_partials = amax_tasks_grid(rows, cols, cols_amax);
+    n_partials = amax_tasks_grid(rows, cols, rht, tr);
     if (fos::launch_amax(a, rht, tr, n_partials, stream) != cudaSuccess) return FOS_ERR_CUDA;
   }
 
@@ -275,7 +276,7 @@ fos_status fos_quantize_batch(const fos_quant_job* jobs, int32_t n_jobs, const f
     a.hk1 = (uint32_t)(opt->hadamard_seed >> 32);
     a.aligned32 = aligned(j.x, 32) && j.ld_x % 16 == 0;
     a.partials = slot(0);
-    n_part = amax_tasks_grid(j.rows, j.cols, false);
+    n_part = amax_tasks_grid(j.rows, j.cols, rht, false);
     if (fos::launch_amax(a, rht, false, n_part, stream) != cudaSuccess) return FOS_ERR_CUDA;
   }
   for (int32_t i = 0; i < n_jobs; ++i) {

@@ -76,7 +76,7 @@ struct DequantParams {
   void* out;
 };
 
-int amax_grid(int64_t n_warp_tasks);
+int amax_grid(int64_t n_warp_tasks, bool hadamard, bool transpose);
 int quant_grid(int64_t n_warp_tasks, int kind);
 cudaError_t launch_amax(const AmaxParams& p, bool hadamard, bool transpose, int grid, cudaStream_t s);
 

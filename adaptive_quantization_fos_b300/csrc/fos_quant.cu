@@ -1197,14 +1197,6 @@ static int sm_count() {
   return n > 0 ? n : 148;
 }
 
-int amax_grid(int64_t n_warp_tasks) {
-  int64_t g = (n_warp_tasks + 7) / 8;
-  int64_t cap = (int64_t)sm_count() * 4;
-  if (cap > kMaxAmaxPartials) cap = kMaxAmaxPartials;
-  if (g > cap) g = cap;
-  return (int)(g < 1 ? 1 : g);
-}
-
 cudaError_t launch_amax(const AmaxParams& p, bool hadamard, bool transpose, int grid, cudaStream_t s) {
   if (hadamard && transpose)
     if (p.partials_plain)
@@ -1245,6 +1237,35 @@ static int current_device() {
   return cudaGetDevice(&d) == cudaSuccess ? d : -1;
 }
 
+// Resident CTAs per SM of an amax kernel at 256 threads, found once per device.
+template <typename Fn>
+static int amax_per_sm(Fn fn, std::atomic<int>* per_sm_of) {
+  const int dev = current_device();
+  int n = (dev >= 0 && dev < kMaxDevices) ? per_sm_of[dev].load(std::memory_order_acquire) : 0;
+  if (n == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, 256, 0) != cudaSuccess || n < 1) {
+      (void)cudaGetLastError();  // the query's own error: fall back to four per SM
+      return 4;
+    }
+    if (dev >= 0 && dev < kMaxDevices) per_sm_of[dev].store(n, std::memory_order_release);
+  }
+  return n;
+}
+
+int amax_grid(int64_t n_warp_tasks, bool hadamard, bool transpose) {
+  static std::atomic<int> rows_plain[kMaxDevices], rows_rht[kMaxDevices], cols[kMaxDevices];
+  // one resident wave of the kernel launch_amax picks (the tasks are split
+  // evenly over the grid up front)
+  const int per_sm = hadamard && transpose ? amax_per_sm(amax_cols_kernel<false>, cols)
+                     : hadamard            ? amax_per_sm(amax_rows_kernel<true>, rows_rht)
+                                           : amax_per_sm(amax_rows_kernel<false>, rows_plain);
+  int64_t g = (n_warp_tasks + 7) / 8;
+  int64_t cap = (int64_t)sm_count() * per_sm;
+  if (cap > kMaxAmaxPartials) cap = kMaxAmaxPartials;
+  if (g > cap) g = cap;
+  return (int)(g < 1 ? 1 : g);
+}
+
 template <typename Fn>
 static cudaError_t smem_opt_in(Fn fn, int bytes, std::atomic<int>* done) {
   const int dev = current_device();
@@ -1253,6 +1274,39 @@ static cudaError_t smem_opt_in(Fn fn, int bytes, std::atomic<int>* done) {
   const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess && dev < kMaxDevices) done[dev].store(1, std::memory_order_release);
   return e;
+}
+
+// Cut a quantize launch's grid to the CTAs that fit on the GPU at once (found
+// once per device for each kernel).  The kernels split their tasks evenly over
+// the grid up front, so CTAs beyond one resident wave run as a later, partly
+// filled wave.  Measured on B300: the column kernel 4-5% faster and the RNE 2D
+// kernel 1-3%; the row kernel unchanged; the stochastic-rounding 2D kernel 3%
+// slower, so it keeps its larger grid.
+template <typename Fn>
+static cudaError_t one_wave(Fn fn, int smem, std::atomic<int>* per_sm_of, int* grid) {
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  int per_sm = dev < kMaxDevices ? per_sm_of[dev].load(std::memory_order_acquire) : 0;
+  if (per_sm == 0) {
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, 256, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    if (dev < kMaxDevices) per_sm_of[dev].store(per_sm, std::memory_order_release);
+  }
+  const int64_t cap = (int64_t)per_sm * sm_count();
+  if (*grid > cap) *grid = (int)cap;
+  return cudaSuccess;
+}
+
+template <int RULE, bool RHT, bool SR, bool TRANS>
+static cudaError_t launch_2d(const QuantParams& p, int grid, cudaStream_t s, bool pdl) {
+  auto fn = quant_2d_kernel<RULE, RHT, SR, TRANS>;
+  if constexpr (!SR) {
+    static std::atomic<int> per_sm[kMaxDevices];
+    const cudaError_t e = one_wave(fn, 0, per_sm, &grid);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_params(fn, grid, 256, 0, pdl, p, s);
 }
 
 template <int RULE, bool RHT, bool SR>
@@ -1266,12 +1320,13 @@ static cudaError_t launch_q(const QuantParams& p, int kind, int grid, cudaStream
     }
     case 1: {
       auto fn = quant_cols_kernel<RULE, RHT, SR>;
-      static std::atomic<int> done[kMaxDevices];
-      const cudaError_t e = smem_opt_in(fn, kColSmemBytes, done);
+      static std::atomic<int> done[kMaxDevices], per_sm[kMaxDevices];
+      cudaError_t e = smem_opt_in(fn, kColSmemBytes, done);
+      if (e == cudaSuccess) e = one_wave(fn, kColSmemBytes, per_sm, &grid);
       return e != cudaSuccess ? e : launch_params(fn, grid, 256, kColSmemBytes, pdl, p, s);
     }
-    case 2: return launch_params(quant_2d_kernel<RULE, RHT, SR, false>, grid, 256, 0, pdl, p, s);
-    default: return launch_params(quant_2d_kernel<RULE, RHT, SR, true>, grid, 256, 0, pdl, p, s);
+    case 2: return launch_2d<RULE, RHT, SR, false>(p, grid, s, pdl);
+    default: return launch_2d<RULE, RHT, SR, true>(p, grid, s, pdl);
   }
 }
 
