@@ -336,21 +336,25 @@ def fos_quantize_batch(jobs, opt: fos_quant_options, workspace, workspace_bytes,
 
 class BatchQuantizer:
     """Reusable outputs and workspace for repeated quantization of a fixed set
-    of row-major matrices (e.g. one layer's weights) in one chained batch."""
+    of matrices (e.g. one layer's weights) in one batch call.  shapes are the
+    sources' [rows, cols]; with transpose=True each output is [cols, rows]."""
 
     def __init__(self, shapes, *, device="cuda", with_choice=False, **opts):
         torch = _torch()
         self.opt = options(**opts)
+        self.shapes = [tuple(s) for s in shapes]
+        tr = bool(opts.get("transpose", False))
+        layout = opts.get("sf_layout", FOS_SF_SWIZZLED_128x4)
         self.outs = []
-        for rows, cols in shapes:
-            layout = opts.get("sf_layout", FOS_SF_SWIZZLED_128x4)
-            ldc = max(8, ((cols // 2 + 15) // 16) * 16)
+        for rows, cols in self.shapes:
+            R, C = (cols, rows) if tr else (rows, cols)
+            ldc = max(8, ((C // 2 + 15) // 16) * 16)
             self.outs.append(NVFP4Tensor(
-                codes=torch.empty((rows, ldc), dtype=torch.uint8, device=device),
-                sf=torch.empty(max(1, fos_sf_bytes(rows, cols, layout)), dtype=torch.uint8, device=device),
+                codes=torch.empty((R, ldc), dtype=torch.uint8, device=device),
+                sf=torch.empty(max(1, fos_sf_bytes(R, C, layout)), dtype=torch.uint8, device=device),
                 tensor_scale=torch.empty(1, dtype=torch.float32, device=device),
-                rows=rows, cols=cols, sf_layout=layout,
-                choice=torch.empty((rows, cols // 16), dtype=torch.uint8, device=device) if with_choice else None))
+                rows=R, cols=C, sf_layout=layout,
+                choice=torch.empty((R, C // 16), dtype=torch.uint8, device=device) if with_choice else None))
         self.ws_bytes = fos_quantize_batch_workspace_size(len(self.outs))
         self.workspace = torch.empty(max(1, self.ws_bytes), dtype=torch.uint8, device=device)
         # the job array of the last call, reused while the inputs stay the same
@@ -364,18 +368,18 @@ class BatchQuantizer:
         key = tuple((x.data_ptr(), x.stride(0), x.stride(1)) if x.numel() else (0, 0, 0) for x in xs)
         if key != self._key:
             jobs = []
-            for x, o in zip(xs, self.outs):
-                assert x.dtype == bf16 and x.shape == (o.rows, o.cols)
+            for x, shape, o in zip(xs, self.shapes, self.outs):
+                assert x.dtype == bf16 and tuple(x.shape) == shape
                 assert x.numel() == 0 or x.stride(1) == 1
-                ld = x.stride(0) if x.numel() else max(o.cols, 8)
-                jobs.append(fos_quant_job(x.data_ptr(), o.rows, o.cols, ld, o.codes.data_ptr(),
+                ld = x.stride(0) if x.numel() else max(shape[1], 8)
+                jobs.append(fos_quant_job(x.data_ptr(), shape[0], shape[1], ld, o.codes.data_ptr(),
                                           o.codes.stride(0), o.sf.data_ptr(), o.tensor_scale.data_ptr(),
                                           o.choice.data_ptr() if o.choice is not None else None))
             self._jobs = (fos_quant_job * len(jobs))(*jobs)
             self._key = key
         else:
-            for x, o in zip(xs, self.outs):
-                assert x.dtype == bf16 and x.shape == (o.rows, o.cols)
+            for x, shape in zip(xs, self.shapes):
+                assert x.dtype == bf16 and tuple(x.shape) == shape
         _check(fos_quantize_batch(self._jobs, self.opt, self.workspace.data_ptr(), self.ws_bytes, _stream_ptr(stream)),
                "fos_quantize_batch")
         return self.outs

@@ -48,13 +48,82 @@ __global__ void amax_final_kernel(const float* partials, int n, float* out) {
   if (threadIdx.x == 0) *out = s[0];
 }
 
-// the grid of launch_amax(hadamard, transpose): the RHT down the columns runs
-// the column kernel, everything else the row kernel
+// The warp tasks of launch_amax(hadamard, transpose) over x [rows, cols]: the
+// RHT down the columns runs the column kernel, everything else the row kernel.
+int64_t amax_tasks(int64_t rows, int64_t cols, bool hadamard, bool transpose) {
+  if (hadamard && transpose) return (rows / 16) * ((cols + fos::kAmaxColTask - 1) / fos::kAmaxColTask);
+  return rows * ((cols / 16 + fos::kAmaxRowBlocks - 1) / fos::kAmaxRowBlocks);
+}
+
 int amax_tasks_grid(int64_t rows, int64_t cols, bool hadamard, bool transpose) {
-  const bool cols_kernel = hadamard && transpose;
-  int64_t tasks = cols_kernel ? (rows / 16) * ((cols + fos::kAmaxColTask - 1) / fos::kAmaxColTask)
-                              : rows * ((cols / 16 + fos::kAmaxRowBlocks - 1) / fos::kAmaxRowBlocks);
-  return fos::amax_grid(tasks, hadamard, transpose);
+  return fos::amax_grid(amax_tasks(rows, cols, hadamard, transpose), hadamard, transpose);
+}
+
+// The checks fos_quantize makes of one matrix's source and outputs (less the
+// workspace's).
+bool valid_matrix(const void* x, int64_t rows, int64_t cols, int64_t ld_x, const fos_quant_options* opt,
+                  const uint8_t* codes, int64_t ld_codes, const uint8_t* sf, const float* tensor_scale) {
+  const bool tr = opt->transpose != 0;
+  if (!valid_source(x, rows, cols, ld_x, tr || opt->block_2d)) return false;
+  const int64_t R = tr ? cols : rows, C = tr ? rows : cols;
+  const bool empty = R == 0 || C == 0;
+  if ((!empty && (!codes || !sf)) || !tensor_scale) return false;
+  return ld_codes >= C / 2 && ld_codes % 8 == 0 && aligned(codes, 8) && aligned(sf, 4);
+}
+
+// One matrix's quantize launch: its parameters, with the tensor amax read from
+// amax_src (one float, or n_partials partial maxima), its kernel kind (as
+// launch_quant takes it) and its warp tasks.
+struct QuantLaunch {
+  fos::QuantParams p;
+  int kind;
+  int64_t tasks;
+};
+
+QuantLaunch quant_launch(const void* x, int64_t rows, int64_t cols, int64_t ld_x, const fos_quant_options* opt,
+                         uint8_t* codes, int64_t ld_codes, uint8_t* sf, float* tensor_scale, uint8_t* choice,
+                         const float* amax_src, int n_partials) {
+  const bool tr = opt->transpose != 0, two_d = opt->block_2d != 0, sr = opt->rounding == FOS_ROUND_STOCHASTIC;
+  const int64_t R = tr ? cols : rows, C = tr ? rows : cols, nb = C / 16;
+  QuantLaunch q{};
+  fos::QuantParams& p = q.p;
+  p.x = static_cast<const uint16_t*>(x);
+  p.rows = rows;
+  p.cols = cols;
+  p.ld = ld_x;
+  p.R = R;
+  p.nb = nb;
+  p.codes = codes;
+  p.ld_codes = ld_codes;
+  p.sf = sf;
+  p.sf_layout = opt->sf_layout;
+  p.choice = choice;
+  p.tensor_scale = tensor_scale;
+  p.amax_src = amax_src;
+  p.n_partials = n_partials;
+  p.sr_k0 = (uint32_t)opt->sr_seed;
+  p.sr_k1 = (uint32_t)(opt->sr_seed >> 32);
+  p.hk0 = (uint32_t)opt->hadamard_seed;
+  p.hk1 = (uint32_t)(opt->hadamard_seed >> 32);
+  p.aligned32 = aligned(x, 32) && ld_x % 16 == 0;
+  p.codes16 = aligned(codes, 16) && ld_codes % 16 == 0;
+  p.timeout_ns = fos::kWaitTimeoutNs;
+  if (two_d) {
+    q.kind = tr ? 3 : 2;
+    // warp tasks of 16 source rows x 4 tiles (stochastic rounding, not
+    // transposed) or 2
+    const int tpt = (!tr && sr) ? 4 : 2;
+    q.tasks = (rows / 16) * ((cols / 16 + tpt - 1) / tpt);
+  } else if (tr) {
+    q.kind = 1;
+    // warp tasks of 64 source rows x 128 (RNE) or 64 (stochastic) source columns
+    const int64_t w = sr ? 64 : 128;
+    q.tasks = ((rows / 16 + 3) / 4) * ((cols + w - 1) / w);
+  } else {
+    q.kind = 0;
+    q.tasks = R * ((nb + 127) / 128);
+  }
+  return q;
 }
 
 }  // namespace
@@ -136,17 +205,13 @@ fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
                         uint8_t* codes, int64_t ld_codes, uint8_t* sf, float* tensor_scale, uint8_t* choice,
                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (!valid_options(opt)) return FOS_ERR_INVALID_ARG;
-  const bool tr = opt->transpose != 0, two_d = opt->block_2d != 0, rht = opt->hadamard != 0;
-  if (!valid_source(x, rows, cols, ld_x, tr || two_d)) return FOS_ERR_INVALID_ARG;
-  const int64_t R = tr ? cols : rows, C = tr ? rows : cols, nb = C / 16;
-  const bool empty = R == 0 || C == 0;
-  if ((!empty && (!codes || !sf)) || !tensor_scale) return FOS_ERR_INVALID_ARG;
-  if (ld_codes < C / 2 || ld_codes % 8 != 0 || !aligned(codes, 8) || !aligned(sf, 4)) return FOS_ERR_INVALID_ARG;
+  if (!valid_matrix(x, rows, cols, ld_x, opt, codes, ld_codes, sf, tensor_scale)) return FOS_ERR_INVALID_ARG;
   if (!opt->tensor_amax &&
       (!workspace || workspace_bytes < fos::kQuantWorkspaceBytes || !aligned(workspace, 4)))
     return FOS_ERR_INVALID_ARG;
+  const bool tr = opt->transpose != 0, two_d = opt->block_2d != 0, rht = opt->hadamard != 0;
+  const bool sr = opt->rounding == FOS_ROUND_STOCHASTIC;
 
-  const bool aligned32 = aligned(x, 32) && ld_x % 16 == 0;
   // 1D blocks along rows without a supplied amax: both passes in one launch
   // only on request (two launches measure faster)
   const bool fused = opt->one_launch && !tr && !two_d && !opt->tensor_amax;
@@ -159,69 +224,30 @@ fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
     a.ld = ld_x;
     a.hk0 = (uint32_t)opt->hadamard_seed;
     a.hk1 = (uint32_t)(opt->hadamard_seed >> 32);
-    a.aligned32 = aligned32;
+    a.aligned32 = aligned(x, 32) && ld_x % 16 == 0;
     a.partials = static_cast<float*>(workspace);
     n_partials = amax_tasks_grid(rows, cols, rht, tr);
     if (fos::launch_amax(a, rht, tr, n_partials, stream) != cudaSuccess) return FOS_ERR_CUDA;
   }
 
-  fos::QuantParams p{};
-  p.x = static_cast<const uint16_t*>(x);
-  p.rows = rows;
-  p.cols = cols;
-  p.ld = ld_x;
-  p.R = R;
-  p.nb = nb;
-  p.codes = codes;
-  p.ld_codes = ld_codes;
-  p.sf = sf;
-  p.sf_layout = opt->sf_layout;
-  p.choice = choice;
-  p.tensor_scale = tensor_scale;
-  p.amax_src = opt->tensor_amax ? opt->tensor_amax : static_cast<const float*>(workspace);
-  p.n_partials = n_partials;
-  p.sr_k0 = (uint32_t)opt->sr_seed;
-  p.sr_k1 = (uint32_t)(opt->sr_seed >> 32);
-  p.hk0 = (uint32_t)opt->hadamard_seed;
-  p.hk1 = (uint32_t)(opt->hadamard_seed >> 32);
-  p.aligned32 = aligned32;
-  p.codes16 = aligned(codes, 16) && ld_codes % 16 == 0;
-  p.timeout_ns = fos::kWaitTimeoutNs;
+  QuantLaunch q = quant_launch(x, rows, cols, ld_x, opt, codes, ld_codes, sf, tensor_scale, choice,
+                               opt->tensor_amax ? opt->tensor_amax : static_cast<const float*>(workspace),
+                               n_partials);
   if (fused) {
-    p.ws_partials = static_cast<float*>(workspace);
-    p.ws_barrier = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + fos::kBarrierOffset);
-  }
-
-  int kind;
-  int64_t tasks;
-  if (two_d) {
-    kind = tr ? 3 : 2;
-    // warp tasks of 16 source rows x 4 tiles (stochastic rounding, not
-    // transposed) or 2
-    const int tpt = (!tr && opt->rounding == FOS_ROUND_STOCHASTIC) ? 4 : 2;
-    tasks = (rows / 16) * ((cols / 16 + tpt - 1) / tpt);
-  } else if (tr) {
-    kind = 1;
-    // warp tasks of 64 source rows x 128 (RNE) or 64 (stochastic) source columns
-    tasks = ((rows / 16 + 3) / 4) * ((cols + (opt->rounding == FOS_ROUND_STOCHASTIC ? 63 : 127)) /
-                                     (opt->rounding == FOS_ROUND_STOCHASTIC ? 64 : 128));
+    q.p.ws_partials = static_cast<float*>(workspace);
+    q.p.ws_barrier = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + fos::kBarrierOffset);
+    if (fos::launch_quant_rows_fused(q.p, opt->scale_rule, rht, sr, q.tasks, stream) != cudaSuccess)
+      return FOS_ERR_CUDA;
   } else {
-    kind = 0;
-    tasks = R * ((nb + 127) / 128);
-  }
-  const bool sr = opt->rounding == FOS_ROUND_STOCHASTIC;
-  if (fused) {
-    if (fos::launch_quant_rows_fused(p, opt->scale_rule, rht, sr, tasks, stream) != cudaSuccess) return FOS_ERR_CUDA;
-  } else {
-    const int grid = fos::quant_grid(tasks, kind);
+    const int grid = fos::quant_grid(q.tasks, q.kind);
     // after this call's own amax launch, the quantize launch may overlap its
     // tail; after the caller's work (a supplied amax), it may not: that work
     // may still be writing x
-    if (fos::launch_quant(p, opt->scale_rule, kind, rht, sr, grid, stream, n_partials > 0) != cudaSuccess)
+    if (fos::launch_quant(q.p, opt->scale_rule, q.kind, rht, sr, grid, stream, n_partials > 0) != cudaSuccess)
       return FOS_ERR_CUDA;
   }
-  if (opt->sf_layout == FOS_SF_SWIZZLED_128x4 && (R % 128 != 0 || nb % 4 != 0)) {
-    if (fos::launch_sf_pad(sf, sf_bytes_of(R, nb, opt->sf_layout), R, nb, stream) != cudaSuccess)
+  if (opt->sf_layout == FOS_SF_SWIZZLED_128x4 && (q.p.R % 128 != 0 || q.p.nb % 4 != 0)) {
+    if (fos::launch_sf_pad(sf, sf_bytes_of(q.p.R, q.p.nb, opt->sf_layout), q.p.R, q.p.nb, stream) != cudaSuccess)
       return FOS_ERR_CUDA;
   }
   return FOS_OK;
@@ -236,37 +262,21 @@ fos_status fos_quantize_batch_workspace_size(int32_t n_jobs, size_t* bytes) {
 fos_status fos_quantize_batch(const fos_quant_job* jobs, int32_t n_jobs, const fos_quant_options* opt,
                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (!valid_options(opt) || n_jobs < 0 || (n_jobs > 0 && !jobs)) return FOS_ERR_INVALID_ARG;
-  if (opt->transpose || opt->block_2d || opt->tensor_amax) return FOS_ERR_UNSUPPORTED;
+  if (opt->tensor_amax) return FOS_ERR_UNSUPPORTED;
   if (n_jobs == 0) return FOS_OK;
   if (!workspace || workspace_bytes < (size_t)n_jobs * fos::kBarrierOffset || !aligned(workspace, 4))
     return FOS_ERR_INVALID_ARG;
   for (int32_t i = 0; i < n_jobs; ++i) {
     const fos_quant_job& j = jobs[i];
-    if (!valid_source(j.x, j.rows, j.cols, j.ld_x, false)) return FOS_ERR_INVALID_ARG;
-    const bool empty = j.rows == 0 || j.cols == 0;
-    if ((!empty && (!j.codes || !j.sf)) || !j.tensor_scale) return FOS_ERR_INVALID_ARG;
-    if (j.ld_codes < j.cols / 2 || j.ld_codes % 8 != 0 || !aligned(j.codes, 8) || !aligned(j.sf, 4))
+    if (!valid_matrix(j.x, j.rows, j.cols, j.ld_x, opt, j.codes, j.ld_codes, j.sf, j.tensor_scale))
       return FOS_ERR_INVALID_ARG;
   }
-  const bool rht = opt->hadamard != 0, sr = opt->rounding == FOS_ROUND_STOCHASTIC;
+  const bool tr = opt->transpose != 0, two_d = opt->block_2d != 0, rht = opt->hadamard != 0;
+  const bool sr = opt->rounding == FOS_ROUND_STOCHASTIC;
   auto slot = [&](int32_t i) {
     return reinterpret_cast<float*>(static_cast<char*>(workspace) + (size_t)i * fos::kBarrierOffset);
   };
-  // The scale pads first (bytes no quantize launch writes), so that the
-  // quantize launches follow one another directly: each may then start while
-  // its predecessor finishes (programmatic dependent launch).
-  for (int32_t i = 0; i < n_jobs; ++i) {
-    const fos_quant_job& j = jobs[i];
-    const int64_t nb = j.cols / 16;
-    if (opt->sf_layout == FOS_SF_SWIZZLED_128x4 && (j.rows % 128 != 0 || nb % 4 != 0)) {
-      if (fos::launch_sf_pad(j.sf, sf_bytes_of(j.rows, nb, opt->sf_layout), j.rows, nb, stream) != cudaSuccess)
-        return FOS_ERR_CUDA;
-    }
-  }
-  // job 0's block maxima: the amax pass on its own
-  int n_part;
-  {
-    const fos_quant_job& j = jobs[0];
+  auto amax_of = [&](const fos_quant_job& j, float* partials) {
     fos::AmaxParams a{};
     a.x = static_cast<const uint16_t*>(j.x);
     a.rows = j.rows;
@@ -275,49 +285,71 @@ fos_status fos_quantize_batch(const fos_quant_job* jobs, int32_t n_jobs, const f
     a.hk0 = (uint32_t)opt->hadamard_seed;
     a.hk1 = (uint32_t)(opt->hadamard_seed >> 32);
     a.aligned32 = aligned(j.x, 32) && j.ld_x % 16 == 0;
-    a.partials = slot(0);
-    n_part = amax_tasks_grid(j.rows, j.cols, rht, false);
-    if (fos::launch_amax(a, rht, false, n_part, stream) != cudaSuccess) return FOS_ERR_CUDA;
-  }
+    a.partials = partials;
+    return a;
+  };
+  // The scale pads first (bytes no quantize launch writes), so that the
+  // quantize launches follow one another directly: each may then start while
+  // its predecessor finishes (programmatic dependent launch).
   for (int32_t i = 0; i < n_jobs; ++i) {
     const fos_quant_job& j = jobs[i];
-    const int64_t nb = j.cols / 16;
-    fos::QuantParams p{};
-    p.x = static_cast<const uint16_t*>(j.x);
-    p.rows = j.rows;
-    p.cols = j.cols;
-    p.ld = j.ld_x;
-    p.R = j.rows;
-    p.nb = nb;
-    p.codes = j.codes;
-    p.ld_codes = j.ld_codes;
-    p.sf = j.sf;
-    p.sf_layout = opt->sf_layout;
-    p.choice = j.choice;
-    p.tensor_scale = j.tensor_scale;
-    p.amax_src = slot(i);
-    p.n_partials = n_part;
-    p.sr_k0 = (uint32_t)opt->sr_seed;
-    p.sr_k1 = (uint32_t)(opt->sr_seed >> 32);
-    p.hk0 = (uint32_t)opt->hadamard_seed;
-    p.hk1 = (uint32_t)(opt->hadamard_seed >> 32);
-    p.aligned32 = aligned(j.x, 32) && j.ld_x % 16 == 0;
-    p.codes16 = aligned(j.codes, 16) && j.ld_codes % 16 == 0;
-    p.timeout_ns = fos::kWaitTimeoutNs;
+    const int64_t R = tr ? j.cols : j.rows, nb = (tr ? j.rows : j.cols) / 16;
+    if (opt->sf_layout == FOS_SF_SWIZZLED_128x4 && (R % 128 != 0 || nb % 4 != 0)) {
+      if (fos::launch_sf_pad(j.sf, sf_bytes_of(R, nb, opt->sf_layout), R, nb, stream) != cudaSuccess)
+        return FOS_ERR_CUDA;
+    }
+  }
+
+  if (tr || two_d) {
+    // Transposed or 2D jobs: the amax passes of up to kAmaxBatchJobs jobs in
+    // one launch, then one quantize launch per job, back to back.
+    for (int32_t g0 = 0; g0 < n_jobs; g0 += fos::kAmaxBatchJobs) {
+      fos::AmaxBatch b{};
+      b.n_jobs = n_jobs - g0 < fos::kAmaxBatchJobs ? n_jobs - g0 : fos::kAmaxBatchJobs;
+      int64_t total = 0;
+      for (int32_t k = 0; k < b.n_jobs; ++k) {
+        const fos_quant_job& j = jobs[g0 + k];
+        b.job[k] = amax_of(j, slot(g0 + k));
+        total += amax_tasks(j.rows, j.cols, rht, tr);
+      }
+      int grid = 0;
+      if (fos::launch_amax_batch(b, rht, tr, total, &grid, stream) != cudaSuccess) return FOS_ERR_CUDA;
+      // the quantize launches of this group (each job's grid partial maxima);
+      // the next group's amax launch follows them as a plain launch
+      for (int32_t k = 0; k < b.n_jobs; ++k) {
+        const fos_quant_job& j = jobs[g0 + k];
+        const QuantLaunch q = quant_launch(j.x, j.rows, j.cols, j.ld_x, opt, j.codes, j.ld_codes, j.sf,
+                                           j.tensor_scale, j.choice, slot(g0 + k), grid);
+        if (fos::launch_quant(q.p, opt->scale_rule, q.kind, rht, sr, fos::quant_grid(q.tasks, q.kind), stream,
+                              true) != cudaSuccess)
+          return FOS_ERR_CUDA;
+      }
+    }
+    return FOS_OK;
+  }
+
+  // Blocks along rows: job 0's block maxima in an amax launch of their own,
+  // then launch i quantizes job i while taking job i+1's.
+  int n_part = amax_tasks_grid(jobs[0].rows, jobs[0].cols, rht, false);
+  if (fos::launch_amax(amax_of(jobs[0], slot(0)), rht, false, n_part, stream) != cudaSuccess) return FOS_ERR_CUDA;
+  for (int32_t i = 0; i < n_jobs; ++i) {
+    const fos_quant_job& j = jobs[i];
+    QuantLaunch q = quant_launch(j.x, j.rows, j.cols, j.ld_x, opt, j.codes, j.ld_codes, j.sf, j.tensor_scale,
+                                 j.choice, slot(i), n_part);
     if (i + 1 < n_jobs) {
-      // quantize job i while taking job i+1's block maxima
       const fos_quant_job& nx = jobs[i + 1];
-      p.next_x = static_cast<const uint16_t*>(nx.x);
-      p.next_rows = nx.rows;
-      p.next_cols = nx.cols;
-      p.next_ld = nx.ld_x;
-      p.next_partials = slot(i + 1);
+      q.p.next_x = static_cast<const uint16_t*>(nx.x);
+      q.p.next_rows = nx.rows;
+      q.p.next_cols = nx.cols;
+      q.p.next_ld = nx.ld_x;
+      q.p.next_partials = slot(i + 1);
       const int g = fos::chained_grid();
-      if (fos::launch_quant_rows_chained(p, opt->scale_rule, rht, sr, g, stream) != cudaSuccess) return FOS_ERR_CUDA;
+      if (fos::launch_quant_rows_chained(q.p, opt->scale_rule, rht, sr, g, stream) != cudaSuccess)
+        return FOS_ERR_CUDA;
       n_part = g;
     } else {
-      const int64_t tasks = j.rows * ((nb + 127) / 128);
-      if (fos::launch_quant(p, opt->scale_rule, 0, rht, sr, fos::quant_grid(tasks, 0), stream, true) != cudaSuccess)
+      if (fos::launch_quant(q.p, opt->scale_rule, 0, rht, sr, fos::quant_grid(q.tasks, 0), stream, true) !=
+          cudaSuccess)
         return FOS_ERR_CUDA;
     }
   }

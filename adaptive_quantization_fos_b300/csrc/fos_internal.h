@@ -37,6 +37,13 @@ struct AmaxParams {
   float* partials_plain;  // optional (RHT down columns only): also max |x| untransformed
 };
 
+// The amax passes of up to kAmaxBatchJobs jobs in one launch.
+constexpr int kAmaxBatchJobs = 32;
+struct AmaxBatch {
+  AmaxParams job[kAmaxBatchJobs];
+  int32_t n_jobs;
+};
+
 struct QuantParams {
   const uint16_t* x;
   int64_t rows, cols, ld;  // source matrix
@@ -79,6 +86,11 @@ struct DequantParams {
 int amax_grid(int64_t n_warp_tasks, bool hadamard, bool transpose);
 int quant_grid(int64_t n_warp_tasks, int kind);
 cudaError_t launch_amax(const AmaxParams& p, bool hadamard, bool transpose, int grid, cudaStream_t s);
+// The amax passes of b.n_jobs jobs (kernel chosen as launch_amax chooses) in
+// one launch of *grid CTAs: one resident wave, at most kMaxAmaxPartials and
+// at most (total_tasks + 7) / 8.  Each job gets *grid partial maxima.
+cudaError_t launch_amax_batch(const AmaxBatch& b, bool hadamard, bool transpose, int64_t total_tasks, int* grid,
+                              cudaStream_t s);
 
 // From one read of x [rows, cols] (rows % 16 == 0, 16-byte aligned, ld % 8 == 0):
 // out[0] = max |x| and out[1] = max |y| for y the RHT of x down its columns

@@ -146,18 +146,17 @@ __device__ __forceinline__ float absmax16(const float (&y)[16]) {
 
 // A warp task is a row segment of up to kAmaxRowBlocks blocks (4 KB): each
 // lane has its blocks' four 32-byte loads in flight before it reduces them.
+// The thread's maximum over warp tasks gw, gw + nwarps, ... of p (with RHT:
+// of the transform along the rows, its 1/4 applied).
 template <bool RHT>
-__global__ void __launch_bounds__(256) amax_rows_kernel(AmaxParams p) {
-  __shared__ float s_red[33];
-  pdl_launch_dependents();  // the next launch may start its own reads meanwhile
+__device__ __forceinline__ float amax_rows_share(const AmaxParams& p, int64_t gw, int64_t nwarps) {
   const int lane = threadIdx.x & 31;
   const uint32_t rht_mask = RHT ? rht_sign_mask(p.hk0, p.hk1) : 0u;
   const int64_t nb = p.cols >> 4;
   const int64_t wpr = (nb + kAmaxRowBlocks - 1) / kAmaxRowBlocks;
   const int64_t n_tasks = p.rows * wpr;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   float m = 0.0f;
-  for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n_tasks; t += nwarps) {
+  for (int64_t t = gw; t < n_tasks; t += nwarps) {
     const int64_t r = t / wpr, c0 = (t - r * wpr) * kAmaxRowBlocks;
     const int nblk = nb - c0 < kAmaxRowBlocks ? (int)(nb - c0) : kAmaxRowBlocks;
     const uint16_t* src = p.x + r * p.ld + (c0 + lane) * 16;
@@ -178,7 +177,15 @@ __global__ void __launch_bounds__(256) amax_rows_kernel(AmaxParams p) {
       }
     }
   }
-  if (RHT) m = unscaled_to_amax(m);
+  return RHT ? unscaled_to_amax(m) : m;
+}
+
+template <bool RHT>
+__global__ void __launch_bounds__(256) amax_rows_kernel(AmaxParams p) {
+  __shared__ float s_red[33];
+  pdl_launch_dependents();  // the next launch may start its own reads meanwhile
+  const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  float m = amax_rows_share<RHT>(p, gw, ((int64_t)gridDim.x * blockDim.x) >> 5);
   m = block_max(m, s_red);
   if (threadIdx.x == 0) p.partials[blockIdx.x] = m;
 }
@@ -189,18 +196,18 @@ __global__ void __launch_bounds__(256) amax_rows_kernel(AmaxParams p) {
 // column's magnitudes before the butterflies: the sign flips do not change
 // them) into p.partials_plain.  Two CTAs per SM at 128 registers (a few bytes
 // spilled) measured faster than one at 142, and than 4 columns per lane.
+// The thread's maximum over column warp tasks gw, gw + nwarps, ... of p (the
+// transform down the columns, its 1/4 applied); with PLAIN, *plain gets the
+// maximum of the untransformed values.
 template <bool PLAIN>
-__global__ void __launch_bounds__(256, 2) amax_cols_kernel(AmaxParams p) {
+__device__ __forceinline__ float amax_cols_share(const AmaxParams& p, int64_t gw, int64_t nwarps, float* plain) {
   constexpr int W = kAmaxColCPL / 2;  // words per row and lane
-  __shared__ float s_red[33];
-  pdl_launch_dependents();  // the quantize launch may start its own reads meanwhile
   const int lane = threadIdx.x & 31;
   const uint32_t rht_mask = rht_sign_mask(p.hk0, p.hk1);
   const int64_t ngroups = (p.cols + kAmaxColTask - 1) / kAmaxColTask;
   const int64_t n_tasks = (p.rows >> 4) * ngroups;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   float m = 0.0f, mp = 0.0f;  // mp: PLAIN's maximum
-  for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n_tasks; t += nwarps) {
+  for (int64_t t = gw; t < n_tasks; t += nwarps) {
     int64_t rb = t / ngroups, c0 = (t - rb * ngroups) * kAmaxColTask + kAmaxColCPL * lane;
     if (c0 >= p.cols) continue;  // cols % 16 == 0: the lane's columns all exist
     uint32_t d[16][W];
@@ -229,12 +236,50 @@ __global__ void __launch_bounds__(256, 2) amax_cols_kernel(AmaxParams p) {
       m = fmaxf(m, absmax16(y));
     }
   }
-  m = unscaled_to_amax(m);
+  if (PLAIN) *plain = mp;
+  return unscaled_to_amax(m);
+}
+
+// RHT down columns: a lane owns kAmaxColCPL adjacent columns x 16 rows, so a
+// warp reads 64 * kAmaxColCPL contiguous bytes of each of the 16 rows.  With
+// PLAIN, the same pass also takes max |x| of the untransformed values (the
+// column's magnitudes before the butterflies: the sign flips do not change
+// them) into p.partials_plain.  Two CTAs per SM at 128 registers (a few bytes
+// spilled) measured faster than one at 142, and than 4 columns per lane.
+template <bool PLAIN>
+__global__ void __launch_bounds__(256, 2) amax_cols_kernel(AmaxParams p) {
+  __shared__ float s_red[33];
+  pdl_launch_dependents();  // the quantize launch may start its own reads meanwhile
+  const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  float mp = 0.0f;
+  float m = amax_cols_share<PLAIN>(p, gw, ((int64_t)gridDim.x * blockDim.x) >> 5, &mp);
   m = block_max(m, s_red);
   if (threadIdx.x == 0) p.partials[blockIdx.x] = m;
   if (PLAIN) {
     mp = block_max(mp, s_red);
     if (threadIdx.x == 0) p.partials_plain[blockIdx.x] = mp;
+  }
+}
+
+// The amax passes of several jobs in one launch (a batch of transposed or 2D
+// jobs): every CTA takes its share of each job in turn and leaves one partial
+// maximum per job, at the job's partials[blockIdx.x].  MODE 0: rows, 1: rows
+// with the RHT, 2: the RHT down the columns.
+template <int MODE>
+__global__ void __launch_bounds__(256, MODE == 2 ? 2 : 0) amax_batch_kernel(const __grid_constant__ AmaxBatch b) {
+  __shared__ float s_red[33];
+  pdl_launch_dependents();  // the first quantize launch may start its own reads meanwhile
+  const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int j = 0; j < b.n_jobs; ++j) {
+    const AmaxParams& p = b.job[j];
+    float m;
+    if constexpr (MODE == 2)
+      m = amax_cols_share<false>(p, gw, nwarps, nullptr);
+    else
+      m = amax_rows_share<MODE == 1>(p, gw, nwarps);
+    m = block_max(m, s_red);
+    if (threadIdx.x == 0) p.partials[blockIdx.x] = m;
   }
 }
 
@@ -1264,6 +1309,28 @@ int amax_grid(int64_t n_warp_tasks, bool hadamard, bool transpose) {
   if (cap > kMaxAmaxPartials) cap = kMaxAmaxPartials;
   if (g > cap) g = cap;
   return (int)(g < 1 ? 1 : g);
+}
+
+template <int MODE>
+static cudaError_t launch_amax_batch_mode(const AmaxBatch& b, int64_t total_tasks, int* grid, cudaStream_t s) {
+  auto fn = amax_batch_kernel<MODE>;
+  static std::atomic<int> per_sm_of[kMaxDevices];
+  const int per_sm = amax_per_sm(fn, per_sm_of);
+  int64_t g = (total_tasks + 7) / 8;
+  int64_t cap = (int64_t)sm_count() * per_sm;
+  if (cap > kMaxAmaxPartials) cap = kMaxAmaxPartials;
+  if (g > cap) g = cap;
+  *grid = (int)(g < 1 ? 1 : g);
+  fn<<<*grid, 256, 0, s>>>(b);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_amax_batch(const AmaxBatch& b, bool hadamard, bool transpose, int64_t total_tasks, int* grid,
+                              cudaStream_t s) {
+  if (b.n_jobs < 1 || b.n_jobs > kAmaxBatchJobs) return cudaErrorInvalidValue;
+  if (hadamard && transpose) return launch_amax_batch_mode<2>(b, total_tasks, grid, s);
+  if (hadamard) return launch_amax_batch_mode<1>(b, total_tasks, grid, s);
+  return launch_amax_batch_mode<0>(b, total_tasks, grid, s);
 }
 
 template <typename Fn>

@@ -581,9 +581,38 @@ def secondary(torch, fos, dev, pk) -> dict:
                              "shape": list(g.shape), "options": "MXFP4, 4/6 choice between the MX exponent and one "
                                                                 "more, RNE, single pass"}
     del g, grad
+    res["weights_layout_batch"] = weights_layout_batch(torch, fos, dev, pk, flush)
     res["linear_forward"] = linear_forward(torch, fos, dev, pk)
     res["linear_backward"] = linear_backward(torch, fos, dev, pk)
     return res
+
+
+def weights_layout_batch(torch, fos, dev, pk, flush) -> dict:
+    """The Qwen3-8B layer weight set quantized transposed (W^T, as the dgrad
+    product reads it) and in 2D 16x16 tiles: one fos_quantize_batch call (one
+    amax launch for all seven, then the seven quantize launches) against seven
+    fos_quantize calls, each call or set timed with L2 flushed before it."""
+    mats = workloads.qwen3_8b_weights()
+    order = sorted(mats, key=lambda k: mats[k].size)
+    xs = [_to_dev(torch, mats[k], dev) for k in order]
+    n = sum(x.numel() for x in xs)
+    out = {"values": n}
+    for name, opts in (("transposed", dict(transpose=True)), ("2d", dict(block_2d=True))):
+        bq = fos.BatchQuantizer([tuple(x.shape) for x in xs], device=dev, **opts)
+        qs = [fos.Quantizer(*x.shape, device=dev, **opts) for x in xs]
+
+        def separate():
+            for q, x in zip(qs, xs):
+                q(x)
+
+        tb = _time_flushed(torch, flush, lambda: bq(xs), 10)
+        ts = _time_flushed(torch, flush, separate, 10)
+        gbs = n * BYTES_PER_ELEM_QUANT / (tb * 1e-3) / 1e9
+        out[name] = {"batch_ms": round(tb, 4), "separate_calls_ms": round(ts, 4),
+                     "gelem_s": round(n / (tb * 1e-3) / 1e9, 2), "algorithmic_gbs": round(gbs, 1),
+                     "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4), "options": opts}
+        del bq, qs
+    return out
 
 
 def linear_backward(torch, fos, dev, pk) -> dict:

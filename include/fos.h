@@ -172,15 +172,16 @@ fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
                         cudaStream_t stream);
 
 /* One matrix of a batch (fos_quantize_batch): source and outputs as in
- * fos_quantize, with blocks along the rows (no transpose, no 2D tiles). */
+ * fos_quantize under the batch's options.  R_out x C_out is rows x cols, or
+ * cols x rows when opt->transpose is set. */
 typedef struct fos_quant_job {
   const void* x;        /* device bf16 [rows, cols], row stride ld_x elements */
   int64_t rows, cols, ld_x;
-  uint8_t* codes;       /* device, rows x ld_codes bytes */
+  uint8_t* codes;       /* device, R_out x ld_codes bytes */
   int64_t ld_codes;
-  uint8_t* sf;          /* device, fos_sf_bytes(rows, cols, opt->sf_layout) bytes */
+  uint8_t* sf;          /* device, fos_sf_bytes(R_out, C_out, opt->sf_layout) bytes */
   float* tensor_scale;  /* device float: the job's s_t */
-  uint8_t* choice;      /* optional device [rows][cols/16] bytes, or NULL */
+  uint8_t* choice;      /* optional device [R_out][C_out/16] bytes, or NULL */
 } fos_quant_job;
 
 /* Device scratch fos_quantize_batch needs for n_jobs jobs (8 KiB per job). */
@@ -189,21 +190,28 @@ fos_status fos_quantize_batch_workspace_size(int32_t n_jobs, size_t* bytes);
 /*
  * fos_quantize_batch -- quantize n_jobs matrices (a layer's weight set, say)
  * with the same options, each with its own tensor amax; results identical to
- * one fos_quantize call per job.  The launches are chained so that each
- * job's memory-bound amax pass runs beside the issue-bound quantization of
- * the job before it: launch 0 takes job 0's block maxima, launch i+1
- * quantizes job i while 2 extra warps per CTA take job i+1's block maxima,
- * and the last launch quantizes the last job.  Order the jobs by size,
- * smallest first, to overlap the most.  The quantize launches use
- * programmatic dependent launch: each may start (its input copies and the
- * next job's maxima) while its predecessor finishes, and waits for it before
- * reading the maxima it left.  Scale-pad clears, when a shape needs them,
- * are enqueued before all of these.
- *   opt       shared options; transpose, block_2d and tensor_amax are not
- *             supported here (FOS_ERR_UNSUPPORTED; use fos_quantize).
+ * one fos_quantize call per job.
+ *   - 1D blocks along rows: the launches are chained so that each job's
+ *     memory-bound amax pass runs beside the issue-bound quantization of the
+ *     job before it: launch 0 takes job 0's block maxima, launch i+1
+ *     quantizes job i while 2 extra warps per CTA take job i+1's block
+ *     maxima, and the last launch quantizes the last job.  Order the jobs by
+ *     size, smallest first, to overlap the most.
+ *   - opt->transpose or opt->block_2d: one launch takes the amax passes of up
+ *     to 32 jobs (the tensor maxima of fos_tensor_amax: of the values, or of
+ *     their RHT along the blocks' direction), then one quantize launch per
+ *     job follows; more jobs repeat this per group of 32.
+ * The quantize launches use programmatic dependent launch: each may start
+ * (its input copies, and in the chained form the next job's maxima) while its
+ * predecessor finishes, and waits for it before reading the maxima it needs.
+ * Scale-pad clears, when a shape needs them, are enqueued before all of these.
+ *   opt       shared options; tensor_amax is not supported here
+ *             (FOS_ERR_UNSUPPORTED; use fos_quantize); one_launch does not
+ *             apply and is ignored.
  *   workspace device scratch of fos_quantize_batch_workspace_size() bytes,
  *             4-byte aligned, no initialisation needed.
- * Validation covers every job before anything is enqueued.
+ * Validation covers every job (fos_quantize's checks) before anything is
+ * enqueued.  The jobs' outputs must not overlap one another or any source.
  */
 fos_status fos_quantize_batch(const fos_quant_job* jobs, int32_t n_jobs, const fos_quant_options* opt,
                               void* workspace, size_t workspace_bytes, cudaStream_t stream);

@@ -98,6 +98,27 @@ def test_validation_rejects_without_launch(fos):
     assert fos.fos_e2m1_encode(0, 5, 0, 0) == INVALID
 
 
+def test_batch_validation_rejects_without_launch(fos):
+    """fos_quantize_batch refuses before anything is enqueued: a supplied amax
+    (unsupported), a transposed or 2D job without whole 16-row groups, an
+    output row stride too small for the transposed output."""
+    fake = 1 << 20  # never dereferenced: validation fails first
+    ws = fos.fos_quantize_batch_workspace_size(2)
+
+    def call(opt, rows=32, cols=64, ldc=None):
+        R, C = (cols, rows) if opt.transpose else (rows, cols)
+        job = fos.fos_quant_job(fake, rows, cols, cols, fake, C // 2 if ldc is None else ldc, fake, fake, None)
+        return fos.fos_quantize_batch([job, job], opt, fake, ws, 0)
+
+    bad = fos.options()
+    bad.tensor_amax = fake
+    assert call(bad) == fos.FOS_ERR_UNSUPPORTED
+    assert call(fos.options(transpose=True), rows=24) == fos.FOS_ERR_INVALID_ARG
+    assert call(fos.options(block_2d=True), rows=24) == fos.FOS_ERR_INVALID_ARG
+    assert call(fos.options(transpose=True), ldc=8) == fos.FOS_ERR_INVALID_ARG  # C_out / 2 = 16
+    assert fos.fos_quantize_batch([], fos.options(transpose=True), 0, 0, 0) == fos.FOS_OK
+
+
 def test_gemm_validation(fos):
     INVALID = fos.FOS_ERR_INVALID_ARG
     fake = 1 << 20

@@ -1,6 +1,8 @@
-"""fos_quantize_batch against the oracle: every job of a chained batch must
-equal the oracle's quantization of that matrix bit for bit (codes, scale
-bytes, tensor scale, choices), whatever the shapes of its neighbours."""
+"""fos_quantize_batch against the oracle: every job of a batch must equal the
+oracle's quantization of that matrix bit for bit (codes, scale bytes, tensor
+scale, choices), whatever the shapes of its neighbours.  Both forms: the
+chained row form, and the transposed / 2D form (one amax launch per group of
+up to 32 jobs, then one quantize launch per job)."""
 import numpy as np
 import pytest
 
@@ -91,11 +93,61 @@ def test_batch_with_empty_job_and_single_job(fos):
     assert_same(one[0], oracle_quantize(bits[0]), "single job")
 
 
-def test_batch_rejects_unsupported_options(fos):
+# rows % 16 == 0 (transposed and 2D): 16-row groups; output rows of 16, 80,
+# 1040, 4096 (transposed); tiles per 2D row band 1, 5, 65, 256
+SHAPES_16 = [(64, 256), (304, 1040), (16, 16), (48, 80), (128, 4096), (32, 96)]
+
+
+@pytest.mark.parametrize("opts", [dict(transpose=True), dict(transpose=True, scale_rule=2),
+                                  dict(transpose=True, rounding=1, sr_seed=5, hadamard=True, hadamard_seed=9),
+                                  dict(transpose=True, hadamard=True, hadamard_seed=4, sf_layout=1),
+                                  dict(block_2d=True), dict(block_2d=True, rounding=1, sr_seed=3),
+                                  dict(block_2d=True, hadamard=True, hadamard_seed=2),
+                                  dict(block_2d=True, transpose=True, rounding=1, sr_seed=8, hadamard=True,
+                                       hadamard_seed=6)])
+def test_layout_batch_matches_oracle(fos, opts):
+    bits = [mixed_bits(r, c, seed=141 + i) for i, (r, c) in enumerate(SHAPES_16)]
+    got = run_batch(fos, bits, **opts)
+    for i, b in enumerate(bits):
+        assert_same(got[i], oracle_quantize(b, **opts), f"job {i} {b.shape} {opts}")
+
+
+def test_layout_batch_padded_rows_and_empty_job(fos):
+    """Transposed jobs read from wider rows, with an empty job between them."""
+    bits = [workloads.student_t(256, 1024, seed=151), np.zeros((0, 64), np.uint16),
+            mixed_bits(160, 528, seed=152)]
+    opts = dict(transpose=True, hadamard=True, hadamard_seed=11)
+    got = run_batch(fos, bits, lds=[1032, 64, 544], **opts)
+    assert_same(got[0], oracle_quantize(bits[0], **opts), "job 0")
+    assert_same(got[2], oracle_quantize(bits[2], **opts), "job 2")
+
+
+def test_layout_batch_more_jobs_than_one_amax_launch(fos):
+    """34 jobs: two groups (32 and 2) of one amax launch each."""
+    bits = [mixed_bits(16 * (1 + i % 3), 16 * (2 + i % 5), seed=161 + i) for i in range(34)]
+    opts = dict(block_2d=True, transpose=True)
+    got = run_batch(fos, bits, **opts)
+    for i, b in enumerate(bits):
+        assert_same(got[i], oracle_quantize(b, **opts), f"job {i} {b.shape}")
+
+
+def test_batch_rejects_unsupported_and_invalid(fos):
+    import ctypes
+
     import torch
 
     x = to_device_bf16(mixed_bits(32, 64, seed=1))
-    for bad in (dict(transpose=True), dict(block_2d=True)):
-        with pytest.raises(fos.FosError):
-            fos.BatchQuantizer([x.shape], **bad)([x])
+    amax = torch.ones(1, dtype=torch.float32, device="cuda")
+    with pytest.raises(fos.FosError):
+        fos.BatchQuantizer([x.shape], tensor_amax=amax)([x])
+    # a transposed job needs whole 16-row groups: refused before any launch
+    y = to_device_bf16(mixed_bits(24, 64, seed=2))
+    out = torch.empty(64 * 16, dtype=torch.uint8, device="cuda")
+    ts = torch.empty(1, dtype=torch.float32, device="cuda")
+    job = fos.fos_quant_job(y.data_ptr(), 24, 64, 64, out.data_ptr(), 16, out.data_ptr(), ts.data_ptr(), None)
+    ws = torch.empty(fos.fos_quantize_batch_workspace_size(1), dtype=torch.uint8, device="cuda")
+    st = fos.fos_quantize_batch((fos.fos_quant_job * 1)(job), fos.options(transpose=True), ws.data_ptr(),
+                                ws.numel(), 0)
+    assert st == fos.FOS_ERR_INVALID_ARG
+    assert ctypes.sizeof(fos.fos_quant_job) > 0
     torch.cuda.synchronize()
