@@ -190,12 +190,6 @@ __global__ void __launch_bounds__(256) amax_rows_kernel(AmaxParams p) {
   if (threadIdx.x == 0) p.partials[blockIdx.x] = m;
 }
 
-// RHT down columns: a lane owns kAmaxColCPL adjacent columns x 16 rows, so a
-// warp reads 64 * kAmaxColCPL contiguous bytes of each of the 16 rows.  With
-// PLAIN, the same pass also takes max |x| of the untransformed values (the
-// column's magnitudes before the butterflies: the sign flips do not change
-// them) into p.partials_plain.  Two CTAs per SM at 128 registers (a few bytes
-// spilled) measured faster than one at 142, and than 4 columns per lane.
 // The thread's maximum over column warp tasks gw, gw + nwarps, ... of p (the
 // transform down the columns, its 1/4 applied); with PLAIN, *plain gets the
 // maximum of the untransformed values.
@@ -245,7 +239,8 @@ __device__ __forceinline__ float amax_cols_share(const AmaxParams& p, int64_t gw
 // PLAIN, the same pass also takes max |x| of the untransformed values (the
 // column's magnitudes before the butterflies: the sign flips do not change
 // them) into p.partials_plain.  Two CTAs per SM at 128 registers (a few bytes
-// spilled) measured faster than one at 142, and than 4 columns per lane.
+// spilled) measured faster than one at 142, and than 4 columns per lane (also
+// with the next task's loads issued before the current task's reduction).
 template <bool PLAIN>
 __global__ void __launch_bounds__(256, 2) amax_cols_kernel(AmaxParams p) {
   __shared__ float s_red[33];
