@@ -2,7 +2,9 @@
 byte compared with the oracle (the oracle finishes each in seconds):
 
 - the Qwen3-8B-shaped layer weight set, quantized as one chained batch in the
-  order and launch configuration the benchmark times (smallest first);
+  order and launch configuration the benchmark times (smallest first), and as
+  one batch of transposed jobs and of 2D jobs (one amax launch, then a
+  quantize launch per matrix), as the benchmark also times them;
 - the 16384 x 4096 activation with the RHT, row-major and transposed;
 - the 8192 x 12288 gradient with stochastic rounding, 1D and 2D, and 2D RNE.
 """
@@ -38,6 +40,22 @@ def test_qwen3_weight_set_as_one_batch(fos):
         got = QOut(codes=o.codes[:, : o.cols // 2].cpu().numpy(), sf=o.sf.cpu().numpy(),
                    s_t=np.float32(o.tensor_scale.item()), choice=o.choice.cpu().numpy())
         assert_same(got, oracle_quantize(mats[k]), k)
+
+
+@pytest.mark.parametrize("opts", [dict(transpose=True), dict(block_2d=True)])
+def test_qwen3_weight_set_layout_batch(fos, opts):
+    import torch
+
+    mats = workloads.qwen3_8b_weights()
+    order = sorted(mats, key=lambda k: mats[k].size)
+    xs = [to_device_bf16(mats[k]) for k in order]
+    bq = fos.BatchQuantizer([x.shape for x in xs], with_choice=True, **opts)
+    outs = bq(xs)
+    torch.cuda.synchronize()
+    for k, o in zip(order, outs):
+        got = QOut(codes=o.codes[:, : o.cols // 2].cpu().numpy(), sf=o.sf.cpu().numpy(),
+                   s_t=np.float32(o.tensor_scale.item()), choice=o.choice.cpu().numpy())
+        assert_same(got, oracle_quantize(mats[k], **opts), f"{k} {opts}")
 
 
 @pytest.mark.parametrize("transpose", [False, True])
