@@ -71,22 +71,17 @@ bool valid_matrix(const void* x, int64_t rows, int64_t cols, int64_t ld_x, const
   return ld_codes >= C / 2 && ld_codes % 8 == 0 && aligned(codes, 8) && aligned(sf, 4);
 }
 
-// One matrix's quantize launch: its parameters, with the tensor amax read from
-// amax_src (one float, or n_partials partial maxima), its kernel kind (as
-// launch_quant takes it) and its warp tasks.
-struct QuantLaunch {
-  fos::QuantParams p;
-  int kind;
-  int64_t tasks;
-};
 
+}  // namespace
+
+namespace fos {
 QuantLaunch quant_launch(const void* x, int64_t rows, int64_t cols, int64_t ld_x, const fos_quant_options* opt,
                          uint8_t* codes, int64_t ld_codes, uint8_t* sf, float* tensor_scale, uint8_t* choice,
                          const float* amax_src, int n_partials) {
   const bool tr = opt->transpose != 0, two_d = opt->block_2d != 0, sr = opt->rounding == FOS_ROUND_STOCHASTIC;
   const int64_t R = tr ? cols : rows, C = tr ? rows : cols, nb = C / 16;
   QuantLaunch q{};
-  fos::QuantParams& p = q.p;
+  QuantParams& p = q.p;
   p.x = static_cast<const uint16_t*>(x);
   p.rows = rows;
   p.cols = cols;
@@ -126,9 +121,11 @@ QuantLaunch quant_launch(const void* x, int64_t rows, int64_t cols, int64_t ld_x
   return q;
 }
 
-}  // namespace
+cudaError_t pad_scales(const QuantParams& p, cudaStream_t s) {
+  if (p.sf_layout != FOS_SF_SWIZZLED_128x4 || (p.R % 128 == 0 && p.nb % 4 == 0)) return cudaSuccess;
+  return launch_sf_pad(p.sf, sf_bytes_of(p.R, p.nb, p.sf_layout), p.R, p.nb, s);
+}
 
-namespace fos {
 cudaError_t amax_plain_and_rht_cols(const void* x, int64_t rows, int64_t cols, int64_t ld, uint64_t hadamard_seed,
                                     float* out, void* workspace, cudaStream_t s) {
   AmaxParams a{};
@@ -230,7 +227,7 @@ fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
     if (fos::launch_amax(a, rht, tr, n_partials, stream) != cudaSuccess) return FOS_ERR_CUDA;
   }
 
-  QuantLaunch q = quant_launch(x, rows, cols, ld_x, opt, codes, ld_codes, sf, tensor_scale, choice,
+  fos::QuantLaunch q = fos::quant_launch(x, rows, cols, ld_x, opt, codes, ld_codes, sf, tensor_scale, choice,
                                opt->tensor_amax ? opt->tensor_amax : static_cast<const float*>(workspace),
                                n_partials);
   if (fused) {
@@ -246,10 +243,7 @@ fos_status fos_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
     if (fos::launch_quant(q.p, opt->scale_rule, q.kind, rht, sr, grid, stream, n_partials > 0) != cudaSuccess)
       return FOS_ERR_CUDA;
   }
-  if (opt->sf_layout == FOS_SF_SWIZZLED_128x4 && (q.p.R % 128 != 0 || q.p.nb % 4 != 0)) {
-    if (fos::launch_sf_pad(sf, sf_bytes_of(q.p.R, q.p.nb, opt->sf_layout), q.p.R, q.p.nb, stream) != cudaSuccess)
-      return FOS_ERR_CUDA;
-  }
+  if (fos::pad_scales(q.p, stream) != cudaSuccess) return FOS_ERR_CUDA;
   return FOS_OK;
 }
 
@@ -318,7 +312,7 @@ fos_status fos_quantize_batch(const fos_quant_job* jobs, int32_t n_jobs, const f
       // the next group's amax launch follows them as a plain launch
       for (int32_t k = 0; k < b.n_jobs; ++k) {
         const fos_quant_job& j = jobs[g0 + k];
-        const QuantLaunch q = quant_launch(j.x, j.rows, j.cols, j.ld_x, opt, j.codes, j.ld_codes, j.sf,
+        const fos::QuantLaunch q = fos::quant_launch(j.x, j.rows, j.cols, j.ld_x, opt, j.codes, j.ld_codes, j.sf,
                                            j.tensor_scale, j.choice, slot(g0 + k), grid);
         if (fos::launch_quant(q.p, opt->scale_rule, q.kind, rht, sr, fos::quant_grid(q.tasks, q.kind), stream,
                               true) != cudaSuccess)
@@ -334,7 +328,7 @@ fos_status fos_quantize_batch(const fos_quant_job* jobs, int32_t n_jobs, const f
   if (fos::launch_amax(amax_of(jobs[0], slot(0)), rht, false, n_part, stream) != cudaSuccess) return FOS_ERR_CUDA;
   for (int32_t i = 0; i < n_jobs; ++i) {
     const fos_quant_job& j = jobs[i];
-    QuantLaunch q = quant_launch(j.x, j.rows, j.cols, j.ld_x, opt, j.codes, j.ld_codes, j.sf, j.tensor_scale,
+    fos::QuantLaunch q = fos::quant_launch(j.x, j.rows, j.cols, j.ld_x, opt, j.codes, j.ld_codes, j.sf, j.tensor_scale,
                                  j.choice, slot(i), n_part);
     if (i + 1 < n_jobs) {
       const fos_quant_job& nx = jobs[i + 1];

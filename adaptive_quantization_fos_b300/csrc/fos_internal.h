@@ -104,6 +104,28 @@ cudaError_t amax_plain_and_rht_cols(const void* x, int64_t rows, int64_t cols, i
 // x before waiting for it, and the partial maxima after).
 cudaError_t launch_quant(const QuantParams& p, int rule, int kind, bool rht, bool sr, int grid, cudaStream_t s,
                          bool pdl = false);
+// Both stochastic-rounding quantizations of one source in one launch: pc
+// transposed (the RHT down the columns when rht), pr along the rows (no RHT),
+// each with its tensor amax supplied (n_partials 0) and the same seed; n_tasks
+// = the transposed stochastic-rounding kernel's warp tasks.  The results equal
+// the two separate launches'.  A plain launch (no programmatic dependence).
+cudaError_t launch_quant_dual_sr(const QuantParams& pc, const QuantParams& pr, int rule, bool rht, int64_t n_tasks,
+                                 cudaStream_t s);
+
+// One matrix's quantize launch for fos_quantize's arguments: its parameters,
+// with the tensor amax read from amax_src (one float, or n_partials partial
+// maxima), its kernel kind (as launch_quant takes it) and its warp tasks.
+struct QuantLaunch {
+  QuantParams p;
+  int kind;
+  int64_t tasks;
+};
+QuantLaunch quant_launch(const void* x, int64_t rows, int64_t cols, int64_t ld_x, const fos_quant_options* opt,
+                         uint8_t* codes, int64_t ld_codes, uint8_t* sf, float* tensor_scale, uint8_t* choice,
+                         const float* amax_src, int n_partials);
+// Clears the pad bytes of p's swizzled scale tiles, when its shape leaves any.
+cudaError_t pad_scales(const QuantParams& p, cudaStream_t s);
+
 // Rows (1D) quantized from partials of an earlier launch while 2 extra warps
 // per CTA take the block maxima of the next job (p.next_*); grid = chained_grid().
 cudaError_t launch_quant_rows_chained(const QuantParams& p, int rule, bool rht, bool sr, int grid, cudaStream_t s);

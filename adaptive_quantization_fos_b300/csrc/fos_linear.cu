@@ -180,19 +180,37 @@ fos_status fos_linear_backward(const void* dy, int64_t ld_dy, const void* x, int
       return st;
     }
   }
+  fos_quant_options o_dy = opts(opt->grad_rounding, 0, 0, 0);
+  fos_quant_options o_dyt = opts(opt->grad_rounding, 1, opt->wgrad_hadamard, 0);
+  if (both) {
+    o_dy.tensor_amax = amax_dy;
+    o_dyt.tensor_amax = opt->wgrad_hadamard ? amax_dy + 1 : amax_dy;
+  }
+  // With both products under stochastic rounding, dY's two quantizations come
+  // from one launch: one read of dY, and each element's Philox word computed
+  // once for both (they draw from the same word).
+  const bool dual = both && opt->grad_rounding == FOS_ROUND_STOCHASTIC;
+  if (dual) {
+    const auto qr = fos::quant_launch(dy, M, N, ld_dy, &o_dy, const_cast<uint8_t*>(ops[0].codes), ops[0].ld_codes,
+                                      const_cast<uint8_t*>(ops[0].sf), const_cast<float*>(ops[0].tensor_scale),
+                                      nullptr, o_dy.tensor_amax, 0);
+    const auto qc = fos::quant_launch(dy, M, N, ld_dy, &o_dyt, const_cast<uint8_t*>(ops[2].codes), ops[2].ld_codes,
+                                      const_cast<uint8_t*>(ops[2].sf), const_cast<float*>(ops[2].tensor_scale),
+                                      nullptr, o_dyt.tensor_amax, 0);
+    if (fos::launch_quant_dual_sr(qc.p, qr.p, opt->scale_rule, opt->wgrad_hadamard != 0, qc.tasks, stream) !=
+            cudaSuccess ||
+        fos::pad_scales(qr.p, stream) != cudaSuccess || fos::pad_scales(qc.p, stream) != cudaSuccess)
+      return FOS_ERR_CUDA;
+  }
   if (dx) {
-    fos_quant_options o_dy = opts(opt->grad_rounding, 0, 0, 0);
-    if (both) o_dy.tensor_amax = amax_dy;
     const fos_quant_options o_w = opts(FOS_ROUND_RNE, 1, 0, opt->weight_2d);
-    if ((st = quant(0, dy, M, N, ld_dy, o_dy)) != FOS_OK) return st;
+    if (!dual && (st = quant(0, dy, M, N, ld_dy, o_dy)) != FOS_OK) return st;
     if ((st = quant(1, w, N, K, ld_w, o_w)) != FOS_OK) return st;
     if ((st = fos_gemm(&ops[0], &ops[1], dx, ld_dx, dev_status, stream)) != FOS_OK) return st;
   }
   if (dw) {
-    fos_quant_options o_dyt = opts(opt->grad_rounding, 1, opt->wgrad_hadamard, 0);
-    if (both) o_dyt.tensor_amax = opt->wgrad_hadamard ? amax_dy + 1 : amax_dy;
     const fos_quant_options o_xt = opts(FOS_ROUND_RNE, 1, opt->wgrad_hadamard, 0);
-    if ((st = quant(2, dy, M, N, ld_dy, o_dyt)) != FOS_OK) return st;
+    if (!dual && (st = quant(2, dy, M, N, ld_dy, o_dyt)) != FOS_OK) return st;
     if ((st = quant(3, x, M, K, ld_x, o_xt)) != FOS_OK) return st;
     if ((st = fos_gemm(&ops[2], &ops[3], dw, ld_dw, dev_status, stream)) != FOS_OK) return st;
   }

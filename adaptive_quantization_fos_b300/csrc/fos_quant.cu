@@ -958,6 +958,232 @@ __global__ void __launch_bounds__(256, 2) quant_cols_kernel(QuantParams p) {
   }
 }
 
+// ------------------------------------------------------------ dual (SR)
+// One read of x [rows, cols] for both of its stochastic-rounding
+// quantizations: pc along the source columns (transposed; with the RHT when
+// RHT) and pr along the rows (no RHT).  Element i rounds with the Philox word
+// of its source index in both, so each word is computed once: the transposed
+// pass computes a block-row's words as the transposed kernel does (a lane pair
+// shares each call) and leaves them in a per-warp stash, from which the row
+// pass reads its own.  Warp task: 64 source rows (4 block-rows) x 64 source
+// columns.  Per block-row, the transposed pass takes lane l's two columns
+// (2l, 2l + 1) and the row pass lane l's two row blocks (row l/2, columns
+// 32 (l & 1) .. + 31).  Slot rows are padded to 144 bytes and stash rows to 68
+// words, so that the row pass's reads spread over the banks.
+constexpr int kDualRowPitch = 2 * 64 + 16;
+constexpr int kDualSlotBytes = 16 * kDualRowPitch;
+constexpr int kDualSlots = 2;
+constexpr int kDualStashPitch = 68;  // words
+constexpr int kDualStashBytes = 16 * kDualStashPitch * 4;
+constexpr int kDualOutBytes = 2 * 32 * kColOutPitch;
+constexpr int kDualWarpBytes = kDualSlots * kDualSlotBytes + kDualStashBytes + kDualOutBytes;
+constexpr int kDualSmemBytes = kColWarps * kDualWarpBytes;
+
+template <int RULE, bool RHT>
+__global__ void __launch_bounds__(256, 2) quant_dual_sr_kernel(QuantParams pc, QuantParams pr) {
+  extern __shared__ __align__(128) uint8_t d_smem[];
+  __shared__ float s_red[33];
+  __shared__ float2 s_tab_c[128], s_tab_r[128];
+  __shared__ uint64_t s_bar[kColWarps * kDualSlots];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x < kColWarps * kDualSlots) mbar_init(smem_addr(&s_bar[threadIdx.x]), 16);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  __syncthreads();  // the ring barriers are initialised before any copy
+  const uint32_t rht_mask = RHT ? rht_sign_mask(pc.hk0, pc.hk1) : 0u;
+  const int64_t nbr = pc.rows >> 4;             // block-rows of the source
+  const int64_t ngr = (nbr + 3) >> 2;           // task rows (4 block-rows each)
+  const int64_t nch = (pc.cols + 63) >> 6;      // task columns (64 source columns each)
+  const int64_t n_tasks = ngr * nch;
+  const int64_t nwarps = (int64_t)gridDim.x * kColWarps;
+  const int64_t gw = (int64_t)blockIdx.x * kColWarps + warp;
+  const uint64_t stream_once = l2_policy_evict_first();
+  uint8_t* const wbase = d_smem + warp * kDualWarpBytes;
+  uint8_t* const slots = wbase;
+  uint32_t* const stash = reinterpret_cast<uint32_t*>(wbase + kDualSlots * kDualSlotBytes);
+  uint8_t* const obuf = wbase + kDualSlots * kDualSlotBytes + kDualStashBytes + lane * kColOutPitch;
+  const uint32_t bar0 = smem_addr(&s_bar[warp * kDualSlots]);
+
+  // producer cursor (all lanes): the next (task, block-row) to fetch
+  int64_t pt = gw;
+  int psub = 0;
+  auto issue_next = [&](int slot) -> bool {
+    if (pt >= n_tasks) return false;
+    const int64_t g = pt / nch, ch = pt - g * nch;
+    const int64_t rb = 4 * g + psub;
+    const int64_t c0 = ch * 64;
+    const uint32_t bytes = (uint32_t)((pc.cols - c0 < 64 ? pc.cols - c0 : 64) * 2);
+    if (lane < 16)
+      bulk_g2s_hint(smem_addr(slots + slot * kDualSlotBytes + lane * kDualRowPitch),
+                    pc.x + (rb * 16 + lane) * pc.ld + c0, bytes, bar0 + 8u * slot, stream_once);
+    if (++psub == 4 || 4 * g + psub >= nbr) {
+      psub = 0;
+      pt += nwarps;
+    }
+    return true;
+  };
+  int issued = 0, consumed = 0;
+  for (int k = 0; k < kDualSlots; ++k) issued += issue_next(k) ? 1 : 0;
+  // Both tensor maxima are supplied (the launch is plain): nothing to wait for
+  // but the stream order.
+  const TensorConsts tcc = quant_prologue(pc, s_red);
+  const TensorConsts tcr = quant_prologue(pr, s_red);
+  build_scale_table(tcc.s_t, s_tab_c);
+  build_scale_table(tcr.s_t, s_tab_r);
+  __syncthreads();
+
+  const bool odd = lane & 1;
+  int slot = 0;
+  uint32_t ph = 0;
+  bool failed = false;
+  for (int64_t t = gw; t < n_tasks && !failed; t += nwarps) {
+    const int64_t g = t / nch, ch = t - g * nch;
+    const int64_t c0 = ch * 64;
+    const int nsub = nbr - 4 * g < 4 ? (int)(nbr - 4 * g) : 4;
+    uint32_t sfw[2] = {0u, 0u};  // the task's scale bytes of each transposed output row
+    for (int sub = 0; sub < nsub; ++sub) {
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait_for(bar0 + 8u * slot, ph, pc.timeout_ns))) {
+        failed = true;
+        break;
+      }
+      const uint8_t* sl = slots + slot * kDualSlotBytes;
+      const int64_t rb = 4 * g + sub;
+
+      // ---- the block-row's Philox words: 8 calls per lane (rows q, or q + 8
+      // for the odd lane of a pair, of the pair's 4-column group), into the
+      // stash, and swapped with the pair for the transposed pass's draws
+      float n0[16], n1[16];
+      {
+        const uint64_t grp = (uint64_t)(c0 + 4 * (lane >> 1));
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int rr = odd ? q + 8 : q;
+          const uint64_t r = (uint64_t)(rb * 16 + rr);
+          const U4 u = sr_words4(r * (uint64_t)pc.cols + grp, pc.sr_k0, pc.sr_k1);
+          *reinterpret_cast<uint4*>(stash + kDualStashPitch * rr + 4 * (lane >> 1)) = make_uint4(u.x, u.y, u.z, u.w);
+          const uint32_t r0 = __shfl_xor_sync(0xFFFFFFFFu, odd ? u.x : u.z, 1);
+          const uint32_t r1 = __shfl_xor_sync(0xFFFFFFFFu, odd ? u.y : u.w, 1);
+          if (odd) {
+            n0[q] = sr_draw(r0); n1[q] = sr_draw(r1); n0[q + 8] = sr_draw(u.z); n1[q + 8] = sr_draw(u.w);
+          } else {
+            n0[q] = sr_draw(u.x); n1[q] = sr_draw(u.y); n0[q + 8] = sr_draw(r0); n1[q + 8] = sr_draw(r1);
+          }
+        }
+      }
+
+      // ---- transposed pass: the lane's two source columns
+      {
+        uint32_t v[16];  // row i: columns 2 lane, 2 lane + 1
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = *reinterpret_cast<const uint32_t*>(sl + kDualRowPitch * i + 4 * lane);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          float y[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const uint32_t s = RHT ? (((rht_mask >> i) & 1u) << 31) : 0u;
+            y[i] = __uint_as_float((k ? (v[i] & 0xFFFF0000u) : (v[i] << 16)) ^ s);
+          }
+          if (RHT) hadamard16(y);
+          const float ab = absmax16(y);
+          uint64_t yp[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) yp[j] = pack_f2(y[2 * j], y[2 * j + 1]);
+          uint32_t lo, hi, sf;
+          bool four;
+          quant_block_tab<RULE, true>(yp, ab, tcc, s_tab_c, k ? n1 : n0, lo, hi, sf, four);
+          *reinterpret_cast<uint2*>(obuf + k * 32 * kColOutPitch + 8 * sub) = make_uint2(lo, hi);
+          sfw[k] |= sf << (8 * sub);
+          const int64_t orow = c0 + 2 * lane + k;  // output row = source column
+          if (pc.choice && orow < pc.cols) pc.choice[orow * nbr + rb] = four ? 1 : 0;
+        }
+      }
+      __syncwarp();  // the stash is complete
+
+      // ---- row pass: the lane's two blocks of row l/2
+      {
+        const int rr = lane >> 1, hb = lane & 1;
+        const int64_t row = rb * 16 + rr;
+        const uint8_t* src = sl + kDualRowPitch * rr + 64 * hb;
+        const uint32_t* wsrc = stash + kDualStashPitch * rr + 32 * hb;
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const int64_t blk = (c0 >> 4) + 2 * hb + b;  // the block's index along the row
+          if (16 * blk >= pr.cols) break;              // past a ragged task's last column
+          uint32_t wv[8];
+          const uint4 a = *reinterpret_cast<const uint4*>(src + 32 * b);
+          const uint4 c = *reinterpret_cast<const uint4*>(src + 32 * b + 16);
+          wv[0] = a.x; wv[1] = a.y; wv[2] = a.z; wv[3] = a.w;
+          wv[4] = c.x; wv[5] = c.y; wv[6] = c.z; wv[7] = c.w;
+          uint64_t yp[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) yp[k] = bf16x2_to_f32x2(wv[k]);
+          const float ab = absmax16_bf16(wv);
+          float n[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 w = *reinterpret_cast<const uint4*>(wsrc + 16 * b + 4 * q);
+            n[4 * q] = sr_draw(w.x); n[4 * q + 1] = sr_draw(w.y);
+            n[4 * q + 2] = sr_draw(w.z); n[4 * q + 3] = sr_draw(w.w);
+          }
+          uint32_t lo, hi, sf;
+          bool four;
+          quant_block_tab<RULE, true>(yp, ab, tcr, s_tab_r, n, lo, hi, sf, four);
+          *reinterpret_cast<uint2*>(pr.codes + row * pr.ld_codes + 8 * blk) = make_uint2(lo, hi);
+          pr.sf[sf_off(row, blk, pr.nb, pr.sf_layout)] = (uint8_t)sf;
+          if (pr.choice) pr.choice[row * pr.nb + blk] = four ? 1 : 0;
+        }
+      }
+      __syncwarp();  // the slot and the stash have been read
+      ++consumed;
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issued += issue_next(slot) ? 1 : 0;
+      if (++slot == kDualSlots) {
+        slot = 0;
+        ph ^= 1u;
+      }
+    }
+    if (failed) break;
+    // the task's transposed output: each row's codes for block-rows 4g .. 4g + nsub - 1
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int64_t orow = c0 + 2 * lane + k;
+      if (orow >= pc.cols) continue;
+      const uint8_t* e = obuf + k * 32 * kColOutPitch;
+      uint8_t* dst = pc.codes + orow * pc.ld_codes + 4 * g * 8;
+      const uint2 d0 = *reinterpret_cast<const uint2*>(e), d1 = *reinterpret_cast<const uint2*>(e + 8);
+      const uint2 d2 = *reinterpret_cast<const uint2*>(e + 16), d3 = *reinterpret_cast<const uint2*>(e + 24);
+      if (nsub == 4 && (reinterpret_cast<uintptr_t>(dst) & 31) == 0) {
+        st_v8(dst, make_uint4(d0.x, d0.y, d1.x, d1.y), make_uint4(d2.x, d2.y, d3.x, d3.y));
+      } else {
+        const uint2 d[4] = {d0, d1, d2, d3};
+#pragma unroll
+        for (int sub = 0; sub < 4; ++sub)
+          if (sub < nsub) *reinterpret_cast<uint2*>(dst + 8 * sub) = d[sub];
+      }
+      const int64_t so = sf_off(orow, 4 * g, nbr, pc.sf_layout);
+      if (nsub == 4 && (pc.sf_layout == FOS_SF_SWIZZLED_128x4 || (nbr & 3) == 0)) {
+        *reinterpret_cast<uint32_t*>(pc.sf + so) = sfw[k];
+      } else {
+#pragma unroll
+        for (int sub = 0; sub < 4; ++sub)
+          if (sub < nsub) pc.sf[sf_off(orow, 4 * g + sub, nbr, pc.sf_layout)] = (uint8_t)(sfw[k] >> (8 * sub));
+      }
+    }
+  }
+  if (failed && lane == 0) {
+    *pc.tensor_scale = __int_as_float(0x7FC00000);  // NaN: the results are not valid
+    *pr.tensor_scale = __int_as_float(0x7FC00000);
+  }
+  // let copies still in flight land before the CTA exits (bounded)
+  for (; consumed < issued; ++consumed) {
+    mbar_wait_for(bar0 + 8u * slot, ph, pc.timeout_ns);
+    if (++slot == kDualSlots) {
+      slot = 0;
+      ph ^= 1u;
+    }
+  }
+}
+
 // -------------------------------------------------------------- quant_2d
 // Warp task = 16 source rows x 32 source columns (two tiles); lane l owns
 // source row (l & 15) of tile (l >> 4).  Tile reductions use xor-shuffles
@@ -1480,6 +1706,30 @@ cudaError_t launch_quant_rows_fused(const QuantParams& p, int rule, bool rht, bo
     case FOS_SCALE_4: return launch_rows_fused_rule<FOS_SCALE_4>(p, rht, sr, n_tasks, s);
     default: return launch_rows_fused_rule<FOS_SCALE_4OVER6>(p, rht, sr, n_tasks, s);
   }
+}
+
+template <int RULE, bool RHT>
+static cudaError_t launch_dual_rule(const QuantParams& pc, const QuantParams& pr, int64_t n_tasks, cudaStream_t s) {
+  auto fn = quant_dual_sr_kernel<RULE, RHT>;
+  static std::atomic<int> done[kMaxDevices], per_sm[kMaxDevices];
+  const int64_t want = (n_tasks + kColWarps - 1) / kColWarps;
+  int grid = want < 1 ? 1 : (want > (1 << 20) ? (1 << 20) : (int)want);
+  cudaError_t e = smem_opt_in(fn, kDualSmemBytes, done);
+  if (e == cudaSuccess) e = one_wave(fn, kDualSmemBytes, per_sm, &grid);
+  if (e != cudaSuccess) return e;
+  fn<<<grid, 32 * kColWarps, kDualSmemBytes, s>>>(pc, pr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_dual_sr(const QuantParams& pc, const QuantParams& pr, int rule, bool rht, int64_t n_tasks,
+                                 cudaStream_t s) {
+#define FOS_DUAL(R) return rht ? launch_dual_rule<R, true>(pc, pr, n_tasks, s) : launch_dual_rule<R, false>(pc, pr, n_tasks, s)
+  switch (rule) {
+    case FOS_SCALE_6: FOS_DUAL(FOS_SCALE_6);
+    case FOS_SCALE_4: FOS_DUAL(FOS_SCALE_4);
+    default: FOS_DUAL(FOS_SCALE_4OVER6);
+  }
+#undef FOS_DUAL
 }
 
 cudaError_t launch_quant(const QuantParams& p, int rule, int kind, bool rht, bool sr, int grid, cudaStream_t s,

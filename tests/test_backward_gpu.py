@@ -67,6 +67,10 @@ OPTS = [
     dict(grad_rounding=0, wgrad_hadamard=False),
     dict(weight_2d=True, sr_seed=77, hadamard_seed=3),
     dict(scale_rule=1, grad_rounding=0),
+    # SR without the RHT, and under the 4-only rule: dY's two SR quantizations
+    # share one launch in every SR case with both products
+    dict(wgrad_hadamard=False, sr_seed=5),
+    dict(scale_rule=2, sr_seed=9, hadamard_seed=4),
 ]
 
 
