@@ -901,6 +901,15 @@ def run_case(args) -> None:
         C = torch.empty((8192, 12288), dtype=torch.bfloat16, device=dev)
         for _ in range(3):
             fos.gemm_mxfp4(a, w, out=C)
+    elif args.case == "linear_backward":
+        # the layer's backward at 8192 x 12288 x 4096 (SR on dY, RHT along M):
+        # the fused dY quantization, W^T and X^T, the two GEMMs
+        dy = _to_dev(torch, workloads.gradients(8192, 12288, seed=6001), dev)
+        x = _to_dev(torch, workloads.activations(8192, 4096, seed=6002), dev)
+        w = _to_dev(torch, workloads.student_t(12288, 4096, seed=6003), dev)
+        bw = fos.LinearBackward(8192, 12288, 4096, device=dev, sr_seed=11, hadamard_seed=12)
+        for _ in range(3):
+            bw(dy, x, w)
     else:
         raise SystemExit(f"unknown case {args.case}")
     torch.cuda.synchronize()
