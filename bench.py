@@ -671,7 +671,8 @@ def linear_backward(torch, fos, dev, pk) -> dict:
     flops = 2 * 2.0 * M * N * K
     return {"ms": round(t, 4), "gemm_ms": round(tg, 4), "quantize_ms": round(t - tg, 4),
             "quantize_note": "the layer's time less its two products: four quantizations, dY's two tensor "
-                             "maxima taken from one read",
+                             "maxima taken from one read and its two stochastic-rounding quantizations from "
+                             "one launch",
             "quantize_separate_calls_ms": round(tq, 4), "quantize_ms_each": each,
             "tflops_effective": round(flops / (t * 1e-3) / 1e12, 1),
             "gemm_tflops": round(flops / (tg * 1e-3) / 1e12, 1), "clocks": clk.summary(),
