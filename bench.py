@@ -855,6 +855,14 @@ def run_case(args) -> None:
                           transpose=True, hadamard=True, hadamard_seed=12)
         for _ in range(3):
             q(x)
+    elif args.case == "quant_cols_rht":
+        # the 16384 x 4096 activation transposed with the RHT, RNE, amax
+        # supplied: only the transposed quantize kernel runs
+        x = _to_dev(torch, workloads.activations(16384, 4096, seed=3001), dev)
+        amax = fos.tensor_amax(x, hadamard=True, transpose=True, hadamard_seed=3002)
+        q = fos.Quantizer(*x.shape, device=dev, tensor_amax=amax, hadamard=True, hadamard_seed=3002, transpose=True)
+        for _ in range(3):
+            q(x)
     elif args.case == "quant_rows_rht":
         # 16384 x 4096 activations with the RHT, amax supplied: only the row
         # quantize kernel runs
