@@ -964,8 +964,8 @@ __global__ void __launch_bounds__(256, 2) quant_cols_kernel(QuantParams p) {
 // RHT) and pr along the rows (no RHT).  Element i rounds with the Philox word
 // of its source index in both, so each word is computed once: the transposed
 // pass computes a block-row's words as the transposed kernel does (a lane pair
-// shares each call) and leaves them in a per-warp stash, from which the row
-// pass reads its own.  Warp task: 64 source rows (4 block-rows) x 64 source
+// shares each call) and leaves their draws in a per-warp stash, from which the
+// row pass reads its own.  Warp task: 64 source rows (4 block-rows) x 64 source
 // columns.  Per block-row, the transposed pass takes lane l's two columns
 // (2l, 2l + 1) and the row pass lane l's two row blocks (row l/2, columns
 // 32 (l & 1) .. + 31).  Slot rows are padded to 144 bytes and stash rows to 68
@@ -999,7 +999,7 @@ __global__ void __launch_bounds__(256, 2) quant_dual_sr_kernel(QuantParams pc, Q
   const uint64_t stream_once = l2_policy_evict_first();
   uint8_t* const wbase = d_smem + warp * kDualWarpBytes;
   uint8_t* const slots = wbase;
-  uint32_t* const stash = reinterpret_cast<uint32_t*>(wbase + kDualSlots * kDualSlotBytes);
+  float* const stash = reinterpret_cast<float*>(wbase + kDualSlots * kDualSlotBytes);
   uint8_t* const obuf = wbase + kDualSlots * kDualSlotBytes + kDualStashBytes + lane * kColOutPitch;
   const uint32_t bar0 = smem_addr(&s_bar[warp * kDualSlots]);
 
@@ -1048,9 +1048,10 @@ __global__ void __launch_bounds__(256, 2) quant_dual_sr_kernel(QuantParams pc, Q
       const uint8_t* sl = slots + slot * kDualSlotBytes;
       const int64_t rb = 4 * g + sub;
 
-      // ---- the block-row's Philox words: 8 calls per lane (rows q, or q + 8
-      // for the odd lane of a pair, of the pair's 4-column group), into the
-      // stash, and swapped with the pair for the transposed pass's draws
+      // ---- the block-row's draws: 8 Philox calls per lane (rows q, or q + 8
+      // for the odd lane of a pair, of the pair's 4-column group), each word
+      // converted once (sr_draw), into the stash, and swapped with the pair
+      // for the transposed pass
       float n0[16], n1[16];
       {
         const uint64_t grp = (uint64_t)(c0 + 4 * (lane >> 1));
@@ -1059,13 +1060,14 @@ __global__ void __launch_bounds__(256, 2) quant_dual_sr_kernel(QuantParams pc, Q
           const int rr = odd ? q + 8 : q;
           const uint64_t r = (uint64_t)(rb * 16 + rr);
           const U4 u = sr_words4(r * (uint64_t)pc.cols + grp, pc.sr_k0, pc.sr_k1);
-          *reinterpret_cast<uint4*>(stash + kDualStashPitch * rr + 4 * (lane >> 1)) = make_uint4(u.x, u.y, u.z, u.w);
-          const uint32_t r0 = __shfl_xor_sync(0xFFFFFFFFu, odd ? u.x : u.z, 1);
-          const uint32_t r1 = __shfl_xor_sync(0xFFFFFFFFu, odd ? u.y : u.w, 1);
+          const float f0 = sr_draw(u.x), f1 = sr_draw(u.y), f2 = sr_draw(u.z), f3 = sr_draw(u.w);
+          *reinterpret_cast<float4*>(stash + kDualStashPitch * rr + 4 * (lane >> 1)) = make_float4(f0, f1, f2, f3);
+          const float r0 = __shfl_xor_sync(0xFFFFFFFFu, odd ? f0 : f2, 1);
+          const float r1 = __shfl_xor_sync(0xFFFFFFFFu, odd ? f1 : f3, 1);
           if (odd) {
-            n0[q] = sr_draw(r0); n1[q] = sr_draw(r1); n0[q + 8] = sr_draw(u.z); n1[q + 8] = sr_draw(u.w);
+            n0[q] = r0; n1[q] = r1; n0[q + 8] = f2; n1[q + 8] = f3;
           } else {
-            n0[q] = sr_draw(u.x); n1[q] = sr_draw(u.y); n0[q + 8] = sr_draw(r0); n1[q + 8] = sr_draw(r1);
+            n0[q] = f0; n1[q] = f1; n0[q + 8] = r0; n1[q + 8] = r1;
           }
         }
       }
@@ -1104,7 +1106,7 @@ __global__ void __launch_bounds__(256, 2) quant_dual_sr_kernel(QuantParams pc, Q
         const int rr = lane >> 1, hb = lane & 1;
         const int64_t row = rb * 16 + rr;
         const uint8_t* src = sl + kDualRowPitch * rr + 64 * hb;
-        const uint32_t* wsrc = stash + kDualStashPitch * rr + 32 * hb;
+        const float* nsrc = stash + kDualStashPitch * rr + 32 * hb;
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
           const int64_t blk = (c0 >> 4) + 2 * hb + b;  // the block's index along the row
@@ -1121,9 +1123,8 @@ __global__ void __launch_bounds__(256, 2) quant_dual_sr_kernel(QuantParams pc, Q
           float n[16];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const uint4 w = *reinterpret_cast<const uint4*>(wsrc + 16 * b + 4 * q);
-            n[4 * q] = sr_draw(w.x); n[4 * q + 1] = sr_draw(w.y);
-            n[4 * q + 2] = sr_draw(w.z); n[4 * q + 3] = sr_draw(w.w);
+            const float4 w = *reinterpret_cast<const float4*>(nsrc + 16 * b + 4 * q);
+            n[4 * q] = w.x; n[4 * q + 1] = w.y; n[4 * q + 2] = w.z; n[4 * q + 3] = w.w;
           }
           uint32_t lo, hi, sf;
           bool four;
