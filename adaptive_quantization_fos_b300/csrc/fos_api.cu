@@ -127,7 +127,7 @@ cudaError_t pad_scales(const QuantParams& p, cudaStream_t s) {
 }
 
 cudaError_t amax_plain_and_rht_cols(const void* x, int64_t rows, int64_t cols, int64_t ld, uint64_t hadamard_seed,
-                                    float* out, void* workspace, cudaStream_t s) {
+                                    float* out, void* workspace, cudaStream_t s, int* n_partials) {
   AmaxParams a{};
   a.x = static_cast<const uint16_t*>(x);
   a.rows = rows;
@@ -143,6 +143,10 @@ cudaError_t amax_plain_and_rht_cols(const void* x, int64_t rows, int64_t cols, i
   if (g > kMaxAmaxPartials / 2) g = kMaxAmaxPartials / 2;
   cudaError_t e = launch_amax(a, true, true, g, s);
   if (e != cudaSuccess) return e;
+  if (n_partials) {  // the caller's quantize launches reduce the partials themselves
+    *n_partials = g;
+    return cudaSuccess;
+  }
   amax_final_kernel<<<1, 256, 0, s>>>(a.partials_plain, g, out);
   amax_final_kernel<<<1, 256, 0, s>>>(a.partials, g, out + 1);
   return cudaGetLastError();

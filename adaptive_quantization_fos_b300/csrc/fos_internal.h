@@ -96,8 +96,11 @@ cudaError_t launch_amax_batch(const AmaxBatch& b, bool hadamard, bool transpose,
 // out[0] = max |x| and out[1] = max |y| for y the RHT of x down its columns
 // (blocks of 16 rows), each exactly what the separate amax passes give.
 // workspace: kQuantWorkspaceBytes of device scratch.
+// With n_partials, out is not written: *n_partials receives the partial count,
+// the partial maxima of max |y| at workspace and those of max |x| at
+// workspace + kMaxAmaxPartials / 2 floats.
 cudaError_t amax_plain_and_rht_cols(const void* x, int64_t rows, int64_t cols, int64_t ld, uint64_t hadamard_seed,
-                                    float* out, void* workspace, cudaStream_t s);
+                                    float* out, void* workspace, cudaStream_t s, int* n_partials = nullptr);
 // kind: 0 rows (1D), 1 cols (1D transposed), 2 2D, 3 2D transposed
 // pdl: the launch may overlap the stream's previous kernel, which must be one
 // of this library's amax or row-quantize launches (the quantize kernel reads

@@ -171,10 +171,17 @@ fos_status fos_linear_backward(const void* dy, int64_t ld_dy, const void* x, int
   // quantizations take them as supplied maxima (the same values their own
   // amax passes would find).
   const bool both = dx && dw;
+  // With both products under stochastic rounding, dY's two quantizations come
+  // from one launch: one read of dY, and each element's Philox word computed
+  // once for both (they draw from the same word).
+  const bool dual = both && opt->grad_rounding == FOS_ROUND_STOCHASTIC;
   float* amax_dy = reinterpret_cast<float*>(base + L.amax);  // [max|dY|, max|RHT_M(dY)|]
+  // the fused launch with the RHT reduces the amax pass's partial maxima itself
+  int dual_partials = 0;
   if (both) {
     if (opt->wgrad_hadamard) {
-      if (fos::amax_plain_and_rht_cols(dy, M, N, ld_dy, opt->hadamard_seed, amax_dy, scratch, stream) != cudaSuccess)
+      if (fos::amax_plain_and_rht_cols(dy, M, N, ld_dy, opt->hadamard_seed, amax_dy, scratch, stream,
+                                       dual ? &dual_partials : nullptr) != cudaSuccess)
         return FOS_ERR_CUDA;
     } else if ((st = fos_tensor_amax(dy, M, N, ld_dy, 0, 0, 0, amax_dy, scratch, scratch_bytes, stream)) != FOS_OK) {
       return st;
@@ -186,17 +193,18 @@ fos_status fos_linear_backward(const void* dy, int64_t ld_dy, const void* x, int
     o_dy.tensor_amax = amax_dy;
     o_dyt.tensor_amax = opt->wgrad_hadamard ? amax_dy + 1 : amax_dy;
   }
-  // With both products under stochastic rounding, dY's two quantizations come
-  // from one launch: one read of dY, and each element's Philox word computed
-  // once for both (they draw from the same word).
-  const bool dual = both && opt->grad_rounding == FOS_ROUND_STOCHASTIC;
   if (dual) {
+    // the maxima: one value each, or the amax pass's partials (max |RHT(dY)|
+    // at the scratch, max |dY| half-way into its partial region)
+    const float* part = static_cast<const float*>(scratch);
+    const float* src_r = dual_partials ? part + fos::kMaxAmaxPartials / 2 : o_dy.tensor_amax;
+    const float* src_c = dual_partials ? part : o_dyt.tensor_amax;
     const auto qr = fos::quant_launch(dy, M, N, ld_dy, &o_dy, const_cast<uint8_t*>(ops[0].codes), ops[0].ld_codes,
                                       const_cast<uint8_t*>(ops[0].sf), const_cast<float*>(ops[0].tensor_scale),
-                                      nullptr, o_dy.tensor_amax, 0);
+                                      nullptr, src_r, dual_partials);
     const auto qc = fos::quant_launch(dy, M, N, ld_dy, &o_dyt, const_cast<uint8_t*>(ops[2].codes), ops[2].ld_codes,
                                       const_cast<uint8_t*>(ops[2].sf), const_cast<float*>(ops[2].tensor_scale),
-                                      nullptr, o_dyt.tensor_amax, 0);
+                                      nullptr, src_c, dual_partials);
     if (fos::launch_quant_dual_sr(qc.p, qr.p, opt->scale_rule, opt->wgrad_hadamard != 0, qc.tasks, stream) !=
             cudaSuccess ||
         fos::pad_scales(qr.p, stream) != cudaSuccess || fos::pad_scales(qc.p, stream) != cudaSuccess)
