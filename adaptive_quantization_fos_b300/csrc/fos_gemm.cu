@@ -83,6 +83,7 @@ struct GemmArgs {
   int32_t* status;
   uint64_t timeout_ns;
   int32_t stall_test;    // 1: the producer never fills a stage (bounded-wait self test)
+  int32_t pre_a;         // under programmatic launch: A's first stages before the wait (B's after)
 };
 
 // ------------------------------------------------------------ PTX helpers
@@ -320,37 +321,51 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_a, const CUtenso
       uint32_t ph = 0;
       int issued = 0;
       bool ok = true;
-      // B's codes and scales for the first tile's first stages need nothing
-      // from an earlier kernel, so they are requested before this CTA waits
-      // for the previous kernel of the stream (A's producer, under
-      // programmatic dependent launch); A and its scales follow the wait.
-      // Stage slots start empty, so these stages need no empty-barrier wait.
+      // The operand that no earlier kernel of the stream writes (B, or A with
+      // pre_a) is requested for the first tile's first stages before this
+      // CTA waits for the previous kernel (the other operand's producer,
+      // under programmatic dependent launch); the other operand follows the
+      // wait.  Stage slots start empty, so these stages need no empty-barrier
+      // wait.
       const int pre = (!args.stall_test && (int)blockIdx.x < n_tiles) ? min(C::kStages, args.num_kb) : 0;
       {
         const int mb = (int)blockIdx.x % args.tiles_m, nb = (int)blockIdx.x / args.tiles_m;
         int halves = 0;
         for (int h = 0; h < BN / 128; ++h)
           if ((nb * (BN / 128) + h) * 128 < args.n) ++halves;
-        for (int kb = 0; kb < pre; ++kb) {
+        auto load_b = [&](int kb) {
           const int nch = n_chunks(min(4, kmma_total - 4 * kb));
           const uint32_t st = smem_u32(smem + kb * C::kStageBytes);
           const uint32_t sfa_dst = st + C::kABytes + C::kBBytes;
-          mbar_expect_tx(sf_full(kb), (1 + halves) * nch * kSfChunk);
           for (int h = 0; h < halves; ++h)
             bulk_load(sfa_dst + C::kSfaBytes + h * 4 * kSfChunk,
                       args.sfb + ((int64_t)(nb * (BN / 128) + h) * args.sf_ktiles + kChunksPerStage * kb) * kSfChunk,
                       nch * kSfChunk, sf_full(kb));
-          mbar_expect_tx(full_bar(kb), C::kABytes + C::kBBytes);
           tma_load_2d(st + C::kABytes, &tm_b, kb * kBKBytes, nb * BN, full_bar(kb));
-        }
-        pdl_wait();
-        for (int kb = 0; kb < pre; ++kb) {
+        };
+        auto load_a = [&](int kb) {
           const int nch = n_chunks(min(4, kmma_total - 4 * kb));
           const uint32_t st = smem_u32(smem + kb * C::kStageBytes);
           bulk_load(st + C::kABytes + C::kBBytes,
                     args.sfa + ((int64_t)mb * args.sf_ktiles + kChunksPerStage * kb) * kSfChunk, nch * kSfChunk,
                     sf_full(kb));
           tma_load_2d(st, &tm_a, kb * kBKBytes, mb * kBM, full_bar(kb));
+        };
+        for (int kb = 0; kb < pre; ++kb) {
+          const int nch = n_chunks(min(4, kmma_total - 4 * kb));
+          mbar_expect_tx(sf_full(kb), (1 + halves) * nch * kSfChunk);
+          mbar_expect_tx(full_bar(kb), C::kABytes + C::kBBytes);
+          if (args.pre_a)
+            load_a(kb);
+          else
+            load_b(kb);
+        }
+        pdl_wait();
+        for (int kb = 0; kb < pre; ++kb) {
+          if (args.pre_a)
+            load_b(kb);
+          else
+            load_a(kb);
           ++issued;
         }
         s = pre % C::kStages;
@@ -778,7 +793,7 @@ int sm_count() {
 
 template <int BN, bool MX>
 fos_status launch_gemm(const Operand& A, const Operand& B, void* Cout, int64_t ldc, int32_t* dev_status,
-                       uint64_t timeout_ns, int stall_test, int grid_cap, bool pdl, cudaStream_t stream) {
+                       uint64_t timeout_ns, int stall_test, int grid_cap, int pdl, cudaStream_t stream) {
   using C = Cfg<BN>;
   CUtensorMap ta, tb;
   const int64_t kbytes = A.cols / 2;
@@ -804,6 +819,7 @@ fos_status launch_gemm(const Operand& A, const Operand& B, void* Cout, int64_t l
   a.status = dev_status;
   a.timeout_ns = timeout_ns;
   a.stall_test = stall_test;
+  a.pre_a = pdl == 2;
   const int64_t tiles = (int64_t)a.tiles_m * a.tiles_n;
   if (tiles > INT32_MAX) return FOS_ERR_INVALID_ARG;
   int grid = sm_count();
@@ -825,9 +841,10 @@ fos_status launch_gemm(const Operand& A, const Operand& B, void* Cout, int64_t l
   return cudaLaunchKernelEx(&cfg, kernel, ta, tb, a) == cudaSuccess ? FOS_OK : FOS_ERR_CUDA;
 }
 
+// pdl: 0 a plain launch; 1 a programmatic dependent of A's producer; 2 of B's.
 template <typename T>
 fos_status gemm_checked(const T* A, const T* B, void* C, int64_t ldc, int32_t* dev_status, uint64_t timeout_ns,
-                        int stall_test, bool pdl, cudaStream_t stream) {
+                        int stall_test, int pdl, cudaStream_t stream) {
   constexpr bool MX = std::is_same<T, fos_mxfp4_tensor>::value;
   if (!valid_operand(A) || !valid_operand(B) || !C) return FOS_ERR_INVALID_ARG;
   if (A->cols != B->cols || B->rows % 8 != 0) return FOS_ERR_INVALID_ARG;
@@ -854,12 +871,17 @@ fos_status gemm_stall_selftest(void* scratch, size_t scratch_bytes, uint64_t tim
   fos_nvfp4_tensor B{b + 16384, b + 34816, reinterpret_cast<float*>(b + 36864), 128, 256, 128,
                      FOS_SF_SWIZZLED_128x4, 0};
   if (cudaMemsetAsync(b, 0, 40960, s) != cudaSuccess) return FOS_ERR_CUDA;
-  return launch_gemm<128, false>(operand(&A), operand(&B), b + 40960, 128, status, timeout_ns, 1, 1, false, s);
+  return launch_gemm<128, false>(operand(&A), operand(&B), b + 40960, 128, status, timeout_ns, 1, 1, 0, s);
 }
 
 fos_status gemm_after_producer_of_a(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* C, int64_t ldc,
                                     int32_t* dev_status, cudaStream_t stream) {
-  return gemm_checked(A, B, C, ldc, dev_status, kDefaultTimeoutNs, 0, true, stream);
+  return gemm_checked(A, B, C, ldc, dev_status, kDefaultTimeoutNs, 0, 1, stream);
+}
+
+fos_status gemm_after_producer_of_b(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* C, int64_t ldc,
+                                    int32_t* dev_status, cudaStream_t stream) {
+  return gemm_checked(A, B, C, ldc, dev_status, kDefaultTimeoutNs, 0, 2, stream);
 }
 }  // namespace fos
 
@@ -881,10 +903,10 @@ extern "C" fos_status fos_selftest_mma_rate(int32_t n_cols, int64_t iters, int32
 
 extern "C" fos_status fos_gemm(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* C, int64_t ldc,
                                int32_t* dev_status, cudaStream_t stream) {
-  return gemm_checked(A, B, C, ldc, dev_status, kDefaultTimeoutNs, 0, false, stream);
+  return gemm_checked(A, B, C, ldc, dev_status, kDefaultTimeoutNs, 0, 0, stream);
 }
 
 extern "C" fos_status fos_gemm_mxfp4(const fos_mxfp4_tensor* A, const fos_mxfp4_tensor* B, void* C, int64_t ldc,
                                      int32_t* dev_status, cudaStream_t stream) {
-  return gemm_checked(A, B, C, ldc, dev_status, kDefaultTimeoutNs, 0, false, stream);
+  return gemm_checked(A, B, C, ldc, dev_status, kDefaultTimeoutNs, 0, 0, stream);
 }

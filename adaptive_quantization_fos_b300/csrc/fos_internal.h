@@ -150,6 +150,10 @@ fos_status gemm_stall_selftest(void* scratch, size_t scratch_bytes, uint64_t tim
 // that kernel, then A.  Only for that pairing: B is read before the wait.
 fos_status gemm_after_producer_of_a(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* C, int64_t ldc,
                                     int32_t* dev_status, cudaStream_t stream);
+// The same with the roles exchanged: the previous kernel produces B and A is
+// complete already (A's first stages are loaded before the wait).
+fos_status gemm_after_producer_of_b(const fos_nvfp4_tensor* A, const fos_nvfp4_tensor* B, void* C, int64_t ldc,
+                                    int32_t* dev_status, cudaStream_t stream);
 // *out = FOS_ERR_TIMEOUT if *tensor_scale is NaN, else FOS_OK.
 cudaError_t launch_nan_to_status(const float* tensor_scale, int32_t* out, cudaStream_t s);
 cudaError_t launch_e2m1_encode(const float* x, int64_t n, uint8_t* out, cudaStream_t s);

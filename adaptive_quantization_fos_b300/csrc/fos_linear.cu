@@ -214,13 +214,16 @@ fos_status fos_linear_backward(const void* dy, int64_t ld_dy, const void* x, int
     const fos_quant_options o_w = opts(FOS_ROUND_RNE, 1, 0, opt->weight_2d);
     if (!dual && (st = quant(0, dy, M, N, ld_dy, o_dy)) != FOS_OK) return st;
     if ((st = quant(1, w, N, K, ld_w, o_w)) != FOS_OK) return st;
-    if ((st = fos_gemm(&ops[0], &ops[1], dx, ld_dx, dev_status, stream)) != FOS_OK) return st;
+    // W^T's quantize launch comes right before and dY's operand is complete:
+    // the GEMM loads dY's first stages while that launch finishes
+    if ((st = fos::gemm_after_producer_of_b(&ops[0], &ops[1], dx, ld_dx, dev_status, stream)) != FOS_OK) return st;
   }
   if (dw) {
     const fos_quant_options o_xt = opts(FOS_ROUND_RNE, 1, opt->wgrad_hadamard, 0);
     if (!dual && (st = quant(2, dy, M, N, ld_dy, o_dyt)) != FOS_OK) return st;
     if ((st = quant(3, x, M, K, ld_x, o_xt)) != FOS_OK) return st;
-    if ((st = fos_gemm(&ops[2], &ops[3], dw, ld_dw, dev_status, stream)) != FOS_OK) return st;
+    // likewise after X^T's quantize launch, with dY^T's operand complete
+    if ((st = fos::gemm_after_producer_of_b(&ops[2], &ops[3], dw, ld_dw, dev_status, stream)) != FOS_OK) return st;
   }
   return FOS_OK;
 }

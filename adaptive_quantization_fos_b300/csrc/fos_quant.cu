@@ -800,6 +800,7 @@ __global__ void __launch_bounds__(256, 2) quant_cols_kernel(QuantParams p) {
   if (threadIdx.x < kColWarps * kColSlots) mbar_init(smem_addr(&s_bar[threadIdx.x]), 16);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncthreads();  // the ring barriers are initialised before any copy
+  pdl_launch_dependents();  // a dependent launch (the next quantize launch, a GEMM) may start its own reads
   const uint32_t rht_mask = RHT ? rht_sign_mask(p.hk0, p.hk1) : 0u;
   const int64_t nbr = p.rows >> 4;            // block-rows of the source = blocks per output row
   const int64_t ngr = (nbr + 3) >> 2;          // task rows (4 block-rows each)
@@ -1209,6 +1210,7 @@ template <int RULE, bool RHT, bool SR, bool TRANS>
 __global__ void __launch_bounds__(256, SR ? 3 : 0) quant_2d_kernel(QuantParams p) {
   __shared__ float s_red[33];
   __shared__ float2 s_tab[128];
+  pdl_launch_dependents();  // a dependent launch (the next quantize launch, a GEMM) may start its own reads
   pdl_wait();  // the partial maxima come from the amax launch before this one
   const TensorConsts tc = quant_prologue(p, s_red);
   build_scale_table(tc.s_t, s_tab);

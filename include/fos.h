@@ -381,6 +381,11 @@ fos_status fos_linear_backward_operands(int64_t M, int64_t N, int64_t K, void* w
  *   dW = dY^T . X     [N, K]: dY and X quantized along M (transposed input,
  *                     optional RHT), one fos_gemm.
  * Each quantization is exactly fos_quantize's; each product is fos_gemm's.
+ * With both products and stochastic rounding, dY's two quantizations run as
+ * one launch (one read of dY; each element's Philox word, the same in both, is
+ * evaluated once).  Each GEMM is launched as a programmatic dependent of the
+ * quantize launch before it (W^T's, X^T's): its CTAs load dY's operand, which
+ * is complete, during that launch's tail, and wait for it before the other.
  *   M % 64 == 0, N % 64 == 0 (the contraction lengths), K % 16 == 0; all > 0.
  *   dy, x, w  device bf16, 16-byte aligned, ld % 8 == 0, ld >= the row length.
  *   dx, dw    device bf16 outputs [M][ld_dx], [N][ld_dw] (ld >= K, ld % 8 == 0,
