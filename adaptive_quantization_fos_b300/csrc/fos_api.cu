@@ -312,9 +312,11 @@ fos_status fos_quantize_batch(const fos_quant_job* jobs, int32_t n_jobs, const f
       }
       int grid = 0;
       if (fos::launch_amax_batch(b, rht, tr, total, &grid, stream) != cudaSuccess) return FOS_ERR_CUDA;
-      // the quantize launches of this group (each job's grid partial maxima);
-      // the next group's amax launch follows them as a plain launch
-      for (int32_t k = 0; k < b.n_jobs; ++k) {
+      // the quantize launches of this group (each job's grid partial maxima),
+      // last job first: the amax launch read the jobs in order, so the last
+      // one's input is the most likely to be still in L2; the next group's
+      // amax launch follows them as a plain launch
+      for (int32_t k = b.n_jobs - 1; k >= 0; --k) {
         const fos_quant_job& j = jobs[g0 + k];
         const fos::QuantLaunch q = fos::quant_launch(j.x, j.rows, j.cols, j.ld_x, opt, j.codes, j.ld_codes, j.sf,
                                            j.tensor_scale, j.choice, slot(g0 + k), grid);

@@ -817,6 +817,15 @@ def run_case(args) -> None:
         bq = fos.BatchQuantizer([x.shape for x in xs], device=dev)
         for _ in range(2):
             bq(xs)
+    elif args.case == "quant_cols_batch":
+        # the same weight set quantized transposed as one batch call: one amax
+        # launch for all seven, then one transposed quantize launch per matrix
+        mats = workloads.qwen3_8b_weights()
+        order = sorted(mats, key=lambda k: mats[k].size)
+        xs = [_to_dev(torch, mats[k], dev) for k in order]
+        bq = fos.BatchQuantizer([x.shape for x in xs], device=dev, transpose=True)
+        for _ in range(2):
+            bq(xs)
     elif args.case == "quant_rows_one_launch":
         # 12288 x 4096 bf16 (100.7 MB, the gate/up projection shape), no amax
         # supplied: the one-launch quantizer (amax pass, barrier, quantize pass)
