@@ -200,7 +200,8 @@ fos_status fos_quantize_batch_workspace_size(int32_t n_jobs, size_t* bytes);
  *   - opt->transpose or opt->block_2d: one launch takes the amax passes of up
  *     to 32 jobs (the tensor maxima of fos_tensor_amax: of the values, or of
  *     their RHT along the blocks' direction), then one quantize launch per
- *     job follows; more jobs repeat this per group of 32.
+ *     job follows, last job first (its input is the likeliest to be still in
+ *     L2); more jobs repeat this per group of 32.
  * The quantize launches use programmatic dependent launch: each may start
  * (its input copies, and in the chained form the next job's maxima) while its
  * predecessor finishes, and waits for it before reading the maxima it needs.
