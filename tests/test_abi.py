@@ -119,6 +119,25 @@ def test_batch_validation_rejects_without_launch(fos):
     assert fos.fos_quantize_batch([], fos.options(transpose=True), 0, 0, 0) == fos.FOS_OK
 
 
+def test_batch_quantizer_output_shapes_on_host(fos):
+    """BatchQuantizer sizes its outputs on the host (nothing launches): a
+    transposed job's codes, scales and choices are [cols, rows]-shaped, a row
+    job's [rows, cols]-shaped, each scale buffer fos_sf_bytes of that shape."""
+    for opts, swap in ((dict(), False), (dict(transpose=True), True), (dict(block_2d=True), False),
+                       (dict(transpose=True, sf_layout=fos.FOS_SF_ROWMAJOR), True)):
+        shapes = [(64, 256), (48, 80), (16, 4096)]
+        bq = fos.BatchQuantizer(shapes, device="cpu", with_choice=True, **opts)
+        assert bq.shapes == shapes
+        layout = opts.get("sf_layout", fos.FOS_SF_SWIZZLED_128x4)
+        for (rows, cols), o in zip(shapes, bq.outs):
+            R, C = (cols, rows) if swap else (rows, cols)
+            assert (o.rows, o.cols) == (R, C), opts
+            assert o.codes.shape[0] == R and o.codes.shape[1] >= C // 2 and o.codes.shape[1] % 16 == 0
+            assert o.sf.numel() == fos.fos_sf_bytes(R, C, layout)
+            assert tuple(o.choice.shape) == (R, C // 16)
+        assert bq.ws_bytes == fos.fos_quantize_batch_workspace_size(len(shapes))
+
+
 def test_gemm_validation(fos):
     INVALID = fos.FOS_ERR_INVALID_ARG
     fake = 1 << 20
